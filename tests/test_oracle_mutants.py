@@ -1,0 +1,43 @@
+"""Plant plausible mistakes in copies of oracle.c and check that the pin suite
+catches every one of them (the oracle is pinned to facts, not to itself)."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+# (name, original text, mutated text, replace every occurrence?)
+MUTANTS = [
+    ("rope sin sign", "r[i] = x1 * c - x2 * s;", "r[i] = x1 * c + x2 * s;", False),
+    ("rope frequency exponent", "pow(base, -2.0 * (double)i / (double)d)", "pow(base, -1.0 * (double)i / (double)d)", False),
+    ("rope partner index", "double x1 = r[i], x2 = r[i + half];", "double x1 = r[i], x2 = r[(i + 1) % d];", False),
+    ("gqa head map", "int g = h / G;", "int g = h % hkv;", False),
+    ("dropped scale", "s *= scale;", "s *= 1.0;", False),
+    ("strict causal mask", "kpos[j] > qp", "kpos[j] >= qp", True),
+    ("lse without max", "*lse = M + log(L);", "*lse = log(L);", False),
+    ("values replaced by keys", "const double *vr = vb + j * kstride;", "const double *vr = kb + j * kstride;", False),
+    ("merge weight vs max", "double w = exp(l - L);", "double w = exp(l - mx);", False),
+    ("decode query position", "ctx, ctx - 1, 1, d,", "ctx, ctx - 2, 1, d,", False),
+    ("page slot index", "(j % page)) * (int64_t)d;", "(j / page)) * (int64_t)d;", False),
+    ("bf16 ulp", "int q = e - 8;", "int q = e - 9;", False),
+]
+
+
+@pytest.mark.parametrize("name,old,new,every", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new, every):
+    text = open(SRC).read()
+    assert old in text, f"mutation site for '{name}' not found"
+    text = text.replace(old, new) if every else text.replace(old, new, 1)
+    src = tmp_path / "oracle_mutant.c"
+    src.write_text(text)
+    lib = tmp_path / "liboracle_mutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", str(src),
+                           "-o", str(lib), "-lm"])
+    env = dict(os.environ, ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant '{name}' survived the pin suite:\n{r.stdout[-2000:]}"

@@ -1,0 +1,408 @@
+"""Pins for the fp64 CPU oracle: each test checks it against something other than
+itself — a library routine, a different algorithm from the pages, a closed form,
+an invariant, or a hand-worked case — so that a dropped term, a wrong sign or
+index, or a transposed operand in oracle.c fails at least one of them."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+_ENV = {k: getattr(math, k) for k in ("log", "exp", "cos", "sin", "sqrt", "e", "pi", "inf")}
+
+
+def _ev(x):
+    if isinstance(x, list):
+        return [_ev(y) for y in x]
+    return float(eval(str(x).replace("-inf", "-inf_"), {"__builtins__": {}},
+                      dict(_ENV, inf_=math.inf)))
+
+
+def _rand(shape, seed, std=1.0):
+    return np.random.default_rng(seed).normal(0.0, std, size=shape)
+
+
+# ------------------------------------------------------------------ bf16 rounding
+
+def test_round_bf16_matches_torch_conversion():
+    """RNE to bf16 equals torch's float32 -> bfloat16 conversion (a library routine)
+    on random fp32 values, exact ties, subnormals and overflow."""
+    rng = np.random.default_rng(0)
+    x = np.concatenate([
+        rng.normal(0, 1, 20000), rng.normal(0, 1e-3, 2000), rng.normal(0, 1e30, 2000),
+        rng.uniform(-1e-38, 1e-38, 2000),
+    ]).astype(np.float32)
+    # exact ties: midpoints between neighbouring bf16 values are fp32 values
+    b = torch.from_numpy(rng.normal(0, 1, 4000).astype(np.float32)).to(torch.bfloat16)
+    lo = b.view(torch.int16).to(torch.int32)
+    nxt = (lo + 1).to(torch.int16).view(torch.bfloat16)
+    mid = ((b.to(torch.float64) + nxt.to(torch.float64)) / 2).to(torch.float32).numpy()
+    x = np.concatenate([x, mid, np.array([3.4e38, -3.4e38, 1.0 + 2**-8, 1.0 + 3 * 2**-8],
+                                         dtype=np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_bf16(x.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+# ------------------------------------------------------------------ RoPE
+
+def test_rope_position_zero_is_identity():
+    x = _rand((5, 3, 16), 1)
+    np.testing.assert_array_equal(oracle.rope(x, np.zeros(5, np.int32)), x)
+
+
+def test_rope_d2_is_plane_rotation_by_position():
+    """d = 2: theta_0 = base^0 = 1, so (1, 0) at position p becomes (cos p, sin p)."""
+    p = np.array([0, 1, 2, 7, 1000, 65535], np.int32)
+    x = np.zeros((len(p), 1, 2))
+    x[:, 0, 0] = 1.0
+    y = oracle.rope(x, p)
+    np.testing.assert_allclose(y[:, 0, 0], np.cos(p), atol=1e-12)
+    np.testing.assert_allclose(y[:, 0, 1], np.sin(p), atol=1e-12)
+
+
+def test_rope_equals_complex_multiplication():
+    """Half-split RoPE is z_i * exp(i p theta_i) with z_i = x_i + i x_{i+d/2}."""
+    T, H, d, base = 9, 2, 32, 10000.0
+    x = _rand((T, H, d), 2)
+    p = np.array([0, 1, 5, 17, 100, 4096, 8191, 65535, 131071], np.int32)
+    half = d // 2
+    theta = base ** (-(2.0 * np.arange(half)) / d)
+    z = (x[..., :half] + 1j * x[..., half:]) * np.exp(1j * p[:, None, None] * theta[None, None, :])
+    want = np.concatenate([z.real, z.imag], axis=-1)
+    np.testing.assert_allclose(oracle.rope(x, p, base), want, atol=1e-10, rtol=0)
+
+
+def test_rope_preserves_pair_norms():
+    x = _rand((7, 4, 64), 3)
+    p = np.arange(7, dtype=np.int32) * 1000
+    y = oracle.rope(x, p)
+    n0 = x[..., :32] ** 2 + x[..., 32:] ** 2
+    n1 = y[..., :32] ** 2 + y[..., 32:] ** 2
+    np.testing.assert_allclose(n1, n0, rtol=1e-12)
+
+
+def test_golden_rope():
+    for c in json.load(open(GOLDEN))["rope"]:
+        x = np.array(_ev(c["x"]))[None, None, :]
+        y = oracle.rope(x, np.array([c["pos"]], np.int32), c["base"])
+        np.testing.assert_allclose(y[0, 0], _ev(c["out"]), atol=1e-13)
+
+
+# ------------------------------------------------------------------ attention
+
+def _varlen_case(seed, lens_q, lens_k, q_start, hq, hkv, d, k_start=None):
+    rng = np.random.default_rng(seed)
+    B = len(lens_q)
+    k_start = [0] * B if k_start is None else k_start
+    q = rng.normal(0, 1, (sum(lens_q), hq, d))
+    k = rng.normal(0, 1, (sum(lens_k), hkv, d))
+    v = rng.normal(0, 1, (sum(lens_k), hkv, d))
+    q_seq = np.concatenate([np.full(n, b, np.int32) for b, n in enumerate(lens_q)])
+    q_pos = synth.positions(lens_q, q_start)
+    k_pos = synth.positions(lens_k, k_start)
+    cu_k = synth.cu_seqlens(lens_k)
+    return q, k, v, q_seq, q_pos, k_pos, cu_k
+
+
+def _torch_reference(q, k, v, q_seq, q_pos, k_pos, cu_k, scale, causal):
+    """torch SDPA (float64, CPU) with an explicit visibility mask; GQA by repeating
+    each KV head for its group of query heads."""
+    hq, hkv = q.shape[1], k.shape[1]
+    G = hq // hkv
+    out = np.zeros_like(q)
+    lse = np.zeros(q.shape[:2])
+    for b in range(len(cu_k) - 1):
+        rows = np.nonzero(q_seq == b)[0]
+        kr = slice(cu_k[b], cu_k[b + 1])
+        Q = torch.from_numpy(q[rows]).permute(1, 0, 2)                       # [hq, nq, d]
+        K = torch.from_numpy(k[kr]).permute(1, 0, 2).repeat_interleave(G, 0)  # [hq, nk, d]
+        V = torch.from_numpy(v[kr]).permute(1, 0, 2).repeat_interleave(G, 0)
+        vis = torch.ones(len(rows), K.shape[1], dtype=torch.bool)
+        if causal:
+            vis = torch.from_numpy(k_pos[kr][None, :] <= q_pos[rows][:, None])
+        O = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=vis, scale=scale)
+        S = (Q @ K.transpose(1, 2)) * scale
+        L = torch.logsumexp(S.masked_fill(~vis, -math.inf), dim=-1)
+        out[rows] = O.permute(1, 0, 2).numpy()
+        lse[rows] = L.permute(1, 0).numpy()
+    return out, lse
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 2), (8, 2), (6, 6), (4, 1)])
+def test_attention_matches_torch_sdpa(hq, hkv):
+    lens = [13, 40, 1]
+    q, k, v, q_seq, q_pos, k_pos, cu_k = _varlen_case(10 + hq, lens, lens, [0, 5, 1000], hq, hkv, 8,
+                                                      k_start=[0, 5, 1000])
+    scale = 0.37
+    o, l = oracle.attention(q, q_seq, q_pos, k, v, cu_k, k_pos, scale)
+    wo, wl = _torch_reference(q, k, v, q_seq, q_pos, k_pos, cu_k, scale, True)
+    np.testing.assert_allclose(o, wo, atol=1e-12, rtol=1e-10)
+    np.testing.assert_allclose(l, wl, atol=1e-12, rtol=1e-10)
+
+
+def test_attention_non_causal_and_chunk_offset_matches_torch():
+    """Queries of a chunk at positions 20..29 against 30 keys at 0..29 (the chunked
+    prefill shape), and the same without a mask."""
+    q, k, v, q_seq, q_pos, k_pos, cu_k = _varlen_case(5, [10], [30], [20], 4, 2, 16)
+    for causal in (True, False):
+        o, l = oracle.attention(q, q_seq, q_pos, k, v, cu_k, k_pos, 0.25, causal=causal)
+        wo, wl = _torch_reference(q, k, v, q_seq, q_pos, k_pos, cu_k, 0.25, causal)
+        np.testing.assert_allclose(o, wo, atol=1e-12)
+        np.testing.assert_allclose(l, wl, atol=1e-12)
+
+
+def _online_softmax(q, k, v, q_pos, k_pos, scale, block):
+    """The blockwise recurrence of the Flash Attention page, section 18.3: per K/V block,
+    m_new = max(m_old, rowmax S); O <- O e^{m_old - m_new} + e^{S - m_new} V;
+    l <- l e^{m_old - m_new} + sum e^{S - m_new}; finally O / l."""
+    nq, hq, d = q.shape
+    G = hq // k.shape[1]
+    out = np.zeros_like(q)
+    lse = np.zeros((nq, hq))
+    for h in range(hq):
+        Kh, Vh = k[:, h // G], v[:, h // G]
+        for r in range(nq):
+            m, l, O = -np.inf, 0.0, np.zeros(d)
+            for j0 in range(0, len(Kh), block):
+                Kb, Vb, pb = Kh[j0:j0 + block], Vh[j0:j0 + block], k_pos[j0:j0 + block]
+                s = (Kb @ q[r, h]) * scale
+                s = np.where(pb <= q_pos[r], s, -np.inf)
+                if np.all(s == -np.inf):
+                    continue
+                m_new = max(m, s.max())
+                a = math.exp(m - m_new) if m != -np.inf else 0.0
+                p = np.exp(s - m_new)
+                O = O * a + p @ Vb
+                l = l * a + p.sum()
+                m = m_new
+            out[r, h] = O / l
+            lse[r, h] = m + math.log(l)
+    return out, lse
+
+
+@pytest.mark.parametrize("block", [1, 7, 16, 64])
+def test_online_softmax_recurrence_equals_three_pass(block):
+    """The method's tiled recurrence gives the same result as the oracle's three
+    passes, as section 18.3 of the Flash Attention page states."""
+    q, k, v, q_seq, q_pos, k_pos, cu_k = _varlen_case(7, [70], [70], [0], 4, 2, 16)
+    o, l = oracle.attention(q, q_seq, q_pos, k, v, cu_k, k_pos, 0.3)
+    oo, ll = _online_softmax(q, k, v, q_pos, k_pos, 0.3, block)
+    np.testing.assert_allclose(o, oo, atol=1e-12)
+    np.testing.assert_allclose(l, ll, atol=1e-12)
+
+
+def test_uniform_scores_give_causal_prefix_mean():
+    """q = 0 makes every visible score 0: O_i = mean(V[0..i]), LSE_i = ln(i + 1)."""
+    S, hq, hkv, d = 50, 4, 2, 8
+    q = np.zeros((S, hq, d))
+    k = _rand((S, hkv, d), 11)
+    v = _rand((S, hkv, d), 12)
+    pos = np.arange(S, dtype=np.int32)
+    o, l = oracle.attention(q, np.zeros(S, np.int32), pos, k, v, [0, S], pos, 0.5)
+    G = hq // hkv
+    for h in range(hq):
+        want = np.cumsum(v[:, h // G], axis=0) / np.arange(1, S + 1)[:, None]
+        np.testing.assert_allclose(o[:, h], want, atol=1e-13)
+        np.testing.assert_allclose(l[:, h], np.log(np.arange(1, S + 1)), atol=1e-13)
+
+
+def test_causal_row_zero_is_v0():
+    """The first row sees only key 0: O_0 = V[0] exactly, LSE_0 = scale q0.k0."""
+    S, hq, hkv, d = 20, 8, 2, 16
+    q, k, v = _rand((S, hq, d), 21), _rand((S, hkv, d), 22), _rand((S, hkv, d), 23)
+    pos = np.arange(S, dtype=np.int32)
+    o, l = oracle.attention(q, np.zeros(S, np.int32), pos, k, v, [0, S], pos, 0.25)
+    for h in range(hq):
+        np.testing.assert_array_equal(o[0, h], v[0, h // 4])
+        assert abs(l[0, h] - 0.25 * float(q[0, h] @ k[0, h // 4])) < 1e-14
+
+
+def test_head_mapping_is_consecutive_groups():
+    """With K/V heads made distinguishable (head g's V is constant g), query head h
+    reads KV head h // (hq / hkv)."""
+    S, hq, hkv, d = 6, 8, 2, 4
+    q, k = _rand((S, hq, d), 31), _rand((S, hkv, d), 32)
+    v = np.zeros((S, hkv, d))
+    v[:, 1] = 1.0
+    pos = np.arange(S, dtype=np.int32)
+    o, _ = oracle.attention(q, np.zeros(S, np.int32), pos, k, v, [0, S], pos, 0.5)
+    np.testing.assert_allclose(o[:, :4], 0.0, atol=0)
+    np.testing.assert_allclose(o[:, 4:], 1.0, atol=1e-14)
+
+
+def test_fully_masked_row_is_zero_with_minus_inf_lse():
+    q, k, v, q_seq, q_pos, k_pos, cu_k = _varlen_case(41, [3], [5], [0], 2, 1, 4, k_start=[10])
+    o, l = oracle.attention(q, q_seq, q_pos, k, v, cu_k, k_pos, 1.0)
+    assert np.all(o == 0.0) and np.all(l == -np.inf)
+
+
+def test_rope_shift_invariance_of_attention():
+    """RoPE scores depend on position differences only: adding the same offset to every
+    query and key position leaves O and LSE unchanged (Ulysses page, 3.5, second check)."""
+    S, hq, hkv, d = 40, 4, 2, 32
+    q, k, v = _rand((S, hq, d), 51), _rand((S, hkv, d), 52), _rand((S, hkv, d), 53)
+    pos = np.arange(S, dtype=np.int32)
+    res = []
+    for shift in (0, 1000, 57344):
+        p = pos + shift
+        res.append(oracle.attention(oracle.rope(q, p), np.zeros(S, np.int32), p,
+                                    oracle.rope(k, p), v, [0, S], p, d ** -0.5))
+    for o, l in res[1:]:
+        np.testing.assert_allclose(o, res[0][0], atol=1e-11)
+        np.testing.assert_allclose(l, res[0][1], atol=1e-11)
+
+
+def test_head_slices_concatenate_to_full_call():
+    """Ulysses page, 2.2: four shards of 16 tokens and 8 heads; after the all-to-all
+    each rank computes 2 heads over all 64 tokens.  Those slices put together equal
+    the all-heads result bit for bit."""
+    g = json.load(open(GOLDEN))["ulysses_head_shards"]
+    S = g["sp"] * g["tokens_per_shard"]
+    H = g["heads"]
+    q, k, v = _rand((S, H, 16), 61), _rand((S, H, 16), 62), _rand((S, H, 16), 63)
+    pos = np.arange(S, dtype=np.int32)
+    seq = np.zeros(S, np.int32)
+    full_o, full_l = oracle.attention(q, seq, pos, k, v, [0, S], pos, 0.25)
+    cat_o = np.full_like(full_o, np.nan)
+    cat_l = np.full_like(full_l, np.nan)
+    for heads in g["heads_of_rank"]:
+        o, l = oracle.attention(q, seq, pos, k, v, [0, S], pos, 0.25, h_lo=heads[0], h_hi=heads[-1] + 1)
+        cat_o[:, heads] = o[:, heads]
+        cat_l[:, heads] = l[:, heads]
+    np.testing.assert_array_equal(cat_o, full_o)
+    np.testing.assert_array_equal(cat_l, full_l)
+
+
+# ------------------------------------------------------------------ merge
+
+def _key_partitions(n, parts):
+    idx = np.arange(n)
+    contiguous = np.array_split(idx, parts)
+    striped = [idx[r::parts] for r in range(parts)]
+    # zigzag: 2*parts blocks, part r takes blocks r and 2*parts-1-r
+    blocks = np.array_split(idx, 2 * parts)
+    zigzag = [np.concatenate([blocks[r], blocks[2 * parts - 1 - r]]) for r in range(parts)]
+    return {"contiguous": contiguous, "striped": striped, "zigzag": zigzag}
+
+
+@pytest.mark.parametrize("kind", ["contiguous", "striped", "zigzag"])
+def test_merge_of_key_partitions_equals_unsplit(kind):
+    """Attention over disjoint key sets, merged through the LSE, equals attention over
+    all keys (the ring / striped / zigzag splits of the SGLang page, section 3.5)."""
+    S, hq, hkv, d, parts = 64, 4, 2, 16, 4
+    q, k, v = _rand((S, hq, d), 71), _rand((S, hkv, d), 72), _rand((S, hkv, d), 73)
+    pos = np.arange(S, dtype=np.int32)
+    seq = np.zeros(S, np.int32)
+    full_o, full_l = oracle.attention(q, seq, pos, k, v, [0, S], pos, 0.25)
+    po, pl = [], []
+    for ids in _key_partitions(S, parts)[kind]:
+        o, l = oracle.attention(q, seq, pos, k[ids], v[ids], [0, len(ids)], pos[ids], 0.25)
+        po.append(o)
+        pl.append(l)
+    mo, ml = oracle.lse_merge(np.stack(po), np.stack(pl))
+    np.testing.assert_allclose(mo, full_o, atol=1e-12)
+    np.testing.assert_allclose(ml, full_l, atol=1e-12)
+
+
+def test_golden_merge():
+    for c in json.load(open(GOLDEN))["merge"]:
+        o = np.array(_ev(c["o"]))[:, None, :]
+        l = np.array(_ev(c["lse"]))[:, None]
+        mo, ml = oracle.lse_merge(o, l)
+        np.testing.assert_allclose(mo[0], _ev(c["out"]), atol=1e-14)
+        assert abs(ml[0] - _ev(c["out_lse"])) < 1e-14
+
+
+def test_merge_all_empty_parts():
+    o = np.ones((3, 2, 4))
+    l = np.full((3, 2), -np.inf)
+    mo, ml = oracle.lse_merge(o, l)
+    assert np.all(mo == 0.0) and np.all(ml == -np.inf)
+
+
+def test_golden_attention():
+    for c in json.load(open(GOLDEN))["attention"]:
+        q = np.array(_ev(c["q"]))[:, None, :]
+        k = np.array(_ev(c["k"]))[:, None, :]
+        v = np.array(_ev(c["v"]))[:, None, :]
+        qp = np.array(c["q_pos"], np.int32)
+        kp = np.array(c["k_pos"], np.int32)
+        qr, kr = oracle.rope(q, qp, c["base"]), oracle.rope(k, kp, c["base"])
+        o, l = oracle.attention(qr, np.zeros(len(qp), np.int32), qp, kr, v, [0, len(kp)], kp,
+                                c["scale"])
+        np.testing.assert_allclose(o[:, 0], _ev(c["out"]), atol=1e-14)
+        np.testing.assert_allclose(l[:, 0], _ev(c["lse"]), atol=1e-14)
+
+
+# ------------------------------------------------------------------ paged decode
+
+def _decode_case(seed, ctx, hq=8, hkv=2, d=16, page=4):
+    table, num_pages = synth.shuffled_page_table(ctx, seed, page=page)
+    rng = np.random.default_rng(seed)
+    kc = rng.normal(0, 1, (hkv, num_pages, page, d))
+    vc = rng.normal(0, 1, (hkv, num_pages, page, d))
+    q = rng.normal(0, 1, (len(ctx), hq, d))
+    return q, kc, vc, table, num_pages
+
+
+def test_gather_pages_bit_exact():
+    ctx = [9, 1, 16, 5]
+    q, kc, vc, table, num_pages = _decode_case(81, ctx)
+    for b, c in enumerate(ctx):
+        for g in range(kc.shape[0]):
+            want = np.stack([kc[g, table[b, j // 4], j % 4] for j in range(c)])
+            np.testing.assert_array_equal(oracle.gather_pages(kc, table, num_pages, g, b, c), want)
+
+
+def test_gather_rejects_bad_page_id():
+    q, kc, vc, table, num_pages = _decode_case(82, [8])
+    table = table.copy()
+    table[0, 1] = num_pages
+    with pytest.raises(ValueError):
+        oracle.gather_pages(kc, table, num_pages, 0, 0, 8)
+
+
+def test_decode_equals_attention_over_gathered_keys():
+    """Decode at position ctx-1 over the paged cache equals causal attention of that
+    one query over the keys gathered (here by numpy indexing) in logical order."""
+    ctx = [7, 12, 1, 30]
+    q, kc, vc, table, num_pages = _decode_case(83, ctx)
+    o, l = oracle.decode_paged(q, kc, vc, table, ctx, num_pages, 0.25)
+    hkv = kc.shape[0]
+    for b, c in enumerate(ctx):
+        j = np.arange(c)
+        K = kc[:, table[b, j // 4], j % 4].transpose(1, 0, 2)  # [c, hkv, d]
+        V = vc[:, table[b, j // 4], j % 4].transpose(1, 0, 2)
+        wo, wl = oracle.attention(q[b:b + 1], np.zeros(1, np.int32), np.array([c - 1], np.int32),
+                                  K, V, [0, c], j.astype(np.int32), 0.25)
+        np.testing.assert_array_equal(o[b], wo[0])
+        np.testing.assert_array_equal(l[b], wl[0])
+        wo2, wl2 = _torch_reference(q[b:b + 1], K, V, np.zeros(1, np.int32),
+                                    np.array([c - 1], np.int32), j.astype(np.int32), [0, c], 0.25, True)
+        np.testing.assert_allclose(o[b], wo2[0], atol=1e-12)
+
+
+def test_decode_invariant_under_page_permutation_and_request_order():
+    """Moving pages to other physical slots, or reordering requests, changes no output
+    bit (Ulysses page, 3.5, third check: reuse of the cache with a permuted batch)."""
+    ctx = [7, 12, 5, 30]
+    q, kc, vc, table, num_pages = _decode_case(84, ctx)
+    o, l = oracle.decode_paged(q, kc, vc, table, ctx, num_pages, 0.25)
+    perm = np.random.default_rng(1).permutation(num_pages)
+    inv = np.argsort(perm)
+    kc2, vc2 = kc[:, perm], vc[:, perm]
+    table2 = np.where(table >= 0, inv[np.maximum(table, 0)], -1).astype(np.int32)
+    o2, l2 = oracle.decode_paged(q, kc2, vc2, table2, ctx, num_pages, 0.25)
+    np.testing.assert_array_equal(o2, o)
+    np.testing.assert_array_equal(l2, l)
+    order = np.array([2, 0, 3, 1])
+    o3, l3 = oracle.decode_paged(q[order], kc, vc, table[order], np.array(ctx)[order], num_pages, 0.25)
+    np.testing.assert_array_equal(o3, o[order])
+    np.testing.assert_array_equal(l3, l[order])
