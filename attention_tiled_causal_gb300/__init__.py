@@ -1,0 +1,21 @@
+"""GB300 (sm_103a) exact causal GQA attention: Python binding of libattn_gb300.so.
+
+The binding only marshals arguments: it checks tensor dtypes, devices and
+layouts, passes raw device pointers and the current CUDA stream to the C ABI
+declared in include/attn_gb300.h, and raises on a non-zero status.  Every step
+of the computation runs in the library's CUDA kernels; there is no fallback.
+PyTorch provides device memory and streams.
+
+Entry points (same names as the C ABI):
+    rope_apply(x, positions, base)                      RoPE at absolute positions, in place
+    attn_prefill(q, k, v, out, lse, cu_q, q_pos, ...)   tiled causal GQA attention
+    attn_decode_paged(q, k_cache, v_cache, ...)         split-KV decode over a paged cache
+    attn_lse_merge(part_out, part_lse, out, lse, ...)   log-sum-exp merge of partials
+"""
+from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_device_status,
+                       attn_lse_merge, attn_prefill, decode_workspace, lib_path, library, prefill,
+                       rope_apply)
+
+__all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_device_status",
+           "attn_lse_merge", "attn_prefill", "decode_workspace", "lib_path", "library", "prefill",
+           "rope_apply"]

@@ -1,0 +1,196 @@
+"""ctypes marshalling for libattn_gb300.so (see include/attn_gb300.h for the contracts)."""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libattn_gb300.so")
+
+ATTN_BF16 = 0
+ATTN_FP32 = 1
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"status {status}: {msg}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def library():
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                          f"g.build()\"` (nvcc, sm_103a)")
+    lib = C.CDLL(_LIB_PATH)
+    P, I32, I64, F32, F64 = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_double
+    lib.attn_last_error.restype = C.c_char_p
+    lib.attn_device_status.argtypes = [I32]
+    lib.attn_device_status.restype = I32
+    lib.rope_apply.argtypes = [P, I32, I64, I32, I32, I64, P, F64, P]
+    lib.rope_apply.restype = I32
+    lib.attn_prefill.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, I64, I32, P, P, I64, P, P, I32, I32, I64,
+                                 I32, I32, I32, I32, I32, F32, I32, P]
+    lib.attn_prefill.restype = I32
+    lib.attn_decode_paged.argtypes = [P, P, P, P, P, I32, I32, I32, I64, I32, I32, I32, I32, F32, P, P, P, I32,
+                                      P, P]
+    lib.attn_decode_paged.restype = I32
+    lib.attn_lse_merge.argtypes = [P, P, I32, I64, I32, I32, I64, I64, I64, I64, I64, I64, P, I32, P, P]
+    lib.attn_lse_merge.restype = I32
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise AttnError(status, library().attn_last_error().decode())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the library must live on a CUDA device")
+    return t.data_ptr()
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_FP32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _i32(t: Optional[torch.Tensor], name: str) -> Optional[torch.Tensor]:
+    if t is None:
+        return None
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 tensor")
+    return t
+
+
+def attn_device_status(clear: bool = True) -> None:
+    """Synchronise and raise if a kernel recorded a device-side fault."""
+    _check(library().attn_device_status(1 if clear else 0))
+
+
+def rope_apply(x: torch.Tensor, positions: torch.Tensor, base: float = 10000.0, stream=None) -> torch.Tensor:
+    """Rotate x [tokens, heads, head_dim] in place at absolute `positions` [tokens]."""
+    if x.dim() != 3 or x.stride(2) != 1 or x.stride(1) != x.shape[2]:
+        raise ValueError("x must be [tokens, heads, head_dim] with heads and head_dim packed")
+    positions = _i32(positions, "positions")
+    if positions.numel() != x.shape[0]:
+        raise ValueError("positions must hold one entry per token")
+    _check(library().rope_apply(_ptr(x), _dt(x), x.shape[0], x.shape[1], x.shape[2], x.stride(0),
+                                _ptr(positions), float(base), _stream(stream)))
+    return x
+
+
+def attn_prefill(q, k, v, out, lse, cu_q, q_pos, max_seqlen_q: int, *, cu_k=None, k_pos=None,
+                 page_table=None, k_lens=None, num_pages: int = 0, h_lo: int = 0,
+                 h_hi: Optional[int] = None, scale: Optional[float] = None, causal: bool = True,
+                 stream=None) -> None:
+    """Tiled causal GQA attention.  q [Tq, Hq, d]; contiguous k/v [Tk, Hkv, d] with
+    cu_k/k_pos, or head-major paged caches [Hkv, num_pages, page, d] with
+    page_table [B, max_pages] and k_lens [B].  Writes out [Tq, Hq, d] and lse [Tq, Hq]
+    (if given) for query heads [h_lo, h_hi)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    Tq, hq, d = q.shape
+    paged = page_table is not None
+    if paged:
+        hkv, npg, page, dk = k.shape
+        max_pages = page_table.shape[1]
+        num_pages = num_pages or npg
+        total_k = 0
+    else:
+        Tk, hkv, dk = k.shape
+        page, max_pages, total_k = 0, 0, Tk
+    if dk != d or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("inconsistent q/k/v/out shapes")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (Tq, hq) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 [Tq, Hq] tensor")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k and v must share a dtype")
+    h_hi = hq if h_hi is None else h_hi
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    cu_q = _i32(cu_q, "cu_q")
+    B = cu_q.numel() - 1
+    _check(library().attn_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _dt(out), _ptr(lse), _dt(q), B, _ptr(cu_q),
+        _ptr(_i32(q_pos, "q_pos")), Tq, int(max_seqlen_q), _ptr(_i32(cu_k, "cu_k")),
+        _ptr(_i32(k_pos, "k_pos")), total_k, _ptr(_i32(page_table, "page_table")),
+        _ptr(_i32(k_lens, "k_lens")), max_pages, page, int(num_pages), hq, hkv, d, int(h_lo),
+        int(h_hi), float(scale), 1 if causal else 0, _stream(stream)))
+
+
+def prefill(q, k, v, cu_q, q_pos, max_seqlen_q: int, out_dtype=None, with_lse: bool = True, **kw):
+    """attn_prefill with freshly allocated out (dtype of q unless given) and lse."""
+    out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device) if with_lse else None
+    attn_prefill(q, k, v, out, lse, cu_q, q_pos, max_seqlen_q, **kw)
+    return out, lse
+
+
+def decode_workspace(batch: int, num_q_heads: int, num_splits: int, head_dim: int, device):
+    """Partial-output workspaces for attn_decode_paged."""
+    return (torch.empty((batch, num_q_heads, num_splits, head_dim), dtype=torch.float32, device=device),
+            torch.empty((batch, num_q_heads, num_splits), dtype=torch.float32, device=device))
+
+
+def attn_decode_paged(q, k_cache, v_cache, page_table, ctx_lens, num_splits: int, part_out, part_lse,
+                      out=None, lse=None, scale: Optional[float] = None, stream=None) -> None:
+    """Split-KV decode.  q [B, Hq, d] bf16 (rotated); caches [Hkv, num_pages, page, d] bf16;
+    page_table [B, max_pages]; ctx_lens [B]; partial workspaces from decode_workspace()."""
+    B, hq, d = q.shape
+    hkv, npg, page, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent cache shapes")
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (part_out, "part_out"),
+                 (part_lse, "part_lse")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if tuple(part_out.shape) != (B, hq, num_splits, d) or tuple(part_lse.shape) != (B, hq, num_splits):
+        raise ValueError("workspace shapes must be [B, Hq, splits, d] and [B, Hq, splits]")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    page_table = _i32(page_table, "page_table")
+    _check(library().attn_decode_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(_i32(ctx_lens, "ctx_lens")), B,
+        page_table.shape[1], page, npg, hq, hkv, d, int(num_splits), float(scale), _ptr(part_out),
+        _ptr(part_lse), _ptr(out), _dt(out) if out is not None else 0, _ptr(lse), _stream(stream)))
+
+
+def attn_lse_merge(part_out, part_lse, out, lse=None, stream=None) -> None:
+    """Merge partials part_out [P, rows, H, d] / part_lse [P, rows, H] (any strides, fp32)
+    into out [rows, H, d] and lse [rows, H]."""
+    P, rows, H, d = part_out.shape
+    if tuple(part_lse.shape) != (P, rows, H) or part_out.stride(3) != 1:
+        raise ValueError("part_lse must be [P, rows, H] and part_out's last dim contiguous")
+    if part_out.dtype != torch.float32 or part_lse.dtype != torch.float32:
+        raise ValueError("partials must be float32")
+    if not out.is_contiguous() or tuple(out.shape) != (rows, H, d):
+        raise ValueError("out must be a contiguous [rows, H, d] tensor")
+    so, sl = part_out.stride(), part_lse.stride()
+    _check(library().attn_lse_merge(_ptr(part_out), _ptr(part_lse), P, rows, H, d, so[0], so[1], so[2], sl[0],
+                                    sl[1], sl[2], _ptr(out), _dt(out), _ptr(lse), _stream(stream)))

@@ -1,0 +1,73 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+struct RopeLaunch {
+  void* x;
+  int dtype;  // 0 bf16, 1 fp32
+  int64_t tokens;
+  int heads, head_dim;
+  int64_t stride_token;
+  const int32_t* positions;
+  double base;
+};
+cudaError_t launch_rope(const RopeLaunch& a, cudaStream_t s);
+
+struct MergeLaunch {
+  const float* part_out;
+  const float* part_lse;
+  int n_parts;
+  int64_t rows;
+  int heads, head_dim;
+  int64_t osp, osr, osh, lsp, lsr, lsh;
+  void* out;
+  int out_f32;
+  float* lse_out;
+};
+cudaError_t launch_lse_merge(const MergeLaunch& a, cudaStream_t s);
+
+struct PrefillLaunch {
+  const void *q, *k, *v;
+  void* out;
+  int out_f32;
+  float* lse;
+  int in_f32;
+  int batch;
+  const int32_t *cu_q, *q_pos;
+  int max_seqlen_q;
+  const int32_t *cu_k, *k_pos;
+  const int32_t *page_table, *k_lens;
+  int max_pages, page_size;
+  int64_t num_pages;
+  int hq, hkv, d, h_lo, h_hi;
+  float scale;
+  int causal;
+  unsigned* err;
+};
+// CUDA-core kernel: any supported dtype / head_dim / page size.
+cudaError_t launch_prefill_simt(const PrefillLaunch& a, cudaStream_t s);
+// tcgen05 tensor-core kernel: bf16, head_dim 128, page size 64 when paged.
+// The tensor maps are built by the caller.
+cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t s);
+
+struct DecodeLaunch {
+  const void* q;
+  const int32_t *page_table, *ctx_lens;
+  int batch, max_pages;
+  int64_t num_pages;
+  int hq, hkv, num_splits;
+  float scale;
+  float *part_out, *part_lse;
+  unsigned* err;
+};
+cudaError_t launch_decode_split(const DecodeLaunch& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                cudaStream_t s);
+
+}  // namespace attn

@@ -1,0 +1,460 @@
+// Causal GQA prefill on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// The method is the tiled attention of the Flash Attention page: scores of one
+// query tile against one K/V tile (section 18.3, step 1), the running max m and
+// denominator l updated per tile with the old output rescaled by
+// exp(m_old - m_new) (steps 2-6), the query tile as the outer loop and the
+// division by l deferred to the end (section 18.4), and TMA loads overlapped
+// with compute by warp specialisation (section 18.5).  What is GB300-specific:
+//
+//  * One CTA owns TWO 128-row query tiles (A and B) of one query head and
+//    streams the K/V tiles of that head's KV group once for both.
+//  * Warp 8 (one thread) is the TMA producer: Q tiles once, then K_j and V_j
+//    tiles (128 tokens x 128 dims, two 128-byte-swizzled boxes each) into a
+//    3-slot shared-memory ring, each slot guarded by full/empty mbarriers.
+//  * Warp 9 (one thread) issues tcgen05.mma: S_t = Q_t K_j^T into TMEM
+//    (M = 128, N = 128, K = 16 per instruction, bf16 in, fp32 accumulate),
+//    then O_t += P_t V_j into a second TMEM accumulator.  tcgen05.commit
+//    arrives on mbarriers when the tensor core is done.
+//  * Warps 0-3 (tile A) and 4-7 (tile B) are the softmax warpgroups: thread r
+//    of a warpgroup owns query row r (TMEM lane r), loads its 128 scores with
+//    tcgen05.ld, applies the absolute-position causal mask (Ulysses page,
+//    section 5.3), updates m and l, writes P = exp(S - m) as bf16 into shared
+//    memory in the swizzled K-major layout the MMA reads, and rescales its O
+//    row in TMEM when m grows.  While one warpgroup works on its softmax the
+//    tensor core runs the other tile's MMAs.
+//  * The rescale is thresholded: m only moves (and O is only rescaled) when
+//    some row of the warp would grow by more than 2^8 in exp2 units; P then
+//    stays <= 256, and the final O / l is exact whatever reference max was
+//    used, because numerator and denominator share it.
+//  * TMEM: 512 columns = S_A | S_B | O_A | O_B, 128 fp32 columns each.
+//
+// Every mbarrier wait is bounded; on expiry the kernel records an error code,
+// unwinds, frees its TMEM and returns (no trap).
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace attn {
+namespace tc {
+
+constexpr int BM = 128, BN = 128, D = 128;
+constexpr int NSLOT = 3;
+constexpr int TILE = BM * D * 2;  // 32 KB: one Q, K, V or P tile
+constexpr int HALF = TILE / 2;    // 16 KB: 128 rows x 64 elements (one swizzled box)
+constexpr int OFF_Q = 0;
+constexpr int OFF_KV = OFF_Q + 2 * TILE;
+constexpr int OFF_P = OFF_KV + NSLOT * TILE;
+constexpr int OFF_BAR = OFF_P + 2 * TILE;
+constexpr int NBAR = 16;
+constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 32 + 1024;
+constexpr int NTHREADS = 320;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);    // P K-major, V MN-major
+constexpr float kRescaleLog2 = 8.f;
+
+struct Smem {
+  uint64_t* q_full;    // [2]  TMA -> MMA: Q tile landed
+  uint64_t* kv_full;   // [3]  TMA -> MMA: ring slot landed
+  uint64_t* kv_empty;  // [3]  MMA -> TMA: ring slot consumed
+  uint64_t* s_full;    // [2]  MMA -> softmax: S_t ready in TMEM
+  uint64_t* s_free;    // [2]  softmax -> MMA: S_t read out (128 arrivals)
+  uint64_t* p_full;    // [2]  softmax -> MMA: P_t written, O_t rescaled (128 arrivals)
+  uint64_t* o_done;    // [2]  MMA -> softmax: O_t += P_t V_j finished
+  uint32_t* tmem_slot;
+  int* nkv;            // [2]  K/V tiles each query tile needs
+};
+
+struct Params {
+  const int32_t *cu_q, *q_pos, *cu_k, *k_pos, *page_table, *k_lens;
+  void* out;
+  float* lse;
+  unsigned* err;
+  int64_t num_pages;
+  int max_pages, hq, hkv, h_lo, causal, out_f32;
+  float scale;
+};
+
+// Number of keys with position <= qp among k_pos[0..n), positions non-decreasing.
+__device__ int upper_bound_pos(const int32_t* k_pos, int n, int qp) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (k_pos[mid] <= qp)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+template <bool PAGED>
+__global__ void __maxnreg__(200)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Work item: query head h, pair of 128-row query tiles (longest first), sequence b.
+  const int h = p.h_lo + blockIdx.x;
+  const int pair = gridDim.y - 1 - blockIdx.y;
+  const int b = blockIdx.z;
+  const int q_beg = p.cu_q[b];
+  const int Sq = p.cu_q[b + 1] - q_beg;
+  const int q0 = pair * 2 * BM;
+  if (q0 >= Sq) return;  // the whole CTA leaves together
+  const int g = h / (p.hq / p.hkv);
+  int k_beg = 0, Sk;
+  if (PAGED) {
+    Sk = p.k_lens[b];
+  } else {
+    k_beg = p.cu_k[b];
+    Sk = p.cu_k[b + 1] - k_beg;
+  }
+
+  Smem sm;
+  uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
+  sm.q_full = bars;
+  sm.kv_full = bars + 2;
+  sm.kv_empty = bars + 5;
+  sm.s_full = bars + 8;
+  sm.s_free = bars + 10;
+  sm.p_full = bars + 12;
+  sm.o_done = bars + 14;
+  sm.tmem_slot = (uint32_t*)(bars + NBAR);
+  sm.nkv = (int*)(sm.tmem_slot + 4);
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.q_full[t], 1);
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.s_free[t], 128);
+      mbar_init(&sm.p_full[t], 128);
+      mbar_init(&sm.o_done[t], 1);
+    }
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(&sm.kv_full[i], 1);
+      mbar_init(&sm.kv_empty[i], 1);
+    }
+    fence_mbar_init();
+    // K/V tiles needed by each query tile: keys up to the tile's last position.
+    for (int t = 0; t < 2; ++t) {
+      const int r0 = q0 + t * BM;
+      int nk = 0;
+      if (r0 < Sq) {
+        if (!p.causal) {
+          nk = Sk;
+        } else {
+          const int qp_last = p.q_pos[q_beg + min(r0 + BM, Sq) - 1];
+          nk = PAGED ? max(0, min(Sk, qp_last + 1)) : upper_bound_pos(p.k_pos + k_beg, Sk, qp_last);
+        }
+      }
+      sm.nkv[t] = (nk + BN - 1) / BN;
+    }
+  }
+  if (warp == WARP_MMA) tmem_alloc(sm.tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_slot;
+  const int nkv_a = sm.nkv[0], nkv_b = sm.nkv[1];
+  const int nkv = max(nkv_a, nkv_b);
+
+  if (warp == WARP_TMA) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nkv > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int t = 0; t < 2; ++t) {
+        if (sm.nkv[t] == 0) continue;
+        mbar_arrive_expect_tx(&sm.q_full[t], TILE);
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(smem + OFF_Q + t * TILE + hf * HALF, &tm_q, &sm.q_full[t], hf * 64, h, q_beg + q0 + t * BM);
+      }
+      const int32_t* table = PAGED ? p.page_table + (int64_t)b * p.max_pages : nullptr;
+      int issued = 0;
+      for (int i = 0; i < 2 * nkv; ++i) {
+        const int j = i >> 1, slot = i % NSLOT;
+        if (i >= NSLOT && !mbar_wait(&sm.kv_empty[slot], ((i / NSLOT) - 1) & 1, p.err, DEV_TIMEOUT_TMA)) break;
+        const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
+        uint8_t* dst = smem + OFF_KV + slot * TILE;
+        mbar_arrive_expect_tx(&sm.kv_full[slot], TILE);
+        if (!PAGED) {
+          for (int hf = 0; hf < 2; ++hf) tma_load_3d(dst + hf * HALF, tm, &sm.kv_full[slot], hf * 64, g, k_beg + j * BN);
+        } else {
+          for (int pp = 0; pp < 2; ++pp) {  // two 64-token pages per tile
+            const int lp = j * 2 + pp;
+            int pid = lp < p.max_pages ? table[lp] : -1;
+            if (pid < 0 || pid >= p.num_pages) {
+              if (lp * 64 < Sk) record_error(p.err, DEV_BAD_PAGE);
+              pid = 0;  // tokens past Sk are masked; keep the byte count whole
+            }
+            const int row0 = (int)(((int64_t)g * p.num_pages + pid) * 64);
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_2d(dst + hf * HALF + pp * (HALF / 2), tm, &sm.kv_full[slot], hf * 64, row0);
+          }
+        }
+        issued = i + 1;
+      }
+      // Leave no copy in flight: wait (bounded) for the last slots issued.
+      for (int i = max(0, issued - NSLOT); i < issued; ++i)
+        mbar_wait(&sm.kv_full[i % NSLOT], (i / NSLOT) & 1, nullptr, 0);
+    }
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nkv > 0) {
+      bool ok = true;
+      for (int t = 0; t < 2 && ok; ++t)
+        if (sm.nkv[t] > 0) ok = mbar_wait(&sm.q_full[t], 0, p.err, DEV_TIMEOUT_MMA);
+      tc_fence_after();
+      const uint32_t sQ = smem_u32(smem + OFF_Q), sKV = smem_u32(smem + OFF_KV), sP = smem_u32(smem + OFF_P);
+      for (int j = 0; j < nkv && ok; ++j) {
+        // S_t = Q_t K_j^T
+        const int iK = 2 * j, slotK = iK % NSLOT;
+        if (!(ok = mbar_wait(&sm.kv_full[slotK], (iK / NSLOT) & 1, p.err, DEV_TIMEOUT_MMA))) break;
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if (j >= sm.nkv[t]) continue;
+          if (j > 0) {
+            if (!(ok = mbar_wait(&sm.s_free[t], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA))) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t a = sQ + t * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
+            const uint32_t bb = sKV + slotK * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
+            tc_mma_bf16(tmem + t * BN, sdesc_sw128(a, 16, 1024), sdesc_sw128(bb, 16, 1024), IDESC_QK, kk > 0);
+          }
+          tc_commit(&sm.s_full[t]);
+        }
+        if (!ok) break;
+        tc_commit(&sm.kv_empty[slotK]);
+        // O_t += P_t V_j
+        const int iV = 2 * j + 1, slotV = iV % NSLOT;
+        if (!(ok = mbar_wait(&sm.kv_full[slotV], (iV / NSLOT) & 1, p.err, DEV_TIMEOUT_MMA))) break;
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if (j >= sm.nkv[t]) continue;
+          if (!(ok = mbar_wait(&sm.p_full[t], j & 1, p.err, DEV_TIMEOUT_MMA))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint32_t a = sP + t * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
+            const uint32_t bb = sKV + slotV * TILE + kk * 2048;  // 16 tokens = two 8-row swizzle atoms
+            tc_mma_bf16(tmem + 2 * BN + t * D, sdesc_sw128(a, 16, 1024), sdesc_sw128(bb, HALF, 1024), IDESC_PV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&sm.o_done[t]);
+        }
+        if (!ok) break;
+        tc_commit(&sm.kv_empty[slotV]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2, wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int rq = q0 + t * BM + row;  // row index inside the sequence
+    const bool rv = rq < Sq;
+    const int qp = rv ? p.q_pos[q_beg + rq] : 0;
+    const int nkv_t = sm.nkv[t];
+    const float sl2 = p.scale * 1.4426950408889634f;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * BN;
+    const uint32_t tO = tmem + lane_base + 2 * BN + t * D;
+    uint8_t* sP = smem + OFF_P + t * TILE;
+    uint8_t* prow = sP + (row >> 3) * 1024 + (row & 7) * 128;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < nkv_t; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, p.err, DEV_TIMEOUT_SOFTMAX));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&sm.s_free[t]);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      // causal mask by absolute position; keys past the sequence; rows past it
+      const int key0 = j * BN;
+      bool need_mask = !rv || key0 + BN > Sk;
+      if (!need_mask && p.causal) {
+        const int last_kp = PAGED ? key0 + BN - 1 : __ldg(p.k_pos + k_beg + key0 + BN - 1);
+        need_mask = last_kp > qp;
+      }
+      if (need_mask) {
+        if (PAGED) {  // cached token j sits at position j: one bound per row
+          const int lim = !rv ? -1 : (p.causal ? min(qp, Sk - 1) : Sk - 1) - key0;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > lim) s[c] = -INFINITY;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int kj = key0 + c;
+            bool vis = rv && kj < Sk;
+            if (vis && p.causal) vis = __ldg(p.k_pos + k_beg + kj) <= qp;
+            if (!vis) s[c] = -INFINITY;
+          }
+        }
+      }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) mt = fmaxf(mt, s[c]);
+      const float m_new = fmaxf(m_ref, mt);
+      const bool grow = (m_new - m_ref) * sl2 > kRescaleLog2;  // false when both are -inf
+      const bool any_grow = __any_sync(0xffffffffu, grow);
+      float alpha = 1.f;
+      if (any_grow && m_new > m_ref) {
+        alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2((m_ref - m_new) * sl2);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float pv = fast_exp2(fmaf(s[c], sl2, -mb));
+        s[c] = pv;
+        rs += pv;
+      }
+      l += rs;
+
+      // P_t and O_t are free once the previous O_t += P_t V_{j-1} finished.
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], (j - 1) & 1, p.err, DEV_TIMEOUT_SOFTMAX));
+        if (!ok) break;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 16; ++c8) {
+        uint4 v;
+        v.x = pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
+        v.y = pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
+        v.z = pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
+        v.w = pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
+        *reinterpret_cast<uint4*>(prow + (c8 >> 3) * HALF + (((c8 & 7) ^ (row & 7)) << 4)) = v;
+      }
+      if (any_grow && j > 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[t]);
+    }
+
+    // epilogue: O / l to global memory, LSE = scale * m + ln l
+    if (ok && nkv_t > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], (nkv_t - 1) & 1, p.err, DEV_TIMEOUT_SOFTMAX));
+      tc_fence_after();
+    }
+    const bool have_o = ok && nkv_t > 0;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int64_t orow = ((int64_t)(q_beg + rq) * p.hq + h) * D;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      if (have_o) {
+        tmem_ld32(tO + c * 32, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      if (rv) {
+        if (p.out_f32) {
+          float4* dst = reinterpret_cast<float4*>((float*)p.out + orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                 __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>((__nv_bfloat16*)p.out + orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
+            dst[i] = v;
+          }
+        }
+      }
+    }
+    if (rv && p.lse) p.lse[(int64_t)(q_beg + rq) * p.hq + h] = l > 0.f ? m_ref * p.scale + logf(l) : -INFINITY;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace tc
+
+cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t s) {
+  static bool attr_set[2][64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool paged = a.page_table != nullptr;
+  if (dev < 64 && !attr_set[paged][dev]) {
+    cudaError_t e = paged ? cudaFuncSetAttribute(tc::prefill_tc_kernel<true>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES)
+                          : cudaFuncSetAttribute(tc::prefill_tc_kernel<false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[paged][dev] = true;
+  }
+  if (a.max_seqlen_q == 0 || a.batch == 0 || a.h_hi == a.h_lo) return cudaSuccess;
+  tc::Params p;
+  p.cu_q = a.cu_q;
+  p.q_pos = a.q_pos;
+  p.cu_k = a.cu_k;
+  p.k_pos = a.k_pos;
+  p.page_table = a.page_table;
+  p.k_lens = a.k_lens;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.err = a.err;
+  p.num_pages = a.num_pages;
+  p.max_pages = a.max_pages;
+  p.hq = a.hq;
+  p.hkv = a.hkv;
+  p.h_lo = a.h_lo;
+  p.causal = a.causal;
+  p.out_f32 = a.out_f32;
+  p.scale = a.scale;
+  const int pairs = (a.max_seqlen_q + 2 * tc::BM - 1) / (2 * tc::BM);
+  dim3 grid(a.h_hi - a.h_lo, pairs, a.batch);
+  if (paged)
+    tc::prefill_tc_kernel<true><<<grid, tc::NTHREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, p);
+  else
+    tc::prefill_tc_kernel<false><<<grid, tc::NTHREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,432 @@
+"""Benchmark of the attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload all|prefill|decode] [--no-cpu-baseline]
+
+Headline (the JSON `value`): causal GQA prefill, batch 1 x 8192 tokens, 64 query /
+8 KV heads, head_dim 128, bf16 -- one step = RoPE of Q and K at absolute
+positions + tiled causal attention (O and LSE).  TFLOP/s counts 4*d flops per
+visible (query, key) pair.  The paged split-KV decode workload (32 requests,
+contexts U[16384, 131072], 16 splits + LSE merge) is reported in `decode`,
+as KV-cache GB/s.  Inputs are synthetic and seeded (N(0,1)/sqrt(2) bf16).
+
+Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on
+the launching stream, with an L2 flush (a 512 MB write) between steps outside
+the events; barrier + synchronize around the timed region, max over ranks.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload (rank 0 only).  Under torchrun every rank runs an independent replica
+(the path needs no exchange between GPUs) and `value` sums the ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "prefill attn TFLOP/s (% BF16 peak); decode KV-read GB/s (% HBM peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "attention_tiled_causal_gb300", "csrc")
+
+
+# ------------------------------------------------------------------ environment helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, f"{pre}{k}.")
+                elif isinstance(x, (int, float)):
+                    flat[pre[:-1]] = float(x)
+            walk(d)
+
+            def find(*keys):
+                for k, v in flat.items():
+                    if k.split(".")[-1] in keys:
+                        return v
+                return None
+            hbm = find("hbm_gbs", "hbm_GBs", "copy_gbs")
+            bf = find("bf16_tflops", "bf16_TFLOPs")
+            bfs = find("bf16_tflops_sustained")
+            if hbm and bf:
+                return {"hbm_gbs": hbm, "bf16_tflops": bf, "bf16_tflops_sustained": bfs or bf}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sha(fname):
+    return hashlib.sha256(open(os.path.join(CSRC, fname), "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(summary_name, kernel_file):
+    """DRAM bytes per launch recorded by an ncu capture summary under profiles/,
+    or None if there is none or the kernel source changed since it was taken."""
+    p = os.path.join(PROFILES, summary_name)
+    if not os.path.exists(p):
+        return None
+    rec = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith(("kernel_source_sha256", "dram_bytes_per_launch_full")):
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip().strip("`")
+    if rec.get("kernel_source_sha256") != kernel_sha(kernel_file):
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Timer:
+    """Per-step CUDA events on the launching stream, L2 flush outside the events."""
+
+    def __init__(self, flush_bytes=512 << 20):
+        self.flush = torch.empty(flush_bytes // 4, dtype=torch.float32, device="cuda")
+
+    def run(self, fn, steps, warmup, inner=None):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        tot, sub = 0.0, 0.0
+        s = torch.cuda.current_stream()
+        for _ in range(steps):
+            self.flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev = [] if inner is None else [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e0.record(s)
+            fn(ev)
+            e1.record(s)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+            if ev:
+                sub += ev[0].elapsed_time(ev[1])
+        return tot / steps, (sub / steps if inner else None)
+
+
+def prefill_arm(wl, args, timer, peaks, peak_src):
+    import attention_tiled_causal_gb300 as atc
+    inp = wl.make("cuda")
+    q, k, v, pos, cu = inp["q"], inp["k"], inp["v"], inp["pos"], inp["cu"]
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    launches = 3  # rope(Q), rope(K), prefill
+
+    def step(ev=()):
+        atc.rope_apply(q, pos)
+        atc.rope_apply(k, pos)
+        if ev:
+            ev[0].record()
+        atc.attn_prefill(q, k, v, out, lse, cu, pos, wl.seq, cu_k=cu, k_pos=pos)
+        if ev:
+            ev[1].record()
+
+    ms, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
+    atc.attn_device_status()
+    flops = wl.flops()
+    # end to end through the public API: pinned host inputs in, O and LSE back out
+    hq_, hk_, hv_ = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step(ev=()):
+        q.copy_(hq_, non_blocking=True)
+        k.copy_(hk_, non_blocking=True)
+        v.copy_(hv_, non_blocking=True)
+        step()
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    ms_e2e, _ = timer.run(e2e_step, args.steps, args.warmup)
+    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    peak = peaks["bf16_tflops"]
+    achieved = flops / (ms_kernel * 1e-3) / 1e12
+    traffic = profiled_traffic("prefill_tc_causal_8k.md", "prefill_tc.cu")
+    res = {
+        "ms_per_step": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "attn::tc::prefill_tc_kernel", "kernel_ms": round(ms_kernel, 4),
+                     "peak_source": f"{peak_src} bf16 dense (burst)"},
+        "e2e": {"value": round(flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
+        "launches_per_step": launches,
+        "inputs": (q, k, v, pos, cu),
+    }
+    return res
+
+
+def decode_arm(wl, args, timer, peaks, peak_src):
+    import attention_tiled_causal_gb300 as atc
+    inp = wl.make("cuda")
+    q = inp["q"]
+    po, pl = atc.decode_workspace(wl.batch, wl.hq, wl.splits, wl.d, "cuda")
+    out = torch.empty((wl.batch, wl.hq, wl.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((wl.batch, wl.hq), dtype=torch.float32, device="cuda")
+
+    def step(ev=()):
+        atc.rope_apply(q, inp["q_pos"])
+        if ev:
+            ev[0].record()
+        atc.attn_decode_paged(q, inp["k_cache"], inp["v_cache"], inp["page_table"], inp["ctx_lens"], wl.splits,
+                              po, pl, out, lse)
+        if ev:
+            ev[1].record()
+
+    ms, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
+    atc.attn_device_status()
+    kv = wl.kv_bytes()
+    part = wl.batch * wl.hq * wl.splits * (wl.d + 1) * 4
+    qb = wl.batch * wl.hq * wl.d * 2
+    outb = wl.batch * wl.hq * (wl.d * 2 + 4)
+    alg_step = kv + qb + 2 * part + outb            # cache + q + partials out and back + result
+    peak = peaks["hbm_gbs"]
+    achieved = alg_step / (ms_kernel * 1e-3) / 1e9  # split + merge kernels (rope of q is ~0.5 MB)
+    del inp
+    return {
+        "metric": "decode KV-read GB/s", "unit": "GB/s", "value": round(kv / (ms * 1e-3) / 1e9, 1),
+        "ms_per_step": round(ms, 4), "kv_bytes_per_step": kv,
+        "workload": wl.name,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic("decode_split_paged_b32.md", "decode.cu"),
+                     "kernel": "attn::dec::decode_split_kernel + attn::lse_merge_kernel",
+                     "kernel_ms": round(ms_kernel, 4), "peak_source": f"{peak_src} HBM copy"},
+        "gpu_launches_per_step": 3,
+    }
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def oracle_sample(wl, inputs, n_rows, seed):
+    """Time the oracle on n_rows query rows (all heads) of the prefill workload:
+    RoPE of those rows and of all keys, bf16 rounding, three-pass attention.
+    Returns (seconds, flops of the sample)."""
+    import oracle
+    q, k, v, pos, cu = inputs
+    rows = synth_rows(wl.seq, n_rows, seed)
+    qs = q[torch.from_numpy(rows).to(q.device)].cpu()
+    kc, vc = k.cpu(), v.cpu()
+    posn = pos.cpu().numpy()
+    t0 = time.perf_counter()
+    qr = oracle.round_bf16(oracle.rope(qs.to(torch.float64).numpy(), posn[rows], wl.base))
+    kr = oracle.round_bf16(oracle.rope(kc.to(torch.float64).numpy(), posn, wl.base))
+    oracle.attention(qr, np.zeros(len(rows), np.int32), posn[rows], kr, vc.to(torch.float64).numpy(),
+                     cu.cpu().numpy(), posn, wl.scale)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * wl.d * wl.hq * float(np.sum(rows + 1))
+    return dt, flops
+
+
+def synth_rows(seq, n, seed):
+    import synth
+    return synth.sample_rows(seq, n, seed)
+
+
+def cpu_baseline(wl, inputs, rows=1024):
+    import oracle
+    dt, flops = oracle_sample(wl, inputs, rows, 99)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{rows} seeded query rows x all 64 heads of the 8192-token prefill "
+                      f"(RoPE + bf16 rounding + fp64 three-pass attention), {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="all", choices=["all", "prefill", "decode"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    import synth
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        reference_arm(args, synth)
+        return 0
+
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    peaks, peak_src = load_peaks()
+    timer = Timer()
+    wl = synth.PREFILL_8K
+    res = None
+    if args.workload in ("all", "prefill"):
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            res = prefill_arm(wl, args, timer, peaks, peak_src)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        clocks = clk.summary()
+    dec = None
+    if args.workload in ("all", "decode"):
+        dec = decode_arm(synth.DECODE, args, timer, peaks, peak_src)
+    ms = res["ms_per_step"] if res else dec["ms_per_step"]
+    if pg:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    line = {"metric": METRIC}
+    if res:
+        value = ws * res["flops"] / (ms * 1e-3) / 1e12
+        line.update({"value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+                     "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+                     "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                     "config": {"workload": wl.name + " (RoPE of Q and K + attention, O and LSE)",
+                                "batch": wl.batch, "seq_len": wl.seq, "q_heads": wl.hq, "kv_heads": wl.hkv,
+                                "head_dim": wl.d, "flops_per_step": res["flops"], "l2_flush": True,
+                                "parallelism": f"replicas x{ws}"},
+                     "roofline": res["roofline"], "e2e": res["e2e"], "clocks": clocks,
+                     "gpu_launches": res["launches_per_step"] * args.steps})
+    else:
+        line.update({"value": dec["value"], "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+                     "warmup": args.warmup, "ms_per_step": dec["ms_per_step"], "higher_is_better": True,
+                     "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                     "config": {"workload": dec["workload"]}, "roofline": dec["roofline"],
+                     "gpu_launches": dec["gpu_launches_per_step"] * args.steps})
+    if dec and res:
+        line["decode"] = dec
+    if res and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, res["inputs"])
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def reference_arm(args, synth):
+    """The fp64 CPU oracle on the host cores, on a bounded sample of the same workload."""
+    import oracle
+    oracle.build()
+    wl = synth.PREFILL_8K
+    inp = wl.make("cpu")
+    inputs = (inp["q"], inp["k"], inp["v"], inp["pos"], inp["cu"])
+    rows = 192
+    for i in range(args.warmup):
+        oracle_sample(wl, inputs, 16, 1000 + i)
+    times, flops = [], 0.0
+    for i in range(args.steps):
+        dt, fl = oracle_sample(wl, inputs, rows, 2000 + i)
+        times.append(dt)
+        flops = fl
+    tot = sum(times)
+    total_flops = flops * args.steps
+    value = total_flops / tot / 1e12
+    ms = tot / args.steps * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name + " (RoPE of Q and K + attention, O and LSE)", "batch": wl.batch,
+                       "seq_len": wl.seq, "q_heads": wl.hq, "kv_heads": wl.hkv, "head_dim": wl.d},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"each step: {rows} seeded query rows x 64 heads of the 8192-token "
+                                       f"prefill (RoPE + bf16 rounding + fp64 three-pass attention)"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

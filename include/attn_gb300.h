@@ -1,0 +1,193 @@
+/*
+ * attn_gb300.h -- C ABI of libattn_gb300.so: exact causal GQA attention for
+ * LLM serving on GB300 (sm_103a).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor and table pointers are DEVICE pointers owned by the caller.
+ *    The library never allocates or frees caller memory and keeps no state
+ *    between calls apart from cached per-device constants.
+ *  - Tensors are packed row-major with the head dimension contiguous:
+ *    Q/K/V/O as [tokens][heads][head_dim] ("Ulysses sequence parallelism for
+ *    inference", section 2.2: Q/K/V shaped [seq, heads, head_dim]).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call only
+ *    enqueues work on it and returns; nothing synchronises.
+ *  - Return value: ATTN_OK (0) or an ATTN_ERR_* code.  On an argument error
+ *    nothing is launched; attn_last_error() describes the failure (thread-local).
+ *  - Faults found on the device (a page id outside the cache, a pipeline wait
+ *    that ran out of time) never trap: the kernel records a code that
+ *    attn_device_status() returns after the work has finished.
+ *  - Calls on different streams may run concurrently; they share no scratch.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP32 = 1 } attn_dtype_t;
+
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_ARG = 1,         /* null pointer, negative or inconsistent size */
+  ATTN_ERR_SHAPE = 2,       /* head layout the kernels do not support */
+  ATTN_ERR_ALIGN = 3,       /* a pointer or stride is not 16-byte aligned */
+  ATTN_ERR_UNSUPPORTED = 4, /* dtype / option combination not built */
+  ATTN_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed */
+  ATTN_ERR_DEVICE = 6       /* a kernel recorded a device-side fault */
+};
+
+/* Message for the last non-zero status returned on this thread. */
+ATTN_API const char *attn_last_error(void);
+
+/* Synchronises the current device, then returns ATTN_OK, or ATTN_ERR_DEVICE if
+ * a kernel recorded a fault since the last clear (the code is in the message),
+ * or ATTN_ERR_CUDA if the synchronisation itself failed.  clear != 0 resets
+ * the recorded code. */
+ATTN_API int attn_device_status(int clear);
+
+/*
+ * rope_apply -- rotary position embedding at ABSOLUTE positions, in place.
+ *
+ * Defined by: Ulysses page, section 3.2 (each local token carries its absolute
+ * position from a global token-index table and RoPE uses that position) and
+ * section 5.3 (local indices must never be used).  The pages give no formula;
+ * this library uses the half-split pairing: for i in [0, head_dim/2),
+ *     a = positions[t] * base^(-2i/head_dim)
+ *     x[i]          <- x[i] cos a - x[i + head_dim/2] sin a
+ *     x[i + d/2]    <- x[i + d/2] cos a + x[i] sin a
+ * The rotation is computed in fp32 from an angle reduced in fp64, and the
+ * result is stored back in the tensor's dtype (bf16: round to nearest even).
+ *
+ *  x            [tokens][heads][head_dim] of `dtype`, row t at x + t*stride_token
+ *               elements; 16-byte aligned; rotated in place.
+ *  positions    [tokens] int32 absolute positions (>= 0).
+ *  stride_token elements between consecutive tokens (>= heads*head_dim, multiple
+ *               of 8 for bf16 / 4 for fp32).
+ *  head_dim     even, with head_dim/2 a multiple of 8 (bf16) or 4 (fp32).
+ */
+ATTN_API int rope_apply(void *x, attn_dtype_t dtype, int64_t tokens, int heads, int head_dim,
+               int64_t stride_token, const int32_t *positions, double base, void *stream);
+
+/*
+ * attn_prefill -- exact causal GQA attention, FlashAttention-style tiled.
+ *
+ * Computes, for every query row of every sequence and every query head h in
+ * [h_lo, h_hi):  S = scale * q k^T over the visible keys, A = softmax(S), O = A V,
+ * and LSE = ln sum_j exp(S_j)  ("Flash Attention and distributed parallelism",
+ * section 18.2 for the definition; section 18.3 for the blockwise online
+ * softmax with per-block rescaling by exp(m_old - m_new); section 18.4 for the
+ * query-outer loop with normalisation deferred to the end).  The N x N score
+ * matrix is never stored.  Key j is visible to query i iff (!causal or
+ * kpos_j <= qpos_i) -- positions, not indices (Ulysses page, section 5.3).
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads) (GQA, Ulysses
+ * page, section 3.2).  Heads outside [h_lo, h_hi) of out/lse are not touched,
+ * so head slices of one problem put together equal the all-heads call
+ * ("full sequence, some heads", Ulysses page, sections 2.1-2.2).
+ *
+ *  q          [Tq][num_q_heads][head_dim] (already rotated), Tq = cu_q[batch].
+ *  cu_q       [batch+1] int32 prefix offsets of each sequence's query rows.
+ *  q_pos      [Tq] int32 absolute query positions, non-decreasing within a sequence.
+ *  total_q    Tq as a host value (sizes the TMA descriptor of q).
+ *  max_seqlen_q  largest cu_q[b+1]-cu_q[b] (host value; sizes the grid).
+ *  Contiguous key/value source (page_table == NULL):
+ *    k, v     [Tk][num_kv_heads][head_dim], Tk = cu_k[batch]; cu_k [batch+1];
+ *    k_pos    [Tk] absolute key positions, non-decreasing within a sequence;
+ *    total_k  Tk as a host value.
+ *  Paged key/value source (page_table != NULL; SGLang page, section 2.1:
+ *  token-to-cache-slot indirection; Ulysses page, section 2.3: head-sharded cache):
+ *    k, v     head-major caches [num_kv_heads][num_pages][page_size][head_dim];
+ *    page_table [batch][max_pages] int32 physical page of each logical page;
+ *    k_lens   [batch] int32 cached tokens of each request; cached token j of
+ *             request b is page_table[b][j/page_size], slot j%page_size, and sits
+ *             at position j.  cu_k and k_pos must be NULL, total_k is ignored.
+ *             Unused slots of a request's last page must hold finite values.
+ *  out        [Tq][num_q_heads][head_dim] of out_dtype.
+ *  lse        [Tq][num_q_heads] fp32 natural-log LSE of the scaled scores, or NULL.
+ *             A row with no visible key gets O = 0 and LSE = -inf.
+ *  h_lo, h_hi query-head range; both multiples of num_q_heads/num_kv_heads.
+ *  dtype      ATTN_BF16 (tensor-core path; head_dim 128 uses the tcgen05 kernel)
+ *             or ATTN_FP32 (CUDA-core path).  head_dim: multiple of 32, <= 256.
+ *             bf16 paged sources need page_size 64 for the tensor-core kernel.
+ * All pointers 16-byte aligned.  Errors: ATTN_ERR_ARG / _SHAPE / _ALIGN / _CUDA.
+ */
+ATTN_API int attn_prefill(const void *q, const void *k, const void *v, void *out, attn_dtype_t out_dtype,
+                 float *lse, attn_dtype_t dtype, int batch, const int32_t *cu_q,
+                 const int32_t *q_pos, int64_t total_q, int max_seqlen_q, const int32_t *cu_k,
+                 const int32_t *k_pos, int64_t total_k,
+                 const int32_t *page_table, const int32_t *k_lens, int max_pages, int page_size,
+                 int64_t num_pages, int num_q_heads, int num_kv_heads, int head_dim, int h_lo,
+                 int h_hi, float scale, int causal, void *stream);
+
+/*
+ * attn_decode_paged -- split-KV decode over a head-major paged KV cache.
+ *
+ * One new query token per request at position ctx_lens[b]-1 attends to all
+ * ctx_lens[b] cached tokens (its own K/V already written to the cache).  The
+ * cached tokens are cut into num_splits partitions of whole pages; each
+ * partition yields a partial (O_s, LSE_s) and the partials are combined by the
+ * log-sum-exp merge of attn_lse_merge.  Defined by: Flash Attention page,
+ * section 18.3 (partial softmax states over disjoint key blocks combine through
+ * the rescale exp(m_old - m_new)) and section 18.4 (the key sequence as a
+ * parallel axis); paged cache: SGLang page, section 2.1, and the PagedAttention
+ * reference in section 18.12 of the Flash Attention page; head-major layout:
+ * Ulysses page, section 2.3.  Split s covers logical pages
+ * [s*pps, min((s+1)*pps, n_pages)) with n_pages = ceil(ctx/page_size) and
+ * pps = ceil(n_pages/num_splits); an empty split has LSE_s = -inf.
+ *
+ *  q          [batch][num_q_heads][head_dim] bf16, already rotated.
+ *  k_cache, v_cache  [num_kv_heads][num_pages][page_size][head_dim] bf16.
+ *  page_table [batch][max_pages] int32; ctx_lens [batch] int32 (>= 0,
+ *             <= max_pages*page_size).
+ *  part_out   workspace [batch][num_q_heads][num_splits][head_dim] fp32 and
+ *  part_lse   workspace [batch][num_q_heads][num_splits] fp32, written here.
+ *  out        [batch][num_q_heads][head_dim] of out_dtype; lse [batch][num_q_heads]
+ *             fp32 or NULL.  If out is NULL only the partials are written.
+ *  Supported: bf16, head_dim 128, page_size 64, num_q_heads/num_kv_heads = 8,
+ *  1 <= num_splits <= 256.  Errors: ATTN_ERR_ARG / _SHAPE / _ALIGN / _CUDA.
+ */
+ATTN_API int attn_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *page_table, const int32_t *ctx_lens, int batch,
+                      int max_pages, int page_size, int64_t num_pages, int num_q_heads,
+                      int num_kv_heads, int head_dim, int num_splits, float scale,
+                      float *part_out, float *part_lse, void *out, attn_dtype_t out_dtype,
+                      float *lse, void *stream);
+
+/*
+ * attn_lse_merge -- combine partial attention results over disjoint key sets.
+ *
+ *   LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s
+ * Parts with LSE_s = -inf carry weight 0; if every part is -inf, O = 0 and
+ * LSE = -inf.  Defined by: Flash Attention page, section 18.3 (merging the
+ * running (m, l, O) state of one key block into another by exp(m_old - m_new)),
+ * and the per-step accumulation of ring attention on the SGLang page,
+ * section 3.5.  Used for split-KV decode and for a prefill chunk merged with
+ * its cached prefix.
+ *
+ *  part_out   fp32, element (p, r, h, i) at
+ *             part_out[p*o_stride_part + r*o_stride_row + h*o_stride_head + i]
+ *  part_lse   fp32, element (p, r, h) at
+ *             part_lse[p*l_stride_part + r*l_stride_row + h*l_stride_head]
+ *  out        [rows][heads][head_dim] of out_dtype; lse_out [rows][heads] fp32 or NULL.
+ *  Strides are in elements.  1 <= n_parts <= 1024.
+ */
+ATTN_API int attn_lse_merge(const float *part_out, const float *part_lse, int n_parts, int64_t rows,
+                   int heads, int head_dim, int64_t o_stride_part, int64_t o_stride_row,
+                   int64_t o_stride_head, int64_t l_stride_part, int64_t l_stride_row,
+                   int64_t l_stride_head, void *out, attn_dtype_t out_dtype, float *lse_out,
+                   void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

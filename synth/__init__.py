@@ -28,14 +28,20 @@ PAGE = 64  # tokens per KV-cache page
 _CHUNK = 1 << 26  # draw in slices so the fp32 temporaries stay small
 
 
-def randn(shape, seed: int, std: float = 1.0, dtype=torch.bfloat16) -> torch.Tensor:
-    """N(0, std^2) samples of `shape`, drawn in fp32 and rounded once to `dtype`."""
+def randn(shape, seed: int, std: float = 1.0, dtype=torch.bfloat16, device="cpu") -> torch.Tensor:
+    """N(0, std^2) samples of `shape`, drawn in fp32 and rounded once to `dtype`.
+
+    The stream of numbers depends on (seed, shape, device): a CPU draw and a
+    CUDA draw with the same seed differ, but each is reproducible.  Large
+    workloads are drawn on the GPU and copied back for whatever part the CPU
+    checks need."""
     n = int(np.prod(shape)) if len(shape) else 1
-    out = torch.empty(n, dtype=dtype)
-    g = torch.Generator().manual_seed(int(seed))
+    dev = torch.device(device)
+    out = torch.empty(n, dtype=dtype, device=dev)
+    g = torch.Generator(device=dev).manual_seed(int(seed))
     for s in range(0, n, _CHUNK):
         e = min(n, s + _CHUNK)
-        x = torch.randn(e - s, generator=g, dtype=torch.float32)
+        x = torch.randn(e - s, generator=g, dtype=torch.float32, device=dev)
         if std != 1.0:
             x.mul_(std)
         out[s:e] = x.to(dtype)
@@ -133,14 +139,13 @@ class Prefill:
 
     def make(self, device="cpu"):
         T = self.tokens
-        q = randn((T, self.hq, self.d), self.seed * 16 + 1, self.std, self.dtype)
-        k = randn((T, self.hkv, self.d), self.seed * 16 + 2, self.std, self.dtype)
-        v = randn((T, self.hkv, self.d), self.seed * 16 + 3, self.std, self.dtype)
+        q = randn((T, self.hq, self.d), self.seed * 16 + 1, self.std, self.dtype, device)
+        k = randn((T, self.hkv, self.d), self.seed * 16 + 2, self.std, self.dtype, device)
+        v = randn((T, self.hkv, self.d), self.seed * 16 + 3, self.std, self.dtype, device)
         lens = [self.seq] * self.batch
         pos = positions(lens, [self.q_start] * self.batch)
         cu = cu_seqlens(lens)
-        return dict(q=q.to(device), k=k.to(device), v=v.to(device),
-                    pos=torch.from_numpy(pos).to(device), cu=torch.from_numpy(cu).to(device))
+        return dict(q=q, k=k, v=v, pos=torch.from_numpy(pos).to(device), cu=torch.from_numpy(cu).to(device))
 
 
 @dataclass
@@ -170,16 +175,15 @@ class ChunkedPaged:
     def make(self, device="cpu"):
         B, P = self.batch, PAGE
         table, num_pages = shuffled_page_table([self.prefix] * B, self.seed * 16 + 9)
-        kc = randn((self.hkv, num_pages, P, self.d), self.seed * 16 + 4, self.std)
-        vc = randn((self.hkv, num_pages, P, self.d), self.seed * 16 + 5, self.std)
+        kc = randn((self.hkv, num_pages, P, self.d), self.seed * 16 + 4, self.std, device=device)
+        vc = randn((self.hkv, num_pages, P, self.d), self.seed * 16 + 5, self.std, device=device)
         T = B * self.chunk
-        q = randn((T, self.hq, self.d), self.seed * 16 + 1, self.std)
-        k = randn((T, self.hkv, self.d), self.seed * 16 + 2, self.std)
-        v = randn((T, self.hkv, self.d), self.seed * 16 + 3, self.std)
+        q = randn((T, self.hq, self.d), self.seed * 16 + 1, self.std, device=device)
+        k = randn((T, self.hkv, self.d), self.seed * 16 + 2, self.std, device=device)
+        v = randn((T, self.hkv, self.d), self.seed * 16 + 3, self.std, device=device)
         qpos = positions([self.chunk] * B, [self.prefix] * B)
         kpos_prefix = positions([self.prefix] * B)
-        return dict(q=q.to(device), k=k.to(device), v=v.to(device),
-                    k_cache=kc.to(device), v_cache=vc.to(device),
+        return dict(q=q, k=k, v=v, k_cache=kc, v_cache=vc,
                     page_table=torch.from_numpy(table).to(device), num_pages=num_pages,
                     q_pos=torch.from_numpy(qpos).to(device),
                     prefix_pos=torch.from_numpy(kpos_prefix).to(device),
@@ -221,11 +225,11 @@ class Decode:
     def make(self, device="cpu"):
         ctx = self.ctx_lens()
         table, num_pages = shuffled_page_table(ctx, self.seed * 16 + 8)
-        kc = randn((self.hkv, max(num_pages, 1), PAGE, self.d), self.seed * 16 + 4, self.kv_std)
-        vc = randn((self.hkv, max(num_pages, 1), PAGE, self.d), self.seed * 16 + 5, self.kv_std)
-        q = randn((self.batch, self.hq, self.d), self.seed * 16 + 1, self.q_std)
+        kc = randn((self.hkv, max(num_pages, 1), PAGE, self.d), self.seed * 16 + 4, self.kv_std, device=device)
+        vc = randn((self.hkv, max(num_pages, 1), PAGE, self.d), self.seed * 16 + 5, self.kv_std, device=device)
+        q = randn((self.batch, self.hq, self.d), self.seed * 16 + 1, self.q_std, device=device)
         qpos = (ctx - 1).astype(np.int32)
-        return dict(q=q.to(device), k_cache=kc.to(device), v_cache=vc.to(device),
+        return dict(q=q, k_cache=kc, v_cache=vc,
                     page_table=torch.from_numpy(table).to(device), num_pages=num_pages,
                     ctx_lens=torch.from_numpy(ctx).to(device),
                     q_pos=torch.from_numpy(qpos).to(device))

@@ -1,0 +1,104 @@
+"""The C-ABI library loads and exports every function include/attn_gb300.h declares,
+and its host-side argument checks reject bad calls before touching a GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import attention_tiled_causal_gb300 as atc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_gb300.h")
+
+ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED = 1, 2, 3, 4
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*ATTN_API\s+(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_tiled_causal_gb300 import build
+    build.build()
+    return atc.library()
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for n in ("rope_apply", "attn_prefill", "attn_decode_paged", "attn_lse_merge", "attn_last_error",
+              "attn_device_status"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"libattn_gb300.so does not export {n}"
+
+
+def test_only_the_c_abi_is_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", atc.lib_path()], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {s for s in exported if s.startswith(("attn_", "rope_"))}
+    assert ours == set(declared_functions())
+
+
+def _prefill(lib, **kw):
+    a = dict(q=16, k=16, v=16, out=16, out_dtype=0, lse=None, dtype=0, batch=1, cu_q=16, q_pos=16, total_q=4,
+             max_seqlen_q=4, cu_k=16, k_pos=16, total_k=4, page_table=None, k_lens=None, max_pages=0,
+             page_size=0, num_pages=0, hq=8, hkv=2, d=128, h_lo=0, h_hi=8, scale=0.1, causal=1, stream=None)
+    a.update(kw)
+    return lib.attn_prefill(*a.values())
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    assert _prefill(lib, h_lo=2) == ERR_SHAPE            # not a whole GQA group
+    assert _prefill(lib, h_hi=9) == ERR_SHAPE
+    assert _prefill(lib, hq=6, hkv=4) == ERR_SHAPE       # 6 % 4 != 0
+    assert _prefill(lib, d=96) == ERR_SHAPE
+    assert _prefill(lib, dtype=1, out_dtype=0) == ERR_UNSUPPORTED
+    assert _prefill(lib, batch=-1) == ERR_ARG
+    assert _prefill(lib, q=None) == ERR_ARG
+    assert _prefill(lib, q=8) == ERR_ALIGN               # misaligned device pointer
+    assert _prefill(lib, scale=0.0) == ERR_ARG
+    assert _prefill(lib, cu_k=None) == ERR_ARG           # contiguous source needs cu_k
+    assert _prefill(lib, page_table=16, k_lens=16) == ERR_ARG   # paged source takes no cu_k/k_pos
+    assert b"GQA" in lib.attn_last_error() or len(lib.attn_last_error()) > 0
+
+
+def test_prefill_empty_problem_is_a_no_op(lib):
+    assert _prefill(lib, batch=0) == 0
+    assert _prefill(lib, h_lo=4, h_hi=4) == 0
+    assert _prefill(lib, max_seqlen_q=0) == 0
+
+
+def test_decode_rejects_bad_arguments(lib):
+    base = dict(q=16, kc=16, vc=16, table=16, ctx=16, batch=2, max_pages=4, page=64, num_pages=8, hq=64, hkv=8,
+                d=128, splits=16, scale=0.1, po=16, pl=16, out=16, odt=0, lse=None, stream=None)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return lib.attn_decode_paged(*a.values())
+
+    assert call(hq=32) == ERR_SHAPE
+    assert call(d=64) == ERR_SHAPE
+    assert call(page=32) == ERR_SHAPE
+    assert call(splits=0) == ERR_ARG
+    assert call(splits=257) == ERR_ARG
+    assert call(table=None) == ERR_ARG
+    assert call(kc=24) == ERR_ALIGN
+    assert call(batch=0) == 0
+
+
+def test_rope_and_merge_reject_bad_arguments(lib):
+    assert lib.rope_apply(16, 0, 4, 2, 100, 200, 16, 1e4, None) == ERR_SHAPE   # 50 not a multiple of 8
+    assert lib.rope_apply(16, 0, 4, 2, 128, 100, 16, 1e4, None) == ERR_ARG     # stride < heads*d
+    assert lib.rope_apply(8, 0, 4, 2, 128, 256, 16, 1e4, None) == ERR_ALIGN
+    assert lib.rope_apply(16, 0, 0, 2, 128, 256, 16, 1e4, None) == 0          # nothing to do
+    assert lib.attn_lse_merge(16, 16, 0, 4, 2, 128, 0, 0, 0, 0, 0, 0, 16, 0, None, None) == ERR_ARG
+    assert lib.attn_lse_merge(16, 16, 2, 0, 2, 128, 0, 0, 0, 0, 0, 0, 16, 0, None, None) == 0

@@ -1,0 +1,451 @@
+"""CUDA path vs the fp64 CPU oracle, element by element, on seeded inputs.
+
+Tolerances (bf16 inputs, fp32 accumulation): max |dO| <= 1e-2, mean |dO| <= 1e-3,
+max |dLSE| <= 1e-3.  fp32 inputs (CUDA-core path): 1e-5.  Integer work (page
+gather, positions) is checked bit-exactly through invariance tests.
+
+The path stores RoPE's output in the tensor's dtype, so attention consumes
+bf16-rounded rotated Q/K; the oracle models that step by rounding its own fp64
+rotation to bf16 (ties to even) before its three-pass attention.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import attention_tiled_causal_gb300 as atc
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL_MAX, TOL_MEAN, TOL_LSE = 1e-2, 1e-3, 1e-3
+TOL_F32 = 1e-5
+
+
+def check(out, lse, want_o, want_l, tol_max=TOL_MAX, tol_mean=TOL_MEAN, tol_lse=TOL_LSE, what=""):
+    o = out.float().cpu().numpy() if torch.is_tensor(out) else out
+    d = np.abs(o - want_o)
+    assert np.isfinite(o).all(), f"{what}: non-finite output"
+    assert d.max() <= tol_max, f"{what}: max |dO| = {d.max():.3g}"
+    assert d.mean() <= tol_mean, f"{what}: mean |dO| = {d.mean():.3g}"
+    if lse is not None:
+        l = lse.cpu().numpy() if torch.is_tensor(lse) else lse
+        inf = np.isinf(want_l)
+        assert np.array_equal(np.isinf(l), inf), f"{what}: -inf LSE pattern differs"
+        if (~inf).any():
+            dl = np.abs(l[~inf] - want_l[~inf]).max()
+            assert dl <= tol_lse, f"{what}: max |dLSE| = {dl:.3g}"
+
+
+def rotated_bf16(x, pos, base=10000.0):
+    return oracle.round_bf16(oracle.rope(synth.as_f64(x), np.asarray(pos)))
+
+
+def seq_ids(lens):
+    return np.repeat(np.arange(len(lens), dtype=np.int32), lens)
+
+
+@pytest.fixture(autouse=True)
+def _clean_device_status():
+    atc.attn_device_status(clear=True)
+    yield
+    atc.attn_device_status(clear=True)
+
+
+# ------------------------------------------------------------------ RoPE
+
+def test_rope_bf16_matches_oracle_within_one_ulp():
+    T, H, d = 1500, 8, 128
+    x = synth.randn((T, H, d), 101, 0.7071)
+    pos = np.sort(np.random.default_rng(1).integers(0, 131072, T)).astype(np.int32)
+    pos[:4] = [0, 1, 65535, 131071]
+    xd = x.to(DEV)
+    atc.rope_apply(xd, torch.from_numpy(pos).to(DEV))
+    got = synth.as_f64(xd.cpu())
+    want = rotated_bf16(x, pos)
+    ulp = np.maximum(np.abs(want), 1e-30) * 2.0 ** -7
+    diff = np.abs(got - want)
+    assert (diff <= ulp + 1e-30).all(), f"max diff {diff.max():.3g}"
+    assert (diff > 0).mean() < 0.01, f"{(diff > 0).mean():.3%} of elements differ by one ulp"
+    np.testing.assert_array_equal(got[pos == 0], synth.as_f64(x)[pos == 0])  # position 0: identity
+
+
+def test_rope_fp32_matches_oracle():
+    T, H, d = 333, 2, 64
+    x = synth.randn((T, H, d), 102, 1.0, torch.float32)
+    pos = np.arange(T, dtype=np.int32) * 97
+    xd = x.to(DEV)
+    atc.rope_apply(xd, torch.from_numpy(pos).to(DEV))
+    want = oracle.rope(synth.as_f64(x), pos)
+    assert np.abs(xd.cpu().double().numpy() - want).max() < 2e-6
+
+
+def test_rope_strided_token_rows():
+    """Rotating a [T, H, d] view of a wider buffer touches only that view."""
+    T, H, d = 64, 4, 128
+    big = synth.randn((T, 2 * H, d), 103, 1.0).to(DEV)
+    before = big.clone()
+    pos = torch.arange(T, dtype=torch.int32, device=DEV) + 7
+    atc.rope_apply(big[:, :H], pos)
+    assert torch.equal(big[:, H:], before[:, H:])
+    want = rotated_bf16(before[:, :H].cpu(), pos.cpu().numpy())
+    assert np.abs(synth.as_f64(big[:, :H].cpu()) - want).max() <= 2.0 ** -7 * 4
+
+
+# ------------------------------------------------------------------ LSE merge
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_lse_merge_matches_oracle(out_dtype):
+    P, R, H, d = 5, 37, 6, 128
+    rng = np.random.default_rng(7)
+    po = rng.normal(0, 1, (P, R, H, d)).astype(np.float32)
+    pl = rng.normal(0, 3, (P, R, H)).astype(np.float32)
+    pl[1, :, 0] = -np.inf          # an empty part
+    pl[:, 3, 2] = -np.inf          # a row with no part at all
+    want_o, want_l = oracle.lse_merge(po.astype(np.float64), pl.astype(np.float64))
+    out = torch.empty((R, H, d), dtype=out_dtype, device=DEV)
+    lse = torch.empty((R, H), dtype=torch.float32, device=DEV)
+    atc.attn_lse_merge(torch.from_numpy(po).to(DEV), torch.from_numpy(pl).to(DEV), out, lse)
+    tol = 1e-5 if out_dtype == torch.float32 else 8e-3
+    check(out, lse, want_o, want_l, tol_max=tol, tol_mean=tol, tol_lse=1e-5, what="merge")
+    assert torch.all(out[3, 2] == 0)
+
+
+def test_lse_merge_strided_split_layout():
+    """Partials laid out [rows, H, splits, d] (the decode workspace) via strides."""
+    R, H, S, d = 9, 4, 16, 128
+    rng = np.random.default_rng(8)
+    po = rng.normal(0, 1, (R, H, S, d)).astype(np.float32)
+    pl = rng.normal(0, 1, (R, H, S)).astype(np.float32)
+    pl[:, :, 10:] = -np.inf
+    want_o, want_l = oracle.lse_merge(po.transpose(2, 0, 1, 3), pl.transpose(2, 0, 1))
+    po_d = torch.from_numpy(po).to(DEV)
+    pl_d = torch.from_numpy(pl).to(DEV)
+    out = torch.empty((R, H, d), dtype=torch.float32, device=DEV)
+    lse = torch.empty((R, H), dtype=torch.float32, device=DEV)
+    atc.attn_lse_merge(po_d.permute(2, 0, 1, 3), pl_d.permute(2, 0, 1), out, lse)
+    check(out, lse, want_o, want_l, tol_max=1e-5, tol_mean=1e-6, tol_lse=1e-5, what="strided merge")
+
+
+# ------------------------------------------------------------------ prefill: fp32 tiny (CUDA cores)
+
+def _tiny_run(w, inp, h_lo=0, h_hi=None, key_rows=None):
+    q, k, v = inp["q"].clone().to(DEV), inp["k"].clone().to(DEV), inp["v"].to(DEV)
+    pos = inp["pos"].to(DEV)
+    atc.rope_apply(q, pos)
+    atc.rope_apply(k, pos)
+    cu = inp["cu"].to(DEV)
+    if key_rows is not None:
+        idx = torch.from_numpy(key_rows).to(DEV)
+        k, v, kpos = k[idx].contiguous(), v[idx].contiguous(), pos[idx].contiguous()
+        cu_k = torch.tensor([0, len(key_rows)], dtype=torch.int32, device=DEV)
+    else:
+        kpos, cu_k = pos, cu
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=DEV)
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    atc.attn_prefill(q, k, v, out, lse, cu, pos, w.seq, cu_k=cu_k, k_pos=kpos, h_lo=h_lo, h_hi=h_hi)
+    atc.attn_device_status()
+    return out, lse
+
+
+def test_tiny_fp32_causal_gqa_matches_oracle():
+    w = synth.TINY
+    inp = w.make()
+    out, lse = _tiny_run(w, inp)
+    pos = inp["pos"].numpy()
+    qr = oracle.rope(synth.as_f64(inp["q"]), pos)
+    kr = oracle.rope(synth.as_f64(inp["k"]), pos)
+    want_o, want_l = oracle.attention(qr, seq_ids([w.seq]), pos, kr, synth.as_f64(inp["v"]), inp["cu"].numpy(),
+                                      pos, w.scale)
+    check(out, lse, want_o, want_l, TOL_F32, TOL_F32, TOL_F32, "tiny fp32")
+
+
+def test_tiny_fp32_head_slices_and_key_chunks_recombine():
+    """Ulysses page, 2.2 (4 segments of 16 tokens): two head slices of one KV group
+    each equal the all-heads call, and four key chunks merged by LSE equal it too."""
+    w = synth.TINY
+    inp = w.make()
+    full_o, full_l = _tiny_run(w, inp)
+    G = w.hq // w.hkv
+    for lo in range(0, w.hq, G):
+        o, l = _tiny_run(w, inp, lo, lo + G)
+        assert torch.equal(o[:, lo:lo + G], full_o[:, lo:lo + G])
+        assert torch.equal(l[:, lo:lo + G], full_l[:, lo:lo + G])
+        assert torch.isnan(o[:, :lo]).all() and torch.isnan(o[:, lo + G:]).all()  # other heads untouched
+    po, pl = [], []
+    for c in range(4):
+        o, l = _tiny_run(w, inp, key_rows=np.arange(16 * c, 16 * c + 16))
+        po.append(o)
+        pl.append(l)
+    out = torch.empty_like(full_o)
+    lse = torch.empty_like(full_l)
+    atc.attn_lse_merge(torch.stack(po), torch.stack(pl), out, lse)
+    check(out, lse, full_o.cpu().numpy(), full_l.cpu().numpy(), 1e-5, 1e-6, 1e-5, "chunks merged")
+
+
+# ------------------------------------------------------------------ prefill: bf16, tensor cores
+
+def _bf16_case(lens, hq, hkv, starts, seed, d=128):
+    T = sum(lens)
+    q = synth.randn((T, hq, d), seed, 0.7071)
+    k = synth.randn((T, hkv, d), seed + 1, 0.7071)
+    v = synth.randn((T, hkv, d), seed + 2, 0.7071)
+    pos = synth.positions(lens, starts)
+    cu = synth.cu_seqlens(lens)
+    return q, k, v, pos, cu
+
+
+def _run_prefill(q, k, v, pos, cu, lens, causal=True, h_lo=0, h_hi=None, out_dtype=None, simt=False):
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    posd, cud = torch.from_numpy(pos).to(DEV), torch.from_numpy(cu).to(DEV)
+    atc.rope_apply(qd, posd)
+    atc.rope_apply(kd, posd)
+    out = torch.full(q.shape, float("nan"), dtype=out_dtype or q.dtype, device=DEV)
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    old = os.environ.get("ATTN_GB300_FORCE_SIMT")
+    os.environ["ATTN_GB300_FORCE_SIMT"] = "1" if simt else "0"
+    try:
+        atc.attn_prefill(qd, kd, vd, out, lse, cud, posd, max(lens), cu_k=cud, k_pos=posd, h_lo=h_lo, h_hi=h_hi,
+                         causal=causal)
+        atc.attn_device_status()
+    finally:
+        if old is None:
+            del os.environ["ATTN_GB300_FORCE_SIMT"]
+        else:
+            os.environ["ATTN_GB300_FORCE_SIMT"] = old
+    return out, lse
+
+
+def _oracle_prefill(q, k, v, pos, cu, lens, scale, causal=True, h_lo=0, h_hi=None):
+    qr, kr = rotated_bf16(q, pos), rotated_bf16(k, pos)
+    return oracle.attention(qr, seq_ids(lens), pos, kr, synth.as_f64(v), cu, pos, scale, causal=causal,
+                            h_lo=h_lo, h_hi=h_hi)
+
+
+CASES = [
+    ([300], 16, 2, [0]),                 # several tiles and a ragged tail
+    ([1, 129, 513, 256], 16, 2, [5, 0, 100000, 7]),  # varlen batch, offsets, 1-token sequence
+    ([700], 64, 8, [0]),                 # the 64/8 head layout
+    ([255, 257], 8, 8, [0, 40]),         # MHA, tile edges off by one
+]
+
+
+@pytest.mark.parametrize("lens,hq,hkv,starts", CASES)
+def test_prefill_tc_causal_matches_oracle(lens, hq, hkv, starts):
+    q, k, v, pos, cu = _bf16_case(lens, hq, hkv, starts, 200 + hq + len(lens))
+    out, lse = _run_prefill(q, k, v, pos, cu, lens)
+    want_o, want_l = _oracle_prefill(q, k, v, pos, cu, lens, 128 ** -0.5)
+    check(out, lse, want_o, want_l, what=f"tc causal {lens}")
+
+
+def test_prefill_tc_non_causal_and_fp32_output():
+    lens = [200, 333]
+    q, k, v, pos, cu = _bf16_case(lens, 16, 2, [0, 0], 301)
+    out, lse = _run_prefill(q, k, v, pos, cu, lens, causal=False, out_dtype=torch.float32)
+    want_o, want_l = _oracle_prefill(q, k, v, pos, cu, lens, 128 ** -0.5, causal=False)
+    check(out, lse, want_o, want_l, what="tc non-causal fp32 out")
+
+
+def test_prefill_simt_bf16_matches_oracle():
+    lens = [150, 77]
+    q, k, v, pos, cu = _bf16_case(lens, 16, 2, [0, 3], 302)
+    out, lse = _run_prefill(q, k, v, pos, cu, lens, simt=True)
+    want_o, want_l = _oracle_prefill(q, k, v, pos, cu, lens, 128 ** -0.5)
+    check(out, lse, want_o, want_l, what="simt bf16")
+
+
+def test_prefill_tc_head_slices_are_bit_identical_to_full_call():
+    lens = [600]
+    q, k, v, pos, cu = _bf16_case(lens, 64, 8, [0], 303)
+    full_o, full_l = _run_prefill(q, k, v, pos, cu, lens)
+    for lo, hi in ((16, 32), (0, 8), (56, 64)):
+        o, l = _run_prefill(q, k, v, pos, cu, lens, h_lo=lo, h_hi=hi)
+        assert torch.equal(o[:, lo:hi], full_o[:, lo:hi])
+        assert torch.equal(l[:, lo:hi], full_l[:, lo:hi])
+        assert torch.isnan(o[:, :lo].float()).all() and torch.isnan(o[:, hi:].float()).all()
+
+
+def test_prefill_fully_masked_rows_give_zero_and_minus_inf():
+    """Queries at positions 0..9 against keys at positions 50..249: nothing visible."""
+    d, hq, hkv = 128, 8, 1
+    q = synth.randn((10, hq, d), 304, 0.7).to(DEV)
+    k = synth.randn((200, hkv, d), 305, 0.7).to(DEV)
+    v = synth.randn((200, hkv, d), 306, 0.7).to(DEV)
+    qpos = torch.arange(10, dtype=torch.int32, device=DEV)
+    kpos = torch.arange(50, 250, dtype=torch.int32, device=DEV)
+    out, lse = atc.prefill(q, k, v, torch.tensor([0, 10], dtype=torch.int32, device=DEV), qpos, 10,
+                           cu_k=torch.tensor([0, 200], dtype=torch.int32, device=DEV), k_pos=kpos)
+    atc.attn_device_status()
+    assert torch.all(out == 0) and torch.all(lse == -math.inf)
+
+
+def test_prefill_zero_length_sequence_in_batch():
+    lens = [0, 130, 0]
+    q, k, v, pos, cu = _bf16_case(lens, 8, 1, [0, 0, 0], 307)
+    out, lse = _run_prefill(q, k, v, pos, cu, lens)
+    want_o, want_l = _oracle_prefill(q, k, v, pos, cu, lens, 128 ** -0.5)
+    check(out, lse, want_o, want_l, what="zero-length sequences")
+
+
+# ------------------------------------------------------------------ chunked prefill over a paged prefix
+
+def _chunked_case(prefix, chunk, B, hq, hkv, seed, d=128):
+    table, num_pages = synth.shuffled_page_table([prefix] * B, seed)
+    kc = synth.randn((hkv, num_pages, 64, d), seed + 1, 0.7071)
+    vc = synth.randn((hkv, num_pages, 64, d), seed + 2, 0.7071)
+    q = synth.randn((B * chunk, hq, d), seed + 3, 0.7071)
+    k = synth.randn((B * chunk, hkv, d), seed + 4, 0.7071)
+    v = synth.randn((B * chunk, hkv, d), seed + 5, 0.7071)
+    return table, num_pages, kc, vc, q, k, v
+
+
+def _chunked_gpu(prefix, chunk, B, table, num_pages, kc, vc, q, k, v):
+    qpos = torch.from_numpy(synth.positions([chunk] * B, [prefix] * B)).to(DEV)
+    cu = torch.from_numpy(synth.cu_seqlens([chunk] * B)).to(DEV)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    atc.rope_apply(qd, qpos)
+    atc.rope_apply(kd, qpos)
+    T, hq, d = q.shape
+    po = torch.empty((2, T, hq, d), dtype=torch.float32, device=DEV)
+    pl = torch.empty((2, T, hq), dtype=torch.float32, device=DEV)
+    atc.attn_prefill(qd, kc.to(DEV), vc.to(DEV), po[0], pl[0], cu, qpos, chunk,
+                     page_table=torch.from_numpy(table).to(DEV),
+                     k_lens=torch.full((B,), prefix, dtype=torch.int32, device=DEV), num_pages=num_pages)
+    atc.attn_prefill(qd, kd, vd, po[1], pl[1], cu, qpos, chunk, cu_k=cu, k_pos=qpos)
+    out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((T, hq), dtype=torch.float32, device=DEV)
+    atc.attn_lse_merge(po, pl, out, lse)
+    atc.attn_device_status()
+    return out, lse
+
+
+def _chunked_oracle(prefix, chunk, B, table, num_pages, kc, vc, q, k, v, rows=None):
+    """Oracle: one causal attention of each chunk query over [prefix ; chunk] keys,
+    the prefix gathered from the paged cache in logical order."""
+    hkv = kc.shape[0]
+    qpos = synth.positions([chunk] * B, [prefix] * B)
+    qr = rotated_bf16(q, qpos)
+    kr = rotated_bf16(k, qpos)
+    kcf, vcf = synth.as_f64(kc), synth.as_f64(vc)
+    keys, vals, kpos = [], [], []
+    for b in range(B):
+        kb = np.stack([oracle.gather_pages(kcf, table, num_pages, g, b, prefix) for g in range(hkv)], 1)
+        vb = np.stack([oracle.gather_pages(vcf, table, num_pages, g, b, prefix) for g in range(hkv)], 1)
+        keys += [kb, kr[b * chunk:(b + 1) * chunk]]
+        vals += [vb, synth.as_f64(v[b * chunk:(b + 1) * chunk])]
+        kpos += [np.arange(prefix, dtype=np.int32), qpos[b * chunk:(b + 1) * chunk]]
+    K, V, KP = np.concatenate(keys), np.concatenate(vals), np.concatenate(kpos)
+    cu_k = synth.cu_seqlens([prefix + chunk] * B)
+    sel = np.arange(B * chunk) if rows is None else rows
+    o, l = oracle.attention(qr[sel], seq_ids([chunk] * B)[sel], qpos[sel], K, V, cu_k, KP, 128 ** -0.5)
+    return o, l, sel
+
+
+def test_chunked_prefill_over_shuffled_paged_prefix_matches_oracle():
+    prefix, chunk, B, hq, hkv = 1000, 200, 2, 16, 2
+    case = _chunked_case(prefix, chunk, B, hq, hkv, 400)
+    out, lse = _chunked_gpu(prefix, chunk, B, *case)
+    o, l, _ = _chunked_oracle(prefix, chunk, B, *case)
+    check(out, lse, o, l, what="chunked paged prefill")
+
+
+def test_paged_prefill_invariant_under_page_permutation():
+    """Moving the prefix pages to other physical slots changes no output bit."""
+    prefix, chunk, B, hq, hkv = 640, 130, 2, 8, 1
+    table, num_pages, kc, vc, q, k, v = _chunked_case(prefix, chunk, B, hq, hkv, 401)
+    out1, lse1 = _chunked_gpu(prefix, chunk, B, table, num_pages, kc, vc, q, k, v)
+    perm = np.random.default_rng(3).permutation(num_pages)
+    inv = np.argsort(perm)
+    table2 = np.where(table >= 0, inv[np.maximum(table, 0)], -1).astype(np.int32)
+    out2, lse2 = _chunked_gpu(prefix, chunk, B, table2, num_pages, kc[:, perm].contiguous(),
+                              vc[:, perm].contiguous(), q, k, v)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+# ------------------------------------------------------------------ decode
+
+def _decode(wl, inp, splits):
+    g = {k: (t.to(DEV) if torch.is_tensor(t) else t) for k, t in inp.items()}
+    q = g["q"].clone()
+    atc.rope_apply(q, g["q_pos"])
+    po, pl = atc.decode_workspace(wl.batch, wl.hq, splits, wl.d, DEV)
+    out = torch.empty((wl.batch, wl.hq, wl.d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((wl.batch, wl.hq), dtype=torch.float32, device=DEV)
+    atc.attn_decode_paged(q, g["k_cache"], g["v_cache"], g["page_table"], g["ctx_lens"], splits, po, pl, out, lse)
+    atc.attn_device_status()
+    return out, lse, po, pl
+
+
+def _decode_oracle(wl, inp):
+    qr = rotated_bf16(inp["q"], inp["q_pos"].numpy())
+    return oracle.decode_paged(qr, synth.as_f64(inp["k_cache"]), synth.as_f64(inp["v_cache"]),
+                               inp["page_table"].numpy(), inp["ctx_lens"].numpy(), inp["num_pages"], wl.scale)
+
+
+@pytest.mark.parametrize("splits", [1, 4, 16])
+def test_decode_matches_oracle(splits):
+    ctx = [1, 63, 64, 65, 700, 2049, 130]
+    wl = synth.Decode("decode small", batch=len(ctx), ctx_lo=0, ctx_hi=0, hq=16, hkv=2, d=128, splits=splits,
+                      seed=500 + splits, ctx_fixed=ctx)
+    inp = wl.make()
+    out, lse, _, _ = _decode(wl, inp, splits)
+    want_o, want_l = _decode_oracle(wl, inp)
+    check(out, lse, want_o, want_l, what=f"decode splits={splits}")
+
+
+def test_decode_64_8_heads_zero_context_request():
+    ctx = [0, 3000, 5]
+    wl = synth.Decode("decode 64/8", batch=3, ctx_lo=0, ctx_hi=0, hq=64, hkv=8, d=128, splits=16, seed=510,
+                      ctx_fixed=ctx)
+    inp = wl.make()
+    out, lse, _, _ = _decode(wl, inp, 16)
+    want_o, want_l = _decode_oracle(wl, inp)
+    check(out, lse, want_o, want_l, what="decode 64/8")
+    assert torch.all(out[0] == 0) and torch.all(lse[0] == -math.inf)
+
+
+def test_decode_invariant_under_page_permutation_and_request_order():
+    """Ulysses page, 3.5, third check: reusing the cache with pages moved and the
+    batch reordered changes no output bit."""
+    ctx = [100, 1000, 64, 333]
+    wl = synth.Decode("decode perm", batch=4, ctx_lo=0, ctx_hi=0, hq=16, hkv=2, d=128, splits=4, seed=520,
+                      ctx_fixed=ctx)
+    inp = wl.make()
+    out, lse, _, _ = _decode(wl, inp, 4)
+    n = inp["num_pages"]
+    perm = np.random.default_rng(2).permutation(n)
+    inv = np.argsort(perm)
+    t = inp["page_table"].numpy()
+    inp2 = dict(inp)
+    inp2["k_cache"] = inp["k_cache"][:, perm].contiguous()
+    inp2["v_cache"] = inp["v_cache"][:, perm].contiguous()
+    inp2["page_table"] = torch.from_numpy(np.where(t >= 0, inv[np.maximum(t, 0)], -1).astype(np.int32))
+    out2, lse2, _, _ = _decode(wl, inp2, 4)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    order = [2, 0, 3, 1]
+    inp3 = dict(inp)
+    for key in ("q", "page_table", "ctx_lens", "q_pos"):
+        inp3[key] = inp[key][order].contiguous()
+    out3, lse3, _, _ = _decode(wl, inp3, 4)
+    assert torch.equal(out3, out[order]) and torch.equal(lse3, lse[order])
+
+
+def test_decode_bad_page_id_is_reported_not_faulted():
+    """A page-table entry outside the cache is caught on the device: the kernel
+    reads page 0 instead, records the fault, and the host reports it."""
+    ctx = [200]
+    wl = synth.Decode("decode bad page", batch=1, ctx_lo=0, ctx_hi=0, hq=8, hkv=1, d=128, splits=2, seed=530,
+                      ctx_fixed=ctx)
+    inp = wl.make()
+    inp["page_table"] = inp["page_table"].clone()
+    inp["page_table"][0, 1] = inp["num_pages"] + 5
+    g = {k: (t.to(DEV) if torch.is_tensor(t) else t) for k, t in inp.items()}
+    po, pl = atc.decode_workspace(1, 8, 2, 128, DEV)
+    atc.attn_decode_paged(g["q"], g["k_cache"], g["v_cache"], g["page_table"], g["ctx_lens"], 2, po, pl)
+    with pytest.raises(atc.AttnError) as e:
+        atc.attn_device_status(clear=True)
+    assert e.value.status == 6
+    atc.attn_device_status(clear=True)  # cleared
