@@ -16,6 +16,8 @@
 //    (M = 128, N = 128, K = 16 per instruction, bf16 in, fp32 accumulate),
 //    then O_t += P_t V_j into a second TMEM accumulator.  tcgen05.commit
 //    arrives on mbarriers when the tensor core is done.
+//  * Warps 10-11 only complete the third warpgroup (setmaxnreg acts per
+//    warpgroup).
 //  * Warps 0-3 (tile A) and 4-7 (tile B) are the softmax warpgroups: thread r
 //    of a warpgroup owns query row r (TMEM lane r), loads its 128 scores with
 //    tcgen05.ld, applies the absolute-position causal mask (Ulysses page,
@@ -49,8 +51,14 @@ constexpr int OFF_P = OFF_KV + NSLOT * TILE;
 constexpr int OFF_BAR = OFF_P + 2 * TILE;
 constexpr int NBAR = 16;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 32 + 1024;
-constexpr int NTHREADS = 320;
+// 12 warps = 3 warpgroups.  The register file is split across the SM's four
+// sub-partitions, so 3 warps per sub-partition launch with at most 168
+// registers each; right after set-up the producer warpgroup shrinks to 56 and
+// the two softmax warpgroups grow to 224 (256*224 + 128*56 = 384*168).
+constexpr int NTHREADS = 384;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 224, REGS_PRODUCER = 56;
+static_assert(256 * REGS_SOFTMAX + 128 * REGS_PRODUCER <= NTHREADS * REGS_LAUNCH, "register split exceeds launch");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);    // P K-major, V MN-major
@@ -92,7 +100,7 @@ __device__ int upper_bound_pos(const int32_t* k_pos, int n, int qp) {
 }
 
 template <bool PAGED>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -164,7 +172,9 @@ __global__ void __maxnreg__(200)
   const int nkv_a = sm.nkv[0], nkv_b = sm.nkv[1];
   const int nkv = max(nkv_a, nkv_b);
 
-  if (warp == WARP_TMA) {
+  if (warp >= 8) {
+   regs_dec<REGS_PRODUCER>();
+   if (warp == WARP_TMA) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nkv > 0) {
       tma_prefetch_desc(&tm_q);
@@ -255,8 +265,10 @@ __global__ void __maxnreg__(200)
         tc_commit(&sm.kv_empty[slotV]);
       }
     }
+   }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
+    regs_inc<REGS_SOFTMAX>();
     const int t = warp >> 2, wq = warp & 3;
     const int row = wq * 32 + lane;
     const int rq = q0 + t * BM + row;  // row index inside the sequence
@@ -430,6 +442,19 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, con
     attr_set[paged][dev] = true;
   }
   if (a.max_seqlen_q == 0 || a.batch == 0 || a.h_hi == a.h_lo) return cudaSuccess;
+  {
+    // The in-kernel register split assumes exactly REGS_LAUNCH registers per
+    // thread at launch; with fewer, setmaxnreg.inc would wait forever.
+    static int regs[2][64] = {};
+    if (dev < 64 && regs[paged][dev] == 0) {
+      cudaFuncAttributes fa;
+      cudaError_t e = paged ? cudaFuncGetAttributes(&fa, tc::prefill_tc_kernel<true>)
+                            : cudaFuncGetAttributes(&fa, tc::prefill_tc_kernel<false>);
+      if (e != cudaSuccess) return e;
+      regs[paged][dev] = fa.numRegs;
+    }
+    if (dev >= 64 || regs[paged][dev] != tc::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
+  }
   tc::Params p;
   p.cu_q = a.cu_q;
   p.q_pos = a.q_pos;
