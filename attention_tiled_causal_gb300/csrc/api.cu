@@ -115,6 +115,10 @@ bool force_simt() {
 
 }  // namespace
 
+namespace attn {
+int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace attn
+
 extern "C" {
 
 const char* attn_last_error(void) { return g_msg; }

@@ -163,6 +163,34 @@ ATTN_API int attn_decode_paged(const void *q, const void *k_cache, const void *v
                       float *lse, void *stream);
 
 /*
+ * attn_decode_paged_noalloc -- attn_decode_paged without a caller workspace.
+ *
+ * The pages have no counterpart for this call: it exists for callers that
+ * cannot allocate device memory -- e.g. a serving engine that gives all free
+ * HBM to its KV-cache pool at start-up, a plugin inside a framework whose
+ * caching allocator owns the device memory, or a latency-critical path where
+ * cudaMalloc/cudaFree would synchronise the device.  It computes exactly what
+ * attn_decode_paged computes, with the split partials kept in a scratch array
+ * the library holds statically on each device (16.1 MiB, held until exit).
+ * It calls no allocator.
+ *
+ *  Arguments as attn_decode_paged, minus part_out/part_lse; out must not be
+ *  NULL.  batch * num_q_heads * num_splits must be <= 32768 (e.g. 32 requests
+ *  x 64 heads x 16 splits), else ATTN_ERR_ARG and nothing is launched.
+ *  All calls on a device share the scratch and it keeps the last call's
+ *  contents (no part of it needs to start at zero); calls that overlap on the
+ *  GPU race on it, so serialise them.  The first call on a device looks up the
+ *  scratch's device address (cudaGetSymbolAddress) with that device current;
+ *  make that first call before any stream capture.
+ */
+ATTN_API int attn_decode_paged_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                       const int32_t *page_table, const int32_t *ctx_lens, int batch,
+                                       int max_pages, int page_size, int64_t num_pages,
+                                       int num_q_heads, int num_kv_heads, int head_dim,
+                                       int num_splits, float scale, void *out,
+                                       attn_dtype_t out_dtype, float *lse, void *stream);
+
+/*
  * attn_lse_merge -- combine partial attention results over disjoint key sets.
  *
  *   LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s
