@@ -74,6 +74,7 @@ struct Smem {
   uint64_t* o_done;    // [2]  MMA -> softmax: O_t += P_t V_j finished
   uint32_t* tmem_slot;
   int* nkv;            // [2]  K/V tiles each query tile needs
+  int* nfull;          // [2]  leading K/V tiles every row of the query tile sees in full
 };
 
 struct Params {
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   sm.o_done = bars + 14;
   sm.tmem_slot = (uint32_t*)(bars + NBAR);
   sm.nkv = (int*)(sm.tmem_slot + 4);
+  sm.nfull = sm.nkv + 2;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -149,19 +151,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.kv_empty[i], 1);
     }
     fence_mbar_init();
-    // K/V tiles needed by each query tile: keys up to the tile's last position.
+    // Per query tile: K/V tiles needed (keys up to the tile's last position) and
+    // leading tiles visible in full to every row (keys up to its first position);
+    // only tiles in between need the per-element mask.
     for (int t = 0; t < 2; ++t) {
       const int r0 = q0 + t * BM;
-      int nk = 0;
+      int nk = 0, nk_first = 0;
       if (r0 < Sq) {
         if (!p.causal) {
-          nk = Sk;
+          nk = nk_first = Sk;
         } else {
           const int qp_last = p.q_pos[q_beg + min(r0 + BM, Sq) - 1];
+          const int qp_first = p.q_pos[q_beg + r0];
           nk = PAGED ? max(0, min(Sk, qp_last + 1)) : upper_bound_pos(p.k_pos + k_beg, Sk, qp_last);
+          nk_first = PAGED ? max(0, min(Sk, qp_first + 1)) : upper_bound_pos(p.k_pos + k_beg, Sk, qp_first);
         }
       }
       sm.nkv[t] = (nk + BN - 1) / BN;
+      sm.nfull[t] = nk_first / BN;
     }
   }
   if (warp == WARP_MMA) tmem_alloc(sm.tmem_slot, TMEM_COLS);
@@ -217,51 +224,63 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
+    // Issue order per K/V tile j:  S_A(j), PV_B(j-1), S_B(j), PV_A(j).  Each
+    // softmax then has a full two-MMA window (S of the other tile and one PV)
+    // before its own PV is due, and the previous PV of the same tile always
+    // precedes the next S, so the P buffer it reads is free by then.
     if (lane == 0 && nkv > 0) {
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
         if (sm.nkv[t] > 0) ok = mbar_wait(&sm.q_full[t], 0, p.err, DEV_TIMEOUT_MMA);
       tc_fence_after();
       const uint32_t sQ = smem_u32(smem + OFF_Q), sKV = smem_u32(smem + OFF_KV), sP = smem_u32(smem + OFF_P);
+      auto issue_s = [&](int t, int j, int slotK) -> bool {
+        if (j > 0) {
+          if (!mbar_wait(&sm.s_free[t], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA)) return false;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t a = sQ + t * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
+          const uint32_t bb = sKV + slotK * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
+          tc_mma_bf16(tmem + t * BN, sdesc_sw128(a, 16, 1024), sdesc_sw128(bb, 16, 1024), IDESC_QK, kk > 0);
+        }
+        tc_commit(&sm.s_full[t]);
+        return true;
+      };
+      auto issue_pv = [&](int t, int j, int slotV) -> bool {
+        if (!mbar_wait(&sm.p_full[t], j & 1, p.err, DEV_TIMEOUT_MMA)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint32_t a = sP + t * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
+          const uint32_t bb = sKV + slotV * TILE + kk * 2048;  // 16 tokens = two 8-row swizzle atoms
+          tc_mma_bf16(tmem + 2 * BN + t * D, sdesc_sw128(a, 16, 1024), sdesc_sw128(bb, HALF, 1024), IDESC_PV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&sm.o_done[t]);
+        return true;
+      };
       for (int j = 0; j < nkv && ok; ++j) {
-        // S_t = Q_t K_j^T
         const int iK = 2 * j, slotK = iK % NSLOT;
+        const int iV = 2 * j + 1, slotV = iV % NSLOT;
         if (!(ok = mbar_wait(&sm.kv_full[slotK], (iK / NSLOT) & 1, p.err, DEV_TIMEOUT_MMA))) break;
         tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if (j >= sm.nkv[t]) continue;
-          if (j > 0) {
-            if (!(ok = mbar_wait(&sm.s_free[t], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA))) break;
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t a = sQ + t * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
-            const uint32_t bb = sKV + slotK * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
-            tc_mma_bf16(tmem + t * BN, sdesc_sw128(a, 16, 1024), sdesc_sw128(bb, 16, 1024), IDESC_QK, kk > 0);
-          }
-          tc_commit(&sm.s_full[t]);
+        if (j < nkv_a && !(ok = issue_s(0, j, slotK))) break;
+        if (j > 0) {
+          const int slotVp = (iV - 2) % NSLOT;
+          if (j - 1 < nkv_b && !(ok = issue_pv(1, j - 1, slotVp))) break;
+          tc_commit(&sm.kv_empty[slotVp]);  // V_{j-1} consumed
         }
-        if (!ok) break;
-        tc_commit(&sm.kv_empty[slotK]);
-        // O_t += P_t V_j
-        const int iV = 2 * j + 1, slotV = iV % NSLOT;
+        if (j < nkv_b && !(ok = issue_s(1, j, slotK))) break;
+        tc_commit(&sm.kv_empty[slotK]);  // K_j consumed
         if (!(ok = mbar_wait(&sm.kv_full[slotV], (iV / NSLOT) & 1, p.err, DEV_TIMEOUT_MMA))) break;
         tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if (j >= sm.nkv[t]) continue;
-          if (!(ok = mbar_wait(&sm.p_full[t], j & 1, p.err, DEV_TIMEOUT_MMA))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t a = sP + t * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
-            const uint32_t bb = sKV + slotV * TILE + kk * 2048;  // 16 tokens = two 8-row swizzle atoms
-            tc_mma_bf16(tmem + 2 * BN + t * D, sdesc_sw128(a, 16, 1024), sdesc_sw128(bb, HALF, 1024), IDESC_PV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(&sm.o_done[t]);
-        }
-        if (!ok) break;
+        if (j < nkv_a && !(ok = issue_pv(0, j, slotV))) break;
+      }
+      if (ok) {
+        const int j = nkv - 1, slotV = (2 * j + 1) % NSLOT;
+        if (j < nkv_b) ok = issue_pv(1, j, slotV);
         tc_commit(&sm.kv_empty[slotV]);
       }
     }
@@ -275,12 +294,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool rv = rq < Sq;
     const int qp = rv ? p.q_pos[q_beg + rq] : 0;
     const int nkv_t = sm.nkv[t];
+    const int nfull_t = sm.nfull[t];
     const float sl2 = p.scale * 1.4426950408889634f;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * BN;
     const uint32_t tO = tmem + lane_base + 2 * BN + t * D;
-    uint8_t* sP = smem + OFF_P + t * TILE;
-    uint8_t* prow = sP + (row >> 3) * 1024 + (row & 7) * 128;
+    uint8_t* prow = smem + OFF_P + t * TILE + (row >> 3) * 1024 + (row & 7) * 128;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
 
@@ -288,26 +307,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, p.err, DEV_TIMEOUT_SOFTMAX));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[4][32];
+      float s[128];
+      {
+        uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-      tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+      }
       tc_fence_before();
       mbar_arrive(&sm.s_free[t]);
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
-      // causal mask by absolute position; keys past the sequence; rows past it
-      const int key0 = j * BN;
-      bool need_mask = !rv || key0 + BN > Sk;
-      if (!need_mask && p.causal) {
-        const int last_kp = PAGED ? key0 + BN - 1 : __ldg(p.k_pos + k_beg + key0 + BN - 1);
-        need_mask = last_kp > qp;
-      }
-      if (need_mask) {
+      // Causal mask by absolute position, and keys past the sequence: only the
+      // tiles from nfull_t on (the diagonal band and a ragged last tile).  Rows
+      // past the sequence compute values that are never stored.
+      if (j >= nfull_t) {
+        const int key0 = j * BN;
         if (PAGED) {  // cached token j sits at position j: one bound per row
-          const int lim = !rv ? -1 : (p.causal ? min(qp, Sk - 1) : Sk - 1) - key0;
+          const int lim = (p.causal ? min(qp, Sk - 1) : Sk - 1) - key0;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c > lim) s[c] = -INFINITY;
@@ -315,15 +333,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int kj = key0 + c;
-            bool vis = rv && kj < Sk;
+            bool vis = kj < Sk;
             if (vis && p.causal) vis = __ldg(p.k_pos + k_beg + kj) <= qp;
             if (!vis) s[c] = -INFINITY;
           }
         }
       }
-      float mt = -INFINITY;
+      // row max as a tree (independent chains)
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mt = fmaxf(mt, s[c]);
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m_ref, mt);
       const bool grow = (m_new - m_ref) * sl2 > kRescaleLog2;  // false when both are -inf
       const bool any_grow = __any_sync(0xffffffffu, grow);
@@ -334,30 +357,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         m_ref = m_new;
       }
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float pv = fast_exp2(fmaf(s[c], sl2, -mb));
-        s[c] = pv;
-        rs += pv;
-      }
-      l += rs;
 
-      // P_t and O_t are free once the previous O_t += P_t V_{j-1} finished.
+      // P_t (and O_t) are free once O_t += P_t V_{j-1} finished; in the issue
+      // order above that MMA precedes S_t(j), so this wait is already satisfied.
       if (j > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], (j - 1) & 1, p.err, DEV_TIMEOUT_SOFTMAX));
         if (!ok) break;
         tc_fence_after();
       }
+      // P = exp2(S * scale*log2e - m*scale*log2e), bf16, into the swizzled K-major tile
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int c8 = 0; c8 < 16; ++c8) {
+        float e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          e[i] = fast_exp2(fmaf(s[c8 * 8 + i], sl2, -mb));
+          acc[i] += e[i];
+        }
         uint4 v;
-        v.x = pack_bf16x2(s[c8 * 8 + 0], s[c8 * 8 + 1]);
-        v.y = pack_bf16x2(s[c8 * 8 + 2], s[c8 * 8 + 3]);
-        v.z = pack_bf16x2(s[c8 * 8 + 4], s[c8 * 8 + 5]);
-        v.w = pack_bf16x2(s[c8 * 8 + 6], s[c8 * 8 + 7]);
+        v.x = pack_bf16x2(e[0], e[1]);
+        v.y = pack_bf16x2(e[2], e[3]);
+        v.z = pack_bf16x2(e[4], e[5]);
+        v.w = pack_bf16x2(e[6], e[7]);
         *reinterpret_cast<uint4*>(prow + (c8 >> 3) * HALF + (((c8 & 7) ^ (row & 7)) << 4)) = v;
       }
+      l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       if (any_grow && j > 0) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
