@@ -16,8 +16,7 @@
 //    (M = 128, N = 128, K = 16 per instruction, bf16 in, fp32 accumulate),
 //    then O_t += P_t V_j into a second TMEM accumulator.  tcgen05.commit
 //    arrives on mbarriers when the tensor core is done.
-//  * Warps 10-11 only complete the third warpgroup (setmaxnreg acts per
-//    warpgroup).
+//  * Warps 10-11 idle (the block is three whole warpgroups).
 //  * Warps 0-3 (tile A) and 4-7 (tile B) are the softmax warpgroups: thread r
 //    of a warpgroup owns query row r (TMEM lane r), loads its 128 scores with
 //    tcgen05.ld, applies the absolute-position causal mask (Ulysses page,
@@ -38,6 +37,14 @@
 #include "common.cuh"
 #include "kernels.h"
 
+// Timeline hook: expands to nothing in the library build; a profiling build
+// may define it to record clock64() stamps of pipeline events.
+#ifndef ATTN_TC_TRACE
+#define ATTN_TC_TRACE(event, j) \
+  do {                           \
+  } while (0)
+#endif
+
 namespace attn {
 namespace tc {
 
@@ -53,12 +60,10 @@ constexpr int NBAR = 16;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 32 + 1024;
 // 12 warps = 3 warpgroups.  The register file is split across the SM's four
 // sub-partitions, so 3 warps per sub-partition launch with at most 168
-// registers each; right after set-up the producer warpgroup shrinks to 56 and
-// the two softmax warpgroups grow to 224 (256*224 + 128*56 = 384*168).
+// registers each; every role fits in that without spilling.
 constexpr int NTHREADS = 384;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
-constexpr int REGS_LAUNCH = 168, REGS_SOFTMAX = 224, REGS_PRODUCER = 56;
-static_assert(256 * REGS_SOFTMAX + 128 * REGS_PRODUCER <= NTHREADS * REGS_LAUNCH, "register split exceeds launch");
+constexpr int REGS_LAUNCH = 168;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);    // P K-major, V MN-major
@@ -98,6 +103,25 @@ __device__ int upper_bound_pos(const int32_t* k_pos, int n, int qp) {
       hi = mid;
   }
   return lo;
+}
+
+// S_t = Q_t K_j^T: eight k-steps of 16 over head_dim, both operands K-major.
+__device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint64_t a0, uint64_t b0) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t o = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
+    tc_mma_bf16(d_tmem, a0 + o, b0 + o, IDESC_QK, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O_t (+)= P_t V_j: eight k-steps of 16 tokens; P K-major, V MN-major (16
+// tokens = two 8-row swizzle atoms = 2048 bytes).
+__device__ __forceinline__ void mma_values(uint32_t d_tmem, uint64_t a0, uint64_t b0, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    const uint64_t o = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
+    tc_mma_bf16(d_tmem, a0 + o, b0 + (uint64_t)(kk * (2048 >> 4)), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
 template <bool PAGED>
@@ -180,7 +204,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int nkv = max(nkv_a, nkv_b);
 
   if (warp >= 8) {
-   regs_dec<REGS_PRODUCER>();
    if (warp == WARP_TMA) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nkv > 0) {
@@ -200,6 +223,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (i >= NSLOT && !mbar_wait(&sm.kv_empty[slot], ((i / NSLOT) - 1) & 1, p.err, DEV_TIMEOUT_TMA)) break;
         const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
         uint8_t* dst = smem + OFF_KV + slot * TILE;
+        ATTN_TC_TRACE(20 + (i & 1), j);
         mbar_arrive_expect_tx(&sm.kv_full[slot], TILE);
         if (!PAGED) {
           for (int hf = 0; hf < 2; ++hf) tma_load_3d(dst + hf * HALF, tm, &sm.kv_full[slot], hf * 64, g, k_beg + j * BN);
@@ -233,61 +257,83 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int t = 0; t < 2 && ok; ++t)
         if (sm.nkv[t] > 0) ok = mbar_wait(&sm.q_full[t], 0, p.err, DEV_TIMEOUT_MMA);
       tc_fence_after();
-      const uint32_t sQ = smem_u32(smem + OFF_Q), sKV = smem_u32(smem + OFF_KV), sP = smem_u32(smem + OFF_P);
-      auto issue_s = [&](int t, int j, int slotK) -> bool {
-        if (j > 0) {
-          if (!mbar_wait(&sm.s_free[t], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA)) return false;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t a = sQ + t * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
-          const uint32_t bb = sKV + slotK * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
-          tc_mma_bf16(tmem + t * BN, sdesc_sw128(a, 16, 1024), sdesc_sw128(bb, 16, 1024), IDESC_QK, kk > 0);
-        }
-        tc_commit(&sm.s_full[t]);
-        return true;
-      };
-      auto issue_pv = [&](int t, int j, int slotV) -> bool {
-        if (!mbar_wait(&sm.p_full[t], j & 1, p.err, DEV_TIMEOUT_MMA)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t a = sP + t * TILE + (kk >> 2) * HALF + (kk & 3) * 32;
-          const uint32_t bb = sKV + slotV * TILE + kk * 2048;  // 16 tokens = two 8-row swizzle atoms
-          tc_mma_bf16(tmem + 2 * BN + t * D, sdesc_sw128(a, 16, 1024), sdesc_sw128(bb, HALF, 1024), IDESC_PV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&sm.o_done[t]);
-        return true;
-      };
-      for (int j = 0; j < nkv && ok; ++j) {
+      ATTN_TC_TRACE(0, 0);
+      // Descriptors of every tile base; a k-step adds a constant byte offset
+      // (>> 4) to the 14-bit start-address field, which never carries out of it
+      // because shared-memory addresses stay below 256 KB.
+      const uint64_t dQ = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
+      const uint64_t dKV = sdesc_sw128(smem_u32(smem + OFF_KV), 16, 1024);
+      const uint64_t dP = sdesc_sw128(smem_u32(smem + OFF_P), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(smem + OFF_KV), HALF, 1024);
+      constexpr uint64_t kTile16 = TILE >> 4;
+      for (int j = 0; j < nkv; ++j) {
         const int iK = 2 * j, slotK = iK % NSLOT;
         const int iV = 2 * j + 1, slotV = iV % NSLOT;
         if (!(ok = mbar_wait(&sm.kv_full[slotK], (iK / NSLOT) & 1, p.err, DEV_TIMEOUT_MMA))) break;
         tc_fence_after();
-        if (j < nkv_a && !(ok = issue_s(0, j, slotK))) break;
-        if (j > 0) {
+        ATTN_TC_TRACE(1, j);
+        if (j < nkv_a) {  // S_A(j)
+          if (j > 0) {
+            if (!(ok = mbar_wait(&sm.s_free[0], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA))) break;
+            tc_fence_after();
+          }
+          ATTN_TC_TRACE(22, j);
+          mma_scores(tmem, dQ, dKV + slotK * kTile16);
+          tc_commit(&sm.s_full[0]);
+          ATTN_TC_TRACE(2, j);
+        }
+        if (j > 0) {  // PV_B(j-1)
           const int slotVp = (iV - 2) % NSLOT;
-          if (j - 1 < nkv_b && !(ok = issue_pv(1, j - 1, slotVp))) break;
+          if (j - 1 < nkv_b) {
+            if (!(ok = mbar_wait(&sm.p_full[1], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA))) break;
+            tc_fence_after();
+            ATTN_TC_TRACE(3, j - 1);
+            ATTN_TC_TRACE(25, j - 1);
+            mma_values(tmem + 2 * BN + D, dP + kTile16, dV + slotVp * kTile16, j - 1 > 0);
+            tc_commit(&sm.o_done[1]);
+            ATTN_TC_TRACE(4, j - 1);
+          }
           tc_commit(&sm.kv_empty[slotVp]);  // V_{j-1} consumed
         }
-        if (j < nkv_b && !(ok = issue_s(1, j, slotK))) break;
+        if (j < nkv_b) {  // S_B(j)
+          if (j > 0) {
+            if (!(ok = mbar_wait(&sm.s_free[1], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA))) break;
+            tc_fence_after();
+          }
+          ATTN_TC_TRACE(23, j);
+          mma_scores(tmem + BN, dQ + kTile16, dKV + slotK * kTile16);
+          tc_commit(&sm.s_full[1]);
+          ATTN_TC_TRACE(5, j);
+        }
         tc_commit(&sm.kv_empty[slotK]);  // K_j consumed
         if (!(ok = mbar_wait(&sm.kv_full[slotV], (iV / NSLOT) & 1, p.err, DEV_TIMEOUT_MMA))) break;
         tc_fence_after();
-        if (j < nkv_a && !(ok = issue_pv(0, j, slotV))) break;
+        ATTN_TC_TRACE(6, j);
+        if (j < nkv_a) {  // PV_A(j)
+          if (!(ok = mbar_wait(&sm.p_full[0], j & 1, p.err, DEV_TIMEOUT_MMA))) break;
+          tc_fence_after();
+          ATTN_TC_TRACE(7, j);
+          ATTN_TC_TRACE(24, j);
+          mma_values(tmem + 2 * BN, dP, dV + slotV * kTile16, j > 0);
+          tc_commit(&sm.o_done[0]);
+          ATTN_TC_TRACE(8, j);
+        }
       }
-      if (ok) {
+      if (ok) {  // PV_B of the last tile
         const int j = nkv - 1, slotV = (2 * j + 1) % NSLOT;
-        if (j < nkv_b) ok = issue_pv(1, j, slotV);
+        if (j < nkv_b) {
+          if ((ok = mbar_wait(&sm.p_full[1], j & 1, p.err, DEV_TIMEOUT_MMA))) {
+            tc_fence_after();
+            mma_values(tmem + 2 * BN + D, dP + kTile16, dV + slotV * kTile16, j > 0);
+            tc_commit(&sm.o_done[1]);
+          }
+        }
         tc_commit(&sm.kv_empty[slotV]);
       }
     }
    }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    regs_inc<REGS_SOFTMAX>();
     const int t = warp >> 2, wq = warp & 3;
     const int row = wq * 32 + lane;
     const int rq = q0 + t * BM + row;  // row index inside the sequence
@@ -307,6 +353,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, p.err, DEV_TIMEOUT_SOFTMAX));
       if (!ok) break;
       tc_fence_after();
+      if (row == 0) ATTN_TC_TRACE(10 + t, j);
       float s[128];
       {
         uint32_t sr[4][32];
@@ -318,6 +365,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(&sm.s_free[t]);
+      if (row == 0) ATTN_TC_TRACE(12 + t, j);
 
       // Causal mask by absolute position, and keys past the sequence: only the
       // tiles from nfull_t on (the diagonal band and a ragged last tile).  Rows
@@ -329,14 +377,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c > lim) s[c] = -INFINITY;
-        } else {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int kj = key0 + c;
-            bool vis = kj < Sk;
-            if (vis && p.causal) vis = __ldg(p.k_pos + k_beg + kj) <= qp;
-            if (!vis) s[c] = -INFINITY;
+        } else {  // positions are sorted: the visible keys of the tile are a prefix
+          const int n = min(BN, Sk - key0);
+          int lim = n - 1;
+          if (p.causal) {
+            const int32_t* kp = p.k_pos + k_beg + key0;
+            int lo = 0, hi = n;  // count of keys with position <= qp
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (__ldg(kp + mid) <= qp)
+                lo = mid + 1;
+              else
+                hi = mid;
+            }
+            lim = lo - 1;
           }
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > lim) s[c] = -INFINITY;
         }
       }
       // row max as a tree (independent chains)
@@ -357,6 +415,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         m_ref = m_new;
       }
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
+      if (row == 0) ATTN_TC_TRACE(14 + t, j);
 
       // P_t (and O_t) are free once O_t += P_t V_{j-1} finished; in the issue
       // order above that MMA precedes S_t(j), so this wait is already satisfied.
@@ -385,6 +444,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         *reinterpret_cast<uint4*>(prow + (c8 >> 3) * HALF + (((c8 & 7) ^ (row & 7)) << 4)) = v;
       }
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      if (row == 0) ATTN_TC_TRACE(16 + t, j);
       if (any_grow && j > 0) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -400,6 +460,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.p_full[t]);
+      if (row == 0) ATTN_TC_TRACE(18 + t, j);
     }
 
     // epilogue: O / l to global memory, LSE = scale * m + ln l
@@ -442,6 +503,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     if (rv && p.lse) p.lse[(int64_t)(q_beg + rq) * p.hq + h] = l > 0.f ? m_ref * p.scale + logf(l) : -INFINITY;
+    if (row == 0) ATTN_TC_TRACE(30 + t, 0);
   }
 
   tc_fence_before();
@@ -470,8 +532,8 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, con
   }
   if (a.max_seqlen_q == 0 || a.batch == 0 || a.h_hi == a.h_lo) return cudaSuccess;
   {
-    // The in-kernel register split assumes exactly REGS_LAUNCH registers per
-    // thread at launch; with fewer, setmaxnreg.inc would wait forever.
+    // 384 threads fit on an SM only at <= 168 registers per thread; check the
+    // compiled count so a toolchain change shows up as an error, not a failed launch.
     static int regs[2][64] = {};
     if (dev < 64 && regs[paged][dev] == 0) {
       cudaFuncAttributes fa;
@@ -480,7 +542,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, con
       if (e != cudaSuccess) return e;
       regs[paged][dev] = fa.numRegs;
     }
-    if (dev >= 64 || regs[paged][dev] != tc::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
+    if (dev >= 64 || regs[paged][dev] > tc::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
   }
   tc::Params p;
   p.cu_q = a.cu_q;
