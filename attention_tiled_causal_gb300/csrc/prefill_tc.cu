@@ -74,7 +74,7 @@ struct Smem {
   uint64_t* kv_full;   // [3]  TMA -> MMA: ring slot landed
   uint64_t* kv_empty;  // [3]  MMA -> TMA: ring slot consumed
   uint64_t* s_full;    // [2]  MMA -> softmax: S_t ready in TMEM
-  uint64_t* s_free;    // [2]  softmax -> MMA: S_t read out (128 arrivals)
+  uint64_t* s_free;    // [2]  softmax -> MMA: S_t read out of TMEM (128 arrivals)
   uint64_t* p_full;    // [2]  softmax -> MMA: P_t written, O_t rescaled (128 arrivals)
   uint64_t* o_done;    // [2]  MMA -> softmax: O_t += P_t V_j finished
   uint32_t* tmem_slot;
@@ -272,6 +272,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!(ok = mbar_wait(&sm.kv_full[slotK], (iK / NSLOT) & 1, p.err, DEV_TIMEOUT_MMA))) break;
         tc_fence_after();
         ATTN_TC_TRACE(1, j);
+        // S_t(j) overwrites S_t(j-1) in TMEM only after the softmax has
+        // signalled (s_free) that S_t(j-1) is in its registers.
         if (j < nkv_a) {  // S_A(j)
           if (j > 0) {
             if (!(ok = mbar_wait(&sm.s_free[0], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA))) break;
@@ -354,17 +356,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok) break;
       tc_fence_after();
       if (row == 0) ATTN_TC_TRACE(10 + t, j);
+      // Scores: two halves of 64 columns; the second load overlaps the first
+      // half's max.
+      // Scores: one row of S_t (128 fp32) per thread.
       float s[128];
+      float mx[8];
       {
         uint32_t sr[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
         tmem_wait_ld();
 #pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_regs_ready(sr[c]);
+#pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
       }
       tc_fence_before();
-      mbar_arrive(&sm.s_free[t]);
+      mbar_arrive(&sm.s_free[t]);  // S_t may now be overwritten by S_t(j+1)
+      if (j < nfull_t) {  // no mask on this tile: reduce the first half right away
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+#pragma unroll
+        for (int c = 24; c < 64; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+      }
       if (row == 0) ATTN_TC_TRACE(12 + t, j);
 
       // Causal mask by absolute position, and keys past the sequence: only the
@@ -397,14 +413,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (c > lim) s[c] = -INFINITY;
         }
       }
-      // row max as a tree (independent chains)
-      float mx[8];
+      // row max over eight independent chains of 3-input maxima
+      if (j >= nfull_t) {  // masked tile: the first half was not reduced yet
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[i], s[8 + i], s[16 + i]);
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int c = 24; c < 64; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+      }
+#pragma unroll
+      for (int c = 64; c < 128; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float m_new = fmaxf(m_ref, mt);
       const bool grow = (m_new - m_ref) * sl2 > kRescaleLog2;  // false when both are -inf
       const bool any_grow = __any_sync(0xffffffffu, grow);
@@ -424,17 +446,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      // P = exp2(S * scale*log2e - m*scale*log2e), bf16, into the swizzled K-major tile
-      float acc[8];
+      // P = exp2(S * scale*log2e - m*scale*log2e), bf16, into the swizzled K-major
+      // tile.  The affine step and the row sum run on fp32 pairs.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nmbx2 = f2_pack(-mb, -mb);
+      uint64_t acc[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int i = 0; i < 4; ++i) acc[i] = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c8 = 0; c8 < 16; ++c8) {
         float e[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          e[i] = fast_exp2(fmaf(s[c8 * 8 + i], sl2, -mb));
-          acc[i] += e[i];
+        for (int i = 0; i < 8; i += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[c8 * 8 + i], s[c8 * 8 + i + 1]), sl2x2, nmbx2), x0, x1);
+          e[i] = fast_exp2(x0);
+          e[i + 1] = fast_exp2(x1);
+          acc[i >> 1] = f2_add(acc[i >> 1], f2_pack(e[i], e[i + 1]));
         }
         uint4 v;
         v.x = pack_bf16x2(e[0], e[1]);
@@ -443,19 +470,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         v.w = pack_bf16x2(e[6], e[7]);
         *reinterpret_cast<uint4*>(prow + (c8 >> 3) * HALF + (((c8 & 7) ^ (row & 7)) << 4)) = v;
       }
-      l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      {
+        float a0, a1;
+        f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+        l += a0 + a1;
+      }
       if (row == 0) ATTN_TC_TRACE(16 + t, j);
       if (any_grow && j > 0) {
+        // O_t *= alpha in TMEM.  tcgen05.st reads its source registers
+        // asynchronously, so all four chunks keep their own registers until
+        // the single wait::st.
+        uint32_t o[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tO + c * 32, o[c]);
+        tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_wait_ld();
+          tmem_regs_ready(o[c]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c * 32, o);
+          for (int i = 0; i < 32; ++i) o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * alpha);
+          tmem_st32(tO + c * 32, o[c]);
         }
         tmem_wait_st();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_regs_ready(o[c]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -477,6 +515,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (have_o) {
         tmem_ld32(tO + c * 32, o);
         tmem_wait_ld();
+        tmem_regs_ready(o);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0u;

@@ -452,3 +452,14 @@ def test_decode_bad_page_id_is_reported_not_faulted():
         atc.attn_device_status(clear=True)
     assert e.value.status == 6
     atc.attn_device_status(clear=True)  # cleared
+
+
+def test_prefill_tc_is_deterministic_across_runs():
+    """Repeated calls on the same inputs give bit-identical O and LSE: no part of the
+    pipeline (TMA ring, TMEM score/accumulator reuse, P hand-off) races."""
+    lens = [2048, 700]
+    q, k, v, pos, cu = _bf16_case(lens, 64, 8, [0, 3], 308)
+    first = _run_prefill(q, k, v, pos, cu, lens)
+    for _ in range(3):
+        o, l = _run_prefill(q, k, v, pos, cu, lens)
+        assert torch.equal(o, first[0]) and torch.equal(l, first[1])
