@@ -1,0 +1,154 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times.
+
+The CUDA path runs the whole problem; the fp64 oracle checks every row where it
+finishes in seconds (8K prefill) and seeded samples elsewhere: 512 rows per
+sequence for the 2 x 64K prefill, 96 rows per request for chunked prefill over
+the 57K-token paged prefix, and 6 whole requests of the 32-request decode.
+Inputs are drawn on the GPU by the seeded generators and copied back for the
+oracle before any kernel touches them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_tiled_causal_gb300 as atc
+import oracle
+import synth
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+DEV = "cuda"
+TOL_MAX, TOL_MEAN, TOL_LSE = 1e-2, 1e-3, 1e-3
+
+
+def check(out, lse, want_o, want_l, what):
+    o = out.float().cpu().numpy() if torch.is_tensor(out) else out
+    l = lse.cpu().numpy() if torch.is_tensor(lse) else lse
+    d = np.abs(o - want_o)
+    assert np.isfinite(o).all(), f"{what}: non-finite output"
+    assert d.max() <= TOL_MAX, f"{what}: max |dO| = {d.max():.3g}"
+    assert d.mean() <= TOL_MEAN, f"{what}: mean |dO| = {d.mean():.3g}"
+    dl = np.abs(l - want_l).max()
+    assert dl <= TOL_LSE, f"{what}: max |dLSE| = {dl:.3g}"
+
+
+def rot(x, pos):
+    return oracle.round_bf16(oracle.rope(synth.as_f64(x), np.asarray(pos)))
+
+
+@pytest.fixture(autouse=True)
+def _status():
+    atc.attn_device_status(clear=True)
+    yield
+    torch.cuda.empty_cache()
+
+
+def test_prefill_8k_all_rows():
+    w = synth.PREFILL_8K
+    inp = w.make(DEV)
+    q_raw, k_raw, v = inp["q"].cpu(), inp["k"].cpu(), inp["v"].cpu()
+    pos, cu = inp["pos"], inp["cu"]
+    atc.rope_apply(inp["q"], pos)
+    atc.rope_apply(inp["k"], pos)
+    out, lse = atc.prefill(inp["q"], inp["k"], inp["v"], cu, pos, w.seq, cu_k=cu, k_pos=pos)
+    atc.attn_device_status()
+    p = pos.cpu().numpy()
+    wo, wl = oracle.attention(rot(q_raw, p), np.zeros(w.seq, np.int32), p, rot(k_raw, p), synth.as_f64(v),
+                              cu.cpu().numpy(), p, w.scale)
+    check(out, lse, wo, wl, "8K prefill, all rows")
+
+
+def test_prefill_64k_x2_head_slice_and_all_heads():
+    w = synth.PREFILL_64K
+    inp = w.make(DEV)
+    pos, cu = inp["pos"], inp["cu"]
+    rows = np.concatenate([synth.sample_rows(w.seq, 512, 50 + b) + b * w.seq for b in range(w.batch)])
+    q_raw = inp["q"][torch.from_numpy(rows).to(DEV)].cpu()
+    k_raw, v = inp["k"].cpu(), inp["v"].cpu()
+    atc.rope_apply(inp["q"], pos)
+    atc.rope_apply(inp["k"], pos)
+    out, lse = atc.prefill(inp["q"], inp["k"], inp["v"], cu, pos, w.seq, cu_k=cu, k_pos=pos)
+    out_s = torch.full_like(out, float("nan"))
+    lse_s = torch.full_like(lse, float("nan"))
+    atc.attn_prefill(inp["q"], inp["k"], inp["v"], out_s, lse_s, cu, pos, w.seq, cu_k=cu, k_pos=pos, h_lo=16,
+                     h_hi=32)
+    atc.attn_device_status()
+    # the Ulysses-style head slice equals its part of the all-heads call bit for bit
+    assert torch.equal(out_s[:, 16:32], out[:, 16:32]) and torch.equal(lse_s[:, 16:32], lse[:, 16:32])
+    assert torch.isnan(out_s[:, :16].float()).all() and torch.isnan(out_s[:, 32:].float()).all()
+    p = pos.cpu().numpy()
+    idx = torch.from_numpy(rows).to(DEV)
+    wo, wl = oracle.attention(rot(q_raw, p[rows]), (rows // w.seq).astype(np.int32), p[rows], rot(k_raw, p),
+                              synth.as_f64(v), cu.cpu().numpy(), p, w.scale)
+    check(out[idx], lse[idx], wo, wl, "2 x 64K prefill, 512 rows per sequence, all heads")
+
+
+def test_chunked_prefill_over_57k_paged_prefix():
+    w = synth.CHUNKED
+    inp = w.make(DEV)
+    B, P, C = w.batch, w.prefix, w.chunk
+    rows = np.concatenate([synth.sample_rows(C, 96, 70 + b) + b * C for b in range(B)])
+    q_raw = inp["q"][torch.from_numpy(rows).to(DEV)].cpu()
+    k_raw, v_new = inp["k"].cpu(), inp["v"].cpu()
+    table = inp["page_table"].cpu().numpy()
+    atc.rope_apply(inp["q"], inp["q_pos"])
+    atc.rope_apply(inp["k"], inp["q_pos"])
+    T, hq, d = inp["q"].shape
+    po = torch.empty((2, T, hq, d), dtype=torch.float32, device=DEV)
+    pl = torch.empty((2, T, hq), dtype=torch.float32, device=DEV)
+    atc.attn_prefill(inp["q"], inp["k_cache"], inp["v_cache"], po[0], pl[0], inp["cu_q"], inp["q_pos"], C,
+                     page_table=inp["page_table"], k_lens=inp["prefix_lens"], num_pages=inp["num_pages"])
+    atc.attn_prefill(inp["q"], inp["k"], inp["v"], po[1], pl[1], inp["cu_q"], inp["q_pos"], C, cu_k=inp["cu_q"],
+                     k_pos=inp["q_pos"])
+    out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((T, hq), dtype=torch.float32, device=DEV)
+    atc.attn_lse_merge(po, pl, out, lse)
+    atc.attn_device_status()
+    # oracle: each sampled chunk query over [gathered prefix ; causal chunk]
+    kcf, vcf = synth.as_f64(inp["k_cache"].cpu()), synth.as_f64(inp["v_cache"].cpu())
+    qpos = inp["q_pos"].cpu().numpy()
+    krot = rot(k_raw, qpos)
+    want_o = np.empty((len(rows), hq, d))
+    want_l = np.empty((len(rows), hq))
+    for b in range(B):
+        sel = np.nonzero((rows // C) == b)[0]
+        kb = np.stack([oracle.gather_pages(kcf, table, inp["num_pages"], g, b, P) for g in range(w.hkv)], 1)
+        vb = np.stack([oracle.gather_pages(vcf, table, inp["num_pages"], g, b, P) for g in range(w.hkv)], 1)
+        K = np.concatenate([kb, krot[b * C:(b + 1) * C]])
+        V = np.concatenate([vb, synth.as_f64(v_new[b * C:(b + 1) * C])])
+        KP = np.concatenate([np.arange(P, dtype=np.int32), qpos[b * C:(b + 1) * C]])
+        o, l = oracle.attention(rot(q_raw[sel], qpos[rows[sel]]), np.zeros(len(sel), np.int32), qpos[rows[sel]], K,
+                                V, [0, P + C], KP, w.scale)
+        want_o[sel], want_l[sel] = o, l
+        del kb, vb, K, V
+    idx = torch.from_numpy(rows).to(DEV)
+    check(out[idx], lse[idx], want_o, want_l, "chunked prefill, 96 rows per request")
+
+
+def test_decode_b32_16_splits_on_sampled_requests():
+    w = synth.DECODE
+    inp = w.make(DEV)
+    q_raw = inp["q"].cpu()
+    q = inp["q"].clone()
+    atc.rope_apply(q, inp["q_pos"])
+    po, pl = atc.decode_workspace(w.batch, w.hq, w.splits, w.d, DEV)
+    out = torch.empty((w.batch, w.hq, w.d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((w.batch, w.hq), dtype=torch.float32, device=DEV)
+    atc.attn_decode_paged(q, inp["k_cache"], inp["v_cache"], inp["page_table"], inp["ctx_lens"], w.splits, po, pl,
+                          out, lse)
+    atc.attn_device_status()
+    ctx = inp["ctx_lens"].cpu().numpy()
+    table = inp["page_table"].cpu().numpy()
+    qpos = inp["q_pos"].cpu().numpy()
+    picks = [int(np.argmax(ctx)), int(np.argmin(ctx))] + list(np.random.default_rng(5).choice(w.batch, 4, False))
+    for b in dict.fromkeys(picks):
+        n = (int(ctx[b]) + 63) // 64
+        pages = torch.from_numpy(table[b, :n].astype(np.int64)).to(DEV)
+        kc = inp["k_cache"][:, pages].cpu()  # this request's pages, in logical order
+        vc = inp["v_cache"][:, pages].cpu()
+        ident = np.arange(n, dtype=np.int32)[None, :]
+        wo, wl = oracle.decode_paged(rot(q_raw[b:b + 1], qpos[b:b + 1]), synth.as_f64(kc), synth.as_f64(vc), ident,
+                                     ctx[b:b + 1], n, w.scale)
+        check(out[b:b + 1], lse[b:b + 1], wo, wl, f"decode request {b} (ctx {ctx[b]})")
+        del kc, vc
