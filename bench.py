@@ -1,7 +1,7 @@
 """Benchmark of the attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload all|prefill|decode] [--no-cpu-baseline]
+                    [--workload all|prefill|decode] [--no-cpu-baseline] [--decode-requests N]
 
 Headline (the JSON `value`): causal GQA prefill, batch 1 x 8192 tokens, 64 query /
 8 KV heads, head_dim 128, bf16 -- one step = RoPE of Q and K at absolute
@@ -159,6 +159,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ replicas
+
+def max_over_ranks(ms: float, pg=None, device="cpu") -> float:
+    """Slowest rank's time per step (every rank runs an independent replica)."""
+    if pg is None:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_rank: float, world_size: int, ms_max: float) -> float:
+    """Units per second of the whole job: every rank's work over the slowest rank's time."""
+    return world_size * work_per_rank / (ms_max * 1e-3)
+
+
 # ------------------------------------------------------------------ our arm
 
 class Timer:
@@ -307,7 +323,7 @@ def synth_rows(seq, n, seed):
     return synth.sample_rows(seq, n, seed)
 
 
-def cpu_baseline(wl, inputs, rows=1024):
+def cpu_baseline(wl, inputs, rows=4096):
     import oracle
     dt, flops = oracle_sample(wl, inputs, rows, 99)
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
@@ -326,6 +342,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="all", choices=["all", "prefill", "decode"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-requests", type=int, default=None,
+                    help="decode workload with fewer requests (first N of the seeded 32); for small profiler captures")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     import synth
@@ -358,19 +376,20 @@ def main():
         clocks = clk.summary()
     dec = None
     if args.workload in ("all", "decode"):
-        dec = decode_arm(synth.DECODE, args, timer, peaks, peak_src)
-    ms = res["ms_per_step"] if res else dec["ms_per_step"]
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+        dwl = synth.DECODE
+        if args.decode_requests:
+            import dataclasses
+            dwl = dataclasses.replace(dwl, batch=args.decode_requests,
+                                      name=dwl.name.replace("B32", f"B{args.decode_requests}"))
+        dec = decode_arm(dwl, args, timer, peaks, peak_src)
+    ms = max_over_ranks(res["ms_per_step"] if res else dec["ms_per_step"], pg, "cuda")
     if rank != 0:
         if pg:
             pg.destroy_process_group()
         return 0
     line = {"metric": METRIC}
     if res:
-        value = ws * res["flops"] / (ms * 1e-3) / 1e12
+        value = whole_job_rate(res["flops"], ws, ms) / 1e12
         line.update({"value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
                      "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
