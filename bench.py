@@ -237,6 +237,9 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
         hl.copy_(lse, non_blocking=True)
 
     ms_e2e, _ = timer.run(e2e_step, args.steps, args.warmup)
+    # RoPE alone (S1), an HBM stream: read + write of Q and of K
+    ms_rope, _ = timer.run(lambda ev=(): (atc.rope_apply(q, pos), atc.rope_apply(k, pos)), args.steps, args.warmup)
+    rope_bytes = 2 * (q.numel() + k.numel()) * q.element_size()
     h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
     peak = peaks["bf16_tflops"]
@@ -245,12 +248,13 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
     res = {
         "ms_per_step": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_scope": "prefill_tc_kernel (ncu)",
                      "kernel": "attn::tc::prefill_tc_kernel", "kernel_ms": round(ms_kernel, 4),
                      "peak_source": f"{peak_src} bf16 dense (burst)"},
         "e2e": {"value": round(flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
         "launches_per_step": launches,
+        "rope": hbm_line("rope_apply (Q and K of the 8K prefill)", rope_bytes, ms_rope, peaks, peak_src),
         "inputs": (q, k, v, pos, cu),
     }
     return res
@@ -274,6 +278,9 @@ def decode_arm(wl, args, timer, peaks, peak_src):
             ev[1].record()
 
     ms, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
+    # the LSE merge of the 16 splits alone (S7), an HBM stream
+    ms_merge, _ = timer.run(lambda ev=(): atc.attn_lse_merge(po.permute(2, 0, 1, 3), pl.permute(2, 0, 1), out, lse),
+                            args.steps, args.warmup)
     atc.attn_device_status()
     kv = wl.kv_bytes()
     part = wl.batch * wl.hq * wl.splits * (wl.d + 1) * 4
@@ -290,10 +297,19 @@ def decode_arm(wl, args, timer, peaks, peak_src):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic("decode_split_paged_b32.md", "decode.cu"),
+                     "traffic_scope": "decode_split_kernel (ncu, scaled from a 4-request capture); merge not included",
                      "kernel": "attn::dec::decode_split_kernel + attn::lse_merge_kernel",
                      "kernel_ms": round(ms_kernel, 4), "peak_source": f"{peak_src} HBM copy"},
         "gpu_launches_per_step": 3,
+        "merge": hbm_line("attn_lse_merge of the 16 decode splits", part + outb, ms_merge, peaks, peak_src),
     }
+
+
+def hbm_line(what, nbytes, ms, peaks, peak_src):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"what": what, "bytes": int(nbytes), "ms": round(ms, 4), "value": round(gbs, 1), "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} HBM copy"}}
 
 
 # ------------------------------------------------------------------ oracle timing
@@ -405,6 +421,8 @@ def main():
                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                      "config": {"workload": dec["workload"]}, "roofline": dec["roofline"],
                      "gpu_launches": dec["gpu_launches_per_step"] * args.steps})
+    if res:
+        line["rope"] = res["rope"]
     if dec and res:
         line["decode"] = dec
     if res and not args.no_cpu_baseline:
