@@ -12,7 +12,7 @@
 //  * Warp 8 (one thread) is the TMA producer: Q tiles once, then K_j and V_j
 //    tiles (128 tokens x 128 dims, two 128-byte-swizzled boxes each) into a
 //    3-slot shared-memory ring, each slot guarded by full/empty mbarriers.
-//  * Warp 9 (one thread) issues tcgen05.mma: S_t = Q_t K_j^T into TMEM
+//  * Warp 9 issues tcgen05.mma (the converged warp, one elected lane): S_t = Q_t K_j^T into TMEM
 //    (M = 128, N = 128, K = 16 per instruction, bf16 in, fp32 accumulate),
 //    then O_t += P_t V_j into a second TMEM accumulator.  tcgen05.commit
 //    arrives on mbarriers when the tensor core is done.
@@ -105,12 +105,18 @@ __device__ int upper_bound_pos(const int32_t* k_pos, int n, int qp) {
   return lo;
 }
 
+// K/V ring order.  K runs one tile ahead of V: K0, K1, V0, K2, V1, ...,
+// K_{n-1}, V_{n-2}, V_{n-1}, matching the MMA order S(j) then PV(j-1), so
+// slots are consumed and released first in, first out.
+__device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int ring_pos_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
+
 // S_t = Q_t K_j^T: eight k-steps of 16 over head_dim, both operands K-major.
 __device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint64_t a0, uint64_t b0) {
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t o = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
-    tc_mma_bf16(d_tmem, a0 + o, b0 + o, IDESC_QK, kk > 0 ? 1u : 0u);
+    tc_mma_bf16_warp(d_tmem, a0 + o, b0 + o, IDESC_QK, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -120,7 +126,7 @@ __device__ __forceinline__ void mma_values(uint32_t d_tmem, uint64_t a0, uint64_
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
     const uint64_t o = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
-    tc_mma_bf16(d_tmem, a0 + o, b0 + (uint64_t)(kk * (2048 >> 4)), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+    tc_mma_bf16_warp(d_tmem, a0 + o, b0 + (uint64_t)(kk * (2048 >> 4)), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -219,11 +225,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int32_t* table = PAGED ? p.page_table + (int64_t)b * p.max_pages : nullptr;
       int issued = 0;
       for (int i = 0; i < 2 * nkv; ++i) {
-        const int j = i >> 1, slot = i % NSLOT;
+        // load i of the ring order (see ring_pos_k / ring_pos_v)
+        bool is_v;
+        int j;
+        if (i == 0) {
+          is_v = false, j = 0;
+        } else if (i == 2 * nkv - 1) {
+          is_v = true, j = nkv - 1;
+        } else {
+          is_v = !(i & 1), j = is_v ? (i >> 1) - 1 : (i + 1) >> 1;
+        }
+        const int slot = i % NSLOT;
         if (i >= NSLOT && !mbar_wait(&sm.kv_empty[slot], ((i / NSLOT) - 1) & 1, p.err, DEV_TIMEOUT_TMA)) break;
-        const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
+        const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
         uint8_t* dst = smem + OFF_KV + slot * TILE;
-        ATTN_TC_TRACE(20 + (i & 1), j);
+        ATTN_TC_TRACE(20 + (is_v ? 1 : 0), j);
         mbar_arrive_expect_tx(&sm.kv_full[slot], TILE);
         if (!PAGED) {
           for (int hf = 0; hf < 2; ++hf) tma_load_3d(dst + hf * HALF, tm, &sm.kv_full[slot], hf * 64, g, k_beg + j * BN);
@@ -248,14 +264,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    // Issue order per K/V tile j:  S_A(j), PV_B(j-1), S_B(j), PV_A(j).  Each
-    // softmax then has a full two-MMA window (S of the other tile and one PV)
-    // before its own PV is due, and the previous PV of the same tile always
-    // precedes the next S, so the P buffer it reads is free by then.
-    if (lane == 0 && nkv > 0) {
+    // Issue order per K/V tile j:  S_A(j), S_B(j), PV_A(j-1), PV_B(j-1).  The PV
+    // lags one tile behind the scores, so each softmax has from the end of its
+    // S_t(j) until PV_t(j) in the next round -- five MMA groups -- to produce
+    // P_t(j).  P lives in shared memory, so S_t(j+1) may overwrite S_t in TMEM
+    // while P_t(j) still waits for its PV.
+    if (nkv > 0) {
+      // The whole warp runs this loop in step; waits are made warp-uniform so
+      // that every elect.sync below sees all 32 lanes.
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.err, DEV_TIMEOUT_MMA));
+      };
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
-        if (sm.nkv[t] > 0) ok = mbar_wait(&sm.q_full[t], 0, p.err, DEV_TIMEOUT_MMA);
+        if (sm.nkv[t] > 0) ok = wait(&sm.q_full[t], 0);
       tc_fence_after();
       ATTN_TC_TRACE(0, 0);
       // Descriptors of every tile base; a k-step adds a constant byte offset
@@ -266,71 +288,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t dP = sdesc_sw128(smem_u32(smem + OFF_P), 16, 1024);
       const uint64_t dV = sdesc_sw128(smem_u32(smem + OFF_KV), HALF, 1024);
       constexpr uint64_t kTile16 = TILE >> 4;
-      for (int j = 0; j < nkv; ++j) {
-        const int iK = 2 * j, slotK = iK % NSLOT;
-        const int iV = 2 * j + 1, slotV = iV % NSLOT;
-        if (!(ok = mbar_wait(&sm.kv_full[slotK], (iK / NSLOT) & 1, p.err, DEV_TIMEOUT_MMA))) break;
-        tc_fence_after();
-        ATTN_TC_TRACE(1, j);
-        // S_t(j) overwrites S_t(j-1) in TMEM only after the softmax has
-        // signalled (s_free) that S_t(j-1) is in its registers.
-        if (j < nkv_a) {  // S_A(j)
-          if (j > 0) {
-            if (!(ok = mbar_wait(&sm.s_free[0], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA))) break;
-            tc_fence_after();
-          }
-          ATTN_TC_TRACE(22, j);
-          mma_scores(tmem, dQ, dKV + slotK * kTile16);
-          tc_commit(&sm.s_full[0]);
-          ATTN_TC_TRACE(2, j);
-        }
-        if (j > 0) {  // PV_B(j-1)
-          const int slotVp = (iV - 2) % NSLOT;
-          if (j - 1 < nkv_b) {
-            if (!(ok = mbar_wait(&sm.p_full[1], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA))) break;
-            tc_fence_after();
-            ATTN_TC_TRACE(3, j - 1);
-            ATTN_TC_TRACE(25, j - 1);
-            mma_values(tmem + 2 * BN + D, dP + kTile16, dV + slotVp * kTile16, j - 1 > 0);
-            tc_commit(&sm.o_done[1]);
-            ATTN_TC_TRACE(4, j - 1);
-          }
-          tc_commit(&sm.kv_empty[slotVp]);  // V_{j-1} consumed
-        }
-        if (j < nkv_b) {  // S_B(j)
-          if (j > 0) {
-            if (!(ok = mbar_wait(&sm.s_free[1], (j - 1) & 1, p.err, DEV_TIMEOUT_MMA))) break;
-            tc_fence_after();
-          }
-          ATTN_TC_TRACE(23, j);
-          mma_scores(tmem + BN, dQ + kTile16, dKV + slotK * kTile16);
-          tc_commit(&sm.s_full[1]);
-          ATTN_TC_TRACE(5, j);
-        }
-        tc_commit(&sm.kv_empty[slotK]);  // K_j consumed
-        if (!(ok = mbar_wait(&sm.kv_full[slotV], (iV / NSLOT) & 1, p.err, DEV_TIMEOUT_MMA))) break;
-        tc_fence_after();
-        ATTN_TC_TRACE(6, j);
-        if (j < nkv_a) {  // PV_A(j)
-          if (!(ok = mbar_wait(&sm.p_full[0], j & 1, p.err, DEV_TIMEOUT_MMA))) break;
+      for (int j = 0; j <= nkv && ok; ++j) {
+        if (j < nkv) {
+          const int iK = ring_pos_k(j), slotK = iK % NSLOT;
+          if (!(ok = wait(&sm.kv_full[slotK], (iK / NSLOT) & 1))) break;
           tc_fence_after();
-          ATTN_TC_TRACE(7, j);
-          ATTN_TC_TRACE(24, j);
-          mma_values(tmem + 2 * BN, dP, dV + slotV * kTile16, j > 0);
-          tc_commit(&sm.o_done[0]);
-          ATTN_TC_TRACE(8, j);
-        }
-      }
-      if (ok) {  // PV_B of the last tile
-        const int j = nkv - 1, slotV = (2 * j + 1) % NSLOT;
-        if (j < nkv_b) {
-          if ((ok = mbar_wait(&sm.p_full[1], j & 1, p.err, DEV_TIMEOUT_MMA))) {
-            tc_fence_after();
-            mma_values(tmem + 2 * BN + D, dP + kTile16, dV + slotV * kTile16, j > 0);
-            tc_commit(&sm.o_done[1]);
+          ATTN_TC_TRACE(1, j);
+          // S_t(j) overwrites S_t(j-1) in TMEM only after the softmax has
+          // signalled (s_free) that S_t(j-1) is in its registers.
+          for (int t = 0; t < 2; ++t) {
+            if (j >= (t ? nkv_b : nkv_a)) continue;
+            if (j > 0) {
+              if (!(ok = wait(&sm.s_free[t], (j - 1) & 1))) break;
+              tc_fence_after();
+            }
+            ATTN_TC_TRACE(22 + t, j);
+            mma_scores(tmem + t * BN, dQ + t * kTile16, dKV + slotK * kTile16);
+            tc_commit_warp(&sm.s_full[t]);
+            ATTN_TC_TRACE(2 + 3 * t, j);
           }
+          if (!ok) break;
+          tc_commit_warp(&sm.kv_empty[slotK]);  // K_j consumed
         }
-        tc_commit(&sm.kv_empty[slotV]);
+        if (j > 0) {
+          const int jv = j - 1, iV = ring_pos_v(jv, nkv), slotV = iV % NSLOT;
+          if (!(ok = wait(&sm.kv_full[slotV], (iV / NSLOT) & 1))) break;
+          tc_fence_after();
+          ATTN_TC_TRACE(6, jv);
+          for (int t = 0; t < 2; ++t) {
+            if (jv >= (t ? nkv_b : nkv_a)) continue;
+            if (!(ok = wait(&sm.p_full[t], jv & 1))) break;
+            tc_fence_after();
+            ATTN_TC_TRACE(7 - 4 * t, jv);
+            ATTN_TC_TRACE(24 + t, jv);
+            mma_values(tmem + 2 * BN + t * D, dP + t * kTile16, dV + slotV * kTile16, jv > 0);
+            tc_commit_warp(&sm.o_done[t]);
+            ATTN_TC_TRACE(8 - 4 * t, jv);
+          }
+          if (!ok) break;
+          tc_commit_warp(&sm.kv_empty[slotV]);  // V_{j-1} consumed
+        }
       }
     }
    }
