@@ -12,11 +12,12 @@
 //  * Warp 8 (one thread) is the TMA producer: Q tiles once, then K_j and V_j
 //    tiles (128 tokens x 128 dims, two 128-byte-swizzled boxes each) into a
 //    3-slot shared-memory ring, each slot guarded by full/empty mbarriers.
-//  * Warp 9 issues tcgen05.mma (the converged warp, one elected lane): S_t = Q_t K_j^T into TMEM
-//    (M = 128, N = 128, K = 16 per instruction, bf16 in, fp32 accumulate),
-//    then O_t += P_t V_j into a second TMEM accumulator.  tcgen05.commit
+//  * Warps 9 and 10 issue tcgen05.mma, each as a converged warp with one
+//    elected lane: warp 9 the scores S_t = Q_t K_j^T into TMEM (M = 128,
+//    N = 128, K = 16 per instruction, bf16 in, fp32 accumulate), warp 10 the
+//    updates O_t += P_t V_j into a second TMEM accumulator.  tcgen05.commit
 //    arrives on mbarriers when the tensor core is done.
-//  * Warps 10-11 idle (the block is three whole warpgroups).
+//  * Warp 11 idles (the block is three whole warpgroups).
 //  * Warps 0-3 (tile A) and 4-7 (tile B) are the softmax warpgroups: thread r
 //    of a warpgroup owns query row r (TMEM lane r), loads its 128 scores with
 //    tcgen05.ld, applies the absolute-position causal mask (Ulysses page,
@@ -62,7 +63,7 @@ constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 32 + 1024;
 // sub-partitions, so 3 warps per sub-partition launch with at most 168
 // registers each; every role fits in that without spilling.
 constexpr int NTHREADS = 384;
-constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int WARP_TMA = 8, WARP_MMA_S = 9, WARP_MMA_PV = 10;
 constexpr int REGS_LAUNCH = 168;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       sm.nfull[t] = nk_first / BN;
     }
   }
-  if (warp == WARP_MMA) tmem_alloc(sm.tmem_slot, TMEM_COLS);
+  if (warp == WARP_MMA_S) tmem_alloc(sm.tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -262,34 +263,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int i = max(0, issued - NSLOT); i < issued; ++i)
         mbar_wait(&sm.kv_full[i % NSLOT], (i / NSLOT) & 1, nullptr, 0);
     }
-  } else if (warp == WARP_MMA) {
-    // ------------------------------------------------------------ MMA issuer
-    // Issue order per K/V tile j:  S_A(j), S_B(j), PV_A(j-1), PV_B(j-1).  The PV
-    // lags one tile behind the scores, so each softmax has from the end of its
-    // S_t(j) until PV_t(j) in the next round -- five MMA groups -- to produce
-    // P_t(j).  P lives in shared memory, so S_t(j+1) may overwrite S_t in TMEM
-    // while P_t(j) still waits for its PV.
+  } else if (warp == WARP_MMA_S || warp == WARP_MMA_PV) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two converged warps on different sub-partitions feed the tensor core:
+    // warp 9 issues the scores S_t(j) = Q_t K_j^T, warp 10 the updates
+    // O_t += P_t(j) V_j.  tcgen05.mma issue blocks once a few MMAs are queued,
+    // so whatever an issuer does between its groups (barrier waits, fences,
+    // commits) would leave the tensor core idle; with two issuers the other
+    // one's MMAs fill that time.  Each accumulator still has a single issuer,
+    // so its MMAs run in program order and results do not depend on how the
+    // two streams interleave.  The K/V ring holds K0, K1, V0, K2, V1, ..., so
+    // each softmax has from the end of S_t(j) until PV_t(j) -- which follows
+    // S_t(j+1) -- to produce P_t(j).  P lives in shared memory, so S_t(j+1) may
+    // overwrite S_t in TMEM while P_t(j) still waits for its PV.
     if (nkv > 0) {
-      // The whole warp runs this loop in step; waits are made warp-uniform so
-      // that every elect.sync below sees all 32 lanes.
+      // Warp-uniform bounded waits, so every elect.sync below sees all 32 lanes.
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.err, DEV_TIMEOUT_MMA));
       };
-      bool ok = true;
-      for (int t = 0; t < 2 && ok; ++t)
-        if (sm.nkv[t] > 0) ok = wait(&sm.q_full[t], 0);
-      tc_fence_after();
-      ATTN_TC_TRACE(0, 0);
       // Descriptors of every tile base; a k-step adds a constant byte offset
       // (>> 4) to the 14-bit start-address field, which never carries out of it
       // because shared-memory addresses stay below 256 KB.
-      const uint64_t dQ = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
-      const uint64_t dKV = sdesc_sw128(smem_u32(smem + OFF_KV), 16, 1024);
-      const uint64_t dP = sdesc_sw128(smem_u32(smem + OFF_P), 16, 1024);
-      const uint64_t dV = sdesc_sw128(smem_u32(smem + OFF_KV), HALF, 1024);
       constexpr uint64_t kTile16 = TILE >> 4;
-      for (int j = 0; j <= nkv && ok; ++j) {
-        if (j < nkv) {
+      if (warp == WARP_MMA_S) {
+        bool ok = true;
+        for (int t = 0; t < 2 && ok; ++t)
+          if (sm.nkv[t] > 0) ok = wait(&sm.q_full[t], 0);
+        tc_fence_after();
+        ATTN_TC_TRACE(0, 0);
+        const uint64_t dQ = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
+        const uint64_t dK = sdesc_sw128(smem_u32(smem + OFF_KV), 16, 1024);
+        for (int j = 0; j < nkv && ok; ++j) {
           const int iK = ring_pos_k(j), slotK = iK % NSLOT;
           if (!(ok = wait(&sm.kv_full[slotK], (iK / NSLOT) & 1))) break;
           tc_fence_after();
@@ -303,30 +307,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               tc_fence_after();
             }
             ATTN_TC_TRACE(22 + t, j);
-            mma_scores(tmem + t * BN, dQ + t * kTile16, dKV + slotK * kTile16);
+            mma_scores(tmem + t * BN, dQ + t * kTile16, dK + slotK * kTile16);
             tc_commit_warp(&sm.s_full[t]);
             ATTN_TC_TRACE(2 + 3 * t, j);
           }
           if (!ok) break;
           tc_commit_warp(&sm.kv_empty[slotK]);  // K_j consumed
         }
-        if (j > 0) {
-          const int jv = j - 1, iV = ring_pos_v(jv, nkv), slotV = iV % NSLOT;
+      } else {
+        const uint64_t dP = sdesc_sw128(smem_u32(smem + OFF_P), 16, 1024);
+        const uint64_t dV = sdesc_sw128(smem_u32(smem + OFF_KV), HALF, 1024);
+        bool ok = true;
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int iV = ring_pos_v(j, nkv), slotV = iV % NSLOT;
           if (!(ok = wait(&sm.kv_full[slotV], (iV / NSLOT) & 1))) break;
           tc_fence_after();
-          ATTN_TC_TRACE(6, jv);
+          ATTN_TC_TRACE(6, j);
           for (int t = 0; t < 2; ++t) {
-            if (jv >= (t ? nkv_b : nkv_a)) continue;
-            if (!(ok = wait(&sm.p_full[t], jv & 1))) break;
+            if (j >= (t ? nkv_b : nkv_a)) continue;
+            if (!(ok = wait(&sm.p_full[t], j & 1))) break;
             tc_fence_after();
-            ATTN_TC_TRACE(7 - 4 * t, jv);
-            ATTN_TC_TRACE(24 + t, jv);
-            mma_values(tmem + 2 * BN + t * D, dP + t * kTile16, dV + slotV * kTile16, jv > 0);
+            ATTN_TC_TRACE(7 - 4 * t, j);
+            ATTN_TC_TRACE(24 + t, j);
+            mma_values(tmem + 2 * BN + t * D, dP + t * kTile16, dV + slotV * kTile16, j > 0);
             tc_commit_warp(&sm.o_done[t]);
-            ATTN_TC_TRACE(8 - 4 * t, jv);
+            ATTN_TC_TRACE(8 - 4 * t, j);
           }
           if (!ok) break;
-          tc_commit_warp(&sm.kv_empty[slotV]);  // V_{j-1} consumed
+          tc_commit_warp(&sm.kv_empty[slotV]);  // V_j consumed
         }
       }
     }
@@ -544,7 +552,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == WARP_MMA) {
+  if (warp == WARP_MMA_S) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
