@@ -1,14 +1,17 @@
 """Benchmark of the attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload all|prefill|decode] [--no-cpu-baseline] [--decode-requests N]
+                    [--workload all|prefill|decode|long|chunked] [--no-cpu-baseline] [--decode-requests N]
 
 Headline (the JSON `value`): causal GQA prefill, batch 1 x 8192 tokens, 64 query /
 8 KV heads, head_dim 128, bf16 -- one step = RoPE of Q and K at absolute
 positions + tiled causal attention (O and LSE).  TFLOP/s counts 4*d flops per
 visible (query, key) pair.  The paged split-KV decode workload (32 requests,
 contexts U[16384, 131072], 16 splits + LSE merge) is reported in `decode`,
-as KV-cache GB/s.  Inputs are synthetic and seeded (N(0,1)/sqrt(2) bf16).
+as KV-cache GB/s.  `prefill_64k` times 2 x 65536-token causal prefill over all
+heads and over heads 16..31 alone; `chunked` times chunked prefill of 4 x 8192
+new tokens over a 57344-token paged prefix (prefix call + chunk call + merge).
+Inputs are synthetic and seeded (N(0,1)/sqrt(2) bf16).
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on
 the launching stream, with an L2 flush (a 512 MB write) between steps outside
@@ -305,6 +308,89 @@ def decode_arm(wl, args, timer, peaks, peak_src):
     }
 
 
+def long_prefill_arm(wl, args, timer, peaks, peak_src):
+    """2 x 65536-token causal prefill: all 64 heads, and heads 16..31 alone (one
+    Ulysses rank's share of a 4-way head split).  Attention only: RoPE is applied
+    once before the timed calls."""
+    import attention_tiled_causal_gb300 as atc
+    inp = wl.make("cuda")
+    q, k, v, pos, cu = inp["q"], inp["k"], inp["v"], inp["pos"], inp["cu"]
+    atc.rope_apply(q, pos)
+    atc.rope_apply(k, pos)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    peak = peaks["bf16_tflops"]
+    steps, warmup = min(args.steps, 5), 3
+    res = {"workload": wl.name + " (attention only)", "steps": steps, "warmup": warmup}
+    for lo, hi in ((0, wl.hq), (16, 32)):
+        def step(ev=(), lo=lo, hi=hi):
+            atc.attn_prefill(q, k, v, out, lse, cu, pos, wl.seq, cu_k=cu, k_pos=pos, h_lo=lo, h_hi=hi)
+
+        ms, _ = timer.run(step, steps, warmup)
+        fl = wl.flops(lo, hi)
+        tf = fl / (ms * 1e-3) / 1e12
+        res[f"heads_{lo}_{hi}"] = {"flops": fl, "ms": round(ms, 4), "value": round(tf, 2), "unit": "TFLOP/s",
+                                   "frac": round(tf / peak, 4), "peak": peak,
+                                   "peak_source": f"{peak_src} bf16 dense (burst)"}
+    atc.attn_device_status()
+    del inp, q, k, v, out
+    return res
+
+
+def chunked_arm(wl, args, timer, peaks, peak_src):
+    """Chunked prefill: 4 requests, each an 8192-token chunk over a 57344-token
+    prefix in a shuffled head-major paged cache.  One step = the paged-prefix
+    call + the causal chunk call + the LSE merge of the two partial results."""
+    import attention_tiled_causal_gb300 as atc
+    inp = wl.make("cuda")
+    C = wl.chunk
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    atc.rope_apply(q, inp["q_pos"])
+    atc.rope_apply(k, inp["q_pos"])
+    T, hq, d = q.shape
+    po = torch.empty((2, T, hq, d), dtype=torch.float32, device="cuda")
+    pl = torch.empty((2, T, hq), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, hq), dtype=torch.float32, device="cuda")
+
+    def prefix(ev=()):
+        atc.attn_prefill(q, inp["k_cache"], inp["v_cache"], po[0], pl[0], inp["cu_q"], inp["q_pos"], C,
+                         page_table=inp["page_table"], k_lens=inp["prefix_lens"], num_pages=inp["num_pages"])
+
+    def chunk(ev=()):
+        atc.attn_prefill(q, k, v, po[1], pl[1], inp["cu_q"], inp["q_pos"], C, cu_k=inp["cu_q"], k_pos=inp["q_pos"])
+
+    def merge(ev=()):
+        atc.attn_lse_merge(po, pl, out, lse)
+
+    def step(ev=()):
+        prefix()
+        chunk()
+        merge()
+
+    steps, warmup = min(args.steps, 10), 3
+    ms, _ = timer.run(step, steps, warmup)
+    ms_p, _ = timer.run(prefix, steps, warmup)
+    ms_c, _ = timer.run(chunk, steps, warmup)
+    ms_m, _ = timer.run(merge, steps, warmup)
+    atc.attn_device_status()
+    peak = peaks["bf16_tflops"]
+    fl = wl.flops()
+    fl_c = 4.0 * wl.d * wl.hq * wl.batch * (C * (C + 1) // 2)
+    fl_p = fl - fl_c
+    merge_bytes = po.numel() * 4 + pl.numel() * 4 + out.numel() * 2 + lse.numel() * 4
+    del inp, q, k, v, po, pl, out, lse
+    tf = fl / (ms * 1e-3) / 1e12
+    return {"workload": wl.name + " (paged prefix + causal chunk + LSE merge)", "steps": steps, "warmup": warmup,
+            "flops": fl, "ms": round(ms, 4), "value": round(tf, 2), "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+            "peak": peak, "peak_source": f"{peak_src} bf16 dense (burst)",
+            "paged_prefix": {"ms": round(ms_p, 4), "value": round(fl_p / (ms_p * 1e-3) / 1e12, 2),
+                             "unit": "TFLOP/s"},
+            "causal_chunk": {"ms": round(ms_c, 4), "value": round(fl_c / (ms_c * 1e-3) / 1e12, 2),
+                             "unit": "TFLOP/s"},
+            "merge": hbm_line("attn_lse_merge of the two partial results", merge_bytes, ms_m, peaks, peak_src)}
+
+
 def hbm_line(what, nbytes, ms, peaks, peak_src):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"what": what, "bytes": int(nbytes), "ms": round(ms, 4), "value": round(gbs, 1), "unit": "GB/s",
@@ -356,7 +442,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="all", choices=["all", "prefill", "decode"])
+    ap.add_argument("--workload", default="all", choices=["all", "prefill", "decode", "long", "chunked"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-requests", type=int, default=None,
                     help="decode workload with fewer requests (first N of the seeded 32); for small profiler captures")
@@ -398,6 +484,19 @@ def main():
             dwl = dataclasses.replace(dwl, batch=args.decode_requests,
                                       name=dwl.name.replace("B32", f"B{args.decode_requests}"))
         dec = decode_arm(dwl, args, timer, peaks, peak_src)
+    extra = {}
+    if args.workload in ("all", "long"):
+        extra["prefill_64k"] = long_prefill_arm(synth.PREFILL_64K, args, timer, peaks, peak_src)
+        torch.cuda.empty_cache()
+    if args.workload in ("all", "chunked"):
+        extra["chunked"] = chunked_arm(synth.CHUNKED, args, timer, peaks, peak_src)
+        torch.cuda.empty_cache()
+    if not res and not dec:  # a single secondary workload (profiling): print its own object
+        if rank == 0:
+            print(json.dumps(extra), flush=True)
+        if pg:
+            pg.destroy_process_group()
+        return 0
     ms = max_over_ranks(res["ms_per_step"] if res else dec["ms_per_step"], pg, "cuda")
     if rank != 0:
         if pg:
@@ -425,6 +524,7 @@ def main():
         line["rope"] = res["rope"]
     if dec and res:
         line["decode"] = dec
+    line.update(extra)
     if res and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, res["inputs"])
     print(json.dumps(line), flush=True)
