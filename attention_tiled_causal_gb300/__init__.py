@@ -8,14 +8,16 @@ PyTorch provides device memory and streams.
 
 Entry points (same names as the C ABI):
     rope_apply(x, positions, base)                      RoPE at absolute positions, in place
+    attn_kv_append_paged(k_new, v_new, positions, slots, k_cache, v_cache)
+                                                        new K (rotated) / V into the paged cache
     attn_prefill(q, k, v, out, lse, cu_q, q_pos, ...)   tiled causal GQA attention
     attn_decode_paged(q, k_cache, v_cache, ...)         split-KV decode over a paged cache
     attn_lse_merge(part_out, part_lse, out, lse, ...)   log-sum-exp merge of partials
 """
 from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_device_status,
-                       attn_lse_merge, attn_prefill, decode_workspace, lib_path, library, prefill,
-                       rope_apply)
+                       attn_kv_append_paged, attn_lse_merge, attn_prefill, decode_workspace, lib_path, library,
+                       prefill, rope_apply)
 
 __all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_device_status",
-           "attn_lse_merge", "attn_prefill", "decode_workspace", "lib_path", "library", "prefill",
-           "rope_apply"]
+           "attn_kv_append_paged", "attn_lse_merge", "attn_prefill", "decode_workspace", "lib_path", "library",
+           "prefill", "rope_apply"]

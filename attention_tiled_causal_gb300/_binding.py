@@ -42,6 +42,8 @@ def library():
     lib.attn_device_status.restype = I32
     lib.rope_apply.argtypes = [P, I32, I64, I32, I32, I64, P, F64, P]
     lib.rope_apply.restype = I32
+    lib.attn_kv_append_paged.argtypes = [P, P, P, P, I64, I32, I32, P, P, I64, I32, P, F64, P]
+    lib.attn_kv_append_paged.restype = I32
     lib.attn_prefill.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, I64, I32, P, P, I64, P, P, I32, I32, I64,
                                  I32, I32, I32, I32, I32, F32, I32, P]
     lib.attn_prefill.restype = I32
@@ -104,6 +106,39 @@ def rope_apply(x: torch.Tensor, positions: torch.Tensor, base: float = 10000.0, 
     _check(library().rope_apply(_ptr(x), _dt(x), x.shape[0], x.shape[1], x.shape[2], x.stride(0),
                                 _ptr(positions), float(base), _stream(stream)))
     return x
+
+
+def attn_kv_append_paged(k_new, v_new, positions, slots, k_cache, v_cache, *, k_rot_out=None,
+                         base: float = 10000.0, stream=None) -> None:
+    """Write new tokens' K (rotated at `positions`) and V [tokens, Hkv, d] bf16 into the
+    head-major paged caches [Hkv, num_pages, page_size, d] at `slots` [tokens]
+    (page * page_size + offset; -1 skips).  k_rot_out [tokens, Hkv, d] also receives
+    the rotated keys if given.  base = 0 copies the keys unrotated."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{n} must be contiguous bf16")
+    T, hkv, d = k_new.shape
+    if tuple(v_new.shape) != (T, hkv, d):
+        raise ValueError("v_new must have k_new's shape")
+    if k_cache.dim() != 4 or tuple(k_cache.shape) != tuple(v_cache.shape) or k_cache.shape[0] != hkv \
+            or k_cache.shape[3] != d:
+        raise ValueError("caches must be [num_kv_heads, num_pages, page_size, head_dim], alike")
+    if k_rot_out is not None and (tuple(k_rot_out.shape) != (T, hkv, d) or not k_rot_out.is_contiguous()
+                                  or k_rot_out.dtype != torch.bfloat16):
+        raise ValueError("k_rot_out must be contiguous bf16 shaped like k_new")
+    slots = _i32(slots, "slots")
+    if slots.numel() != T:
+        raise ValueError("slots must hold one entry per token")
+    pos_ptr = None
+    if base > 0:
+        positions = _i32(positions, "positions")
+        if positions.numel() != T:
+            raise ValueError("positions must hold one entry per token")
+        pos_ptr = _ptr(positions)
+    _check(library().attn_kv_append_paged(_ptr(k_new), _ptr(v_new), pos_ptr, _ptr(slots), T, hkv, d,
+                                          _ptr(k_cache), _ptr(v_cache), k_cache.shape[1], k_cache.shape[2],
+                                          _ptr(k_rot_out) if k_rot_out is not None else None, float(base),
+                                          _stream(stream)))
 
 
 def attn_prefill(q, k, v, out, lse, cu_q, q_pos, max_seqlen_q: int, *, cu_k=None, k_pos=None,

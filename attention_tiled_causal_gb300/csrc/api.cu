@@ -160,6 +160,31 @@ int rope_apply(void* x, attn_dtype_t dtype, int64_t tokens, int heads, int head_
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "rope_apply launch");
 }
 
+int attn_kv_append_paged(const void* k_new, const void* v_new, const int32_t* positions, const int32_t* slots,
+                         int64_t tokens, int num_kv_heads, int head_dim, void* k_cache, void* v_cache,
+                         int64_t num_pages, int page_size, void* k_rot_out, double base, void* stream) {
+  if (tokens < 0 || num_kv_heads < 0 || head_dim <= 0 || num_pages < 0 || page_size <= 0)
+    return fail(ATTN_ERR_ARG, "attn_kv_append_paged: negative size");
+  if (head_dim % 2 || (head_dim / 2) % 8 || head_dim > 256)
+    return fail(ATTN_ERR_SHAPE, "attn_kv_append_paged: head_dim %d (need head_dim/2 a multiple of 8, <= 256)",
+                head_dim);
+  if (!(base >= 0.0)) return fail(ATTN_ERR_ARG, "attn_kv_append_paged: base must be >= 0 (0 = no rotation)");
+  if (tokens == 0 || num_kv_heads == 0) return ATTN_OK;
+  if (!k_new || !v_new || !slots || !k_cache || !v_cache || (base > 0.0 && !positions))
+    return fail(ATTN_ERR_ARG, "attn_kv_append_paged: null pointer");
+  if (num_pages == 0) return fail(ATTN_ERR_ARG, "attn_kv_append_paged: empty cache");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (k_rot_out && !aligned16(k_rot_out)))
+    return fail(ATTN_ERR_ALIGN, "attn_kv_append_paged: tensors must be 16-byte aligned");
+  unsigned* err = nullptr;
+  int rc = device_error_ptr(&err);
+  if (rc) return rc;
+  attn::AppendLaunch a{k_new, v_new, positions, slots, tokens, num_kv_heads, head_dim, k_cache, v_cache,
+                       num_pages * (int64_t)page_size, k_rot_out, base, err};
+  cudaError_t e = attn::launch_kv_append(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_kv_append_paged launch");
+}
+
 int attn_prefill(const void* q, const void* k, const void* v, void* out, attn_dtype_t out_dtype, float* lse,
                  attn_dtype_t dtype, int batch, const int32_t* cu_q, const int32_t* q_pos, int64_t total_q,
                  int max_seqlen_q, const int32_t* cu_k, const int32_t* k_pos, int64_t total_k,

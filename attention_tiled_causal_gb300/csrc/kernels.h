@@ -19,6 +19,22 @@ struct RopeLaunch {
 };
 cudaError_t launch_rope(const RopeLaunch& a, cudaStream_t s);
 
+struct AppendLaunch {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* positions;
+  const int32_t* slots;
+  int64_t tokens;
+  int heads, head_dim;
+  void* k_cache;
+  void* v_cache;
+  int64_t cache_rows;  // num_pages * page_size
+  void* k_rot_out;
+  double base;  // 0: copy keys unrotated
+  unsigned* err;
+};
+cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s);
+
 struct MergeLaunch {
   const float* part_out;
   const float* part_lse;

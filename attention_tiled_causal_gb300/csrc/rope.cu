@@ -32,15 +32,12 @@ __device__ __forceinline__ void from_f(float x, float& y) { y = x; }
 
 constexpr int kTok = 4;  // tokens per block
 
-template <typename T>
-__global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t tokens, int heads, int d,
-                                                   int64_t stride_tok, const int32_t* __restrict__ pos,
-                                                   const InvFreq f) {
-  constexpr int V = Vec<T>::N;
-  __shared__ float cs_s[kTok][128], sn_s[kTok][128];
-  const int half = d / 2;
-  const int chunks = half / V;
-  const int64_t t0 = (int64_t)blockIdx.x * kTok;
+// cos and sin of pos * base^(-2i/d) for the block's kTok tokens, i < d/2, into
+// shared memory.  The angle is reduced modulo 2 pi in fp64, then sincosf runs
+// on the reduced fp32 angle.  Every kernel that rotates keys calls this, so
+// their results agree bit for bit.
+__device__ __forceinline__ void angle_tables(float (*cs_s)[128], float (*sn_s)[128], int64_t t0, int64_t tokens,
+                                             int half, const int32_t* __restrict__ pos, const InvFreq& f) {
   constexpr double kTwoPi = 6.283185307179586476925286766559;
   constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
   for (int i = threadIdx.x; i < kTok * half; i += blockDim.x) {
@@ -53,6 +50,18 @@ __global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t to
     }
   }
   __syncthreads();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t tokens, int heads, int d,
+                                                   int64_t stride_tok, const int32_t* __restrict__ pos,
+                                                   const InvFreq f) {
+  constexpr int V = Vec<T>::N;
+  __shared__ float cs_s[kTok][128], sn_s[kTok][128];
+  const int half = d / 2;
+  const int chunks = half / V;
+  const int64_t t0 = (int64_t)blockIdx.x * kTok;
+  angle_tables(cs_s, sn_s, t0, tokens, half, pos, f);
   const int items = kTok * heads * chunks;
 #pragma unroll 4
   for (int w = threadIdx.x; w < items; w += blockDim.x) {
@@ -80,6 +89,99 @@ __global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t to
     *reinterpret_cast<uint4*>(p1) = w1;
     *reinterpret_cast<uint4*>(p2) = w2;
   }
+}
+
+// New tokens' K and V into the head-major paged cache (SGLang page, sections
+// 2.1-2.2), K rotated as rope_kernel rotates it.  Each block takes kTok tokens:
+// angle tables first, then one 16-byte vector of the first half of a key head
+// with its partner vector of the second half per thread (rotated, written to
+// the cache row and optionally to k_rot_out), then the value rows copied as
+// 16-byte vectors.  Slots are checked per token: -1 skips, out of range is
+// recorded and skipped.
+__global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const InvFreq f) {
+  constexpr int V = 8;  // bf16 per 16-byte vector
+  __shared__ float cs_s[kTok][128], sn_s[kTok][128];
+  __shared__ int64_t slot_s[kTok];
+  const int d = a.head_dim, half = d / 2;
+  const int64_t t0 = (int64_t)blockIdx.x * kTok;
+  if (threadIdx.x < kTok) {
+    const int64_t t = t0 + threadIdx.x;
+    int64_t sl = -1;
+    if (t < a.tokens) {
+      sl = __ldg(a.slots + t);
+      if (sl < -1 || sl >= a.cache_rows) {
+        record_error(a.err, DEV_BAD_SLOT);
+        sl = -1;
+      }
+    }
+    slot_s[threadIdx.x] = sl;
+  }
+  const bool rotate = a.base > 0.0;
+  if (rotate) angle_tables(cs_s, sn_s, t0, a.tokens, half, a.positions, f);
+  __syncthreads();
+  const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
+  const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
+  __nv_bfloat16* kc = (__nv_bfloat16*)a.k_cache;
+  __nv_bfloat16* vc = (__nv_bfloat16*)a.v_cache;
+  __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
+  const int chunks = half / V;
+  const int kitems = kTok * a.heads * chunks;
+  for (int w = threadIdx.x; w < kitems; w += blockDim.x) {
+    const int c = w % chunks;
+    const int h = (w / chunks) % a.heads;
+    const int tt = w / (chunks * a.heads);
+    const int64_t sl = slot_s[tt];
+    if (sl < 0) continue;
+    const int64_t t = t0 + tt;
+    const int64_t src = (t * a.heads + h) * d + c * V;
+    uint4 u1 = __ldg(reinterpret_cast<const uint4*>(kn + src));
+    uint4 u2 = __ldg(reinterpret_cast<const uint4*>(kn + src + half));
+    if (rotate) {
+      const __nv_bfloat16* a1 = reinterpret_cast<const __nv_bfloat16*>(&u1);
+      const __nv_bfloat16* a2 = reinterpret_cast<const __nv_bfloat16*>(&u2);
+      uint4 w1, w2;
+      __nv_bfloat16* b1 = reinterpret_cast<__nv_bfloat16*>(&w1);
+      __nv_bfloat16* b2 = reinterpret_cast<__nv_bfloat16*>(&w2);
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const float cs = cs_s[tt][c * V + e], sn = sn_s[tt][c * V + e];
+        const float x1 = to_f(a1[e]), x2 = to_f(a2[e]);
+        from_f(x1 * cs - x2 * sn, b1[e]);
+        from_f(x2 * cs + x1 * sn, b2[e]);
+      }
+      u1 = w1;
+      u2 = w2;
+    }
+    const int64_t dst = ((int64_t)h * a.cache_rows + sl) * d + c * V;
+    *reinterpret_cast<uint4*>(kc + dst) = u1;
+    *reinterpret_cast<uint4*>(kc + dst + half) = u2;
+    if (ko) {
+      *reinterpret_cast<uint4*>(ko + src) = u1;
+      *reinterpret_cast<uint4*>(ko + src + half) = u2;
+    }
+  }
+  const int vchunks = d / V;
+  const int vitems = kTok * a.heads * vchunks;
+  for (int w = threadIdx.x; w < vitems; w += blockDim.x) {
+    const int c = w % vchunks;
+    const int h = (w / vchunks) % a.heads;
+    const int tt = w / (vchunks * a.heads);
+    const int64_t sl = slot_s[tt];
+    if (sl < 0) continue;
+    const int64_t t = t0 + tt;
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(vn + (t * a.heads + h) * d + c * V));
+    *reinterpret_cast<uint4*>(vc + ((int64_t)h * a.cache_rows + sl) * d + c * V) = u;
+  }
+}
+
+cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s) {
+  InvFreq f;
+  const int half = a.head_dim / 2;
+  for (int i = 0; i < half; ++i) f.v[i] = a.base > 0.0 ? pow(a.base, -2.0 * (double)i / (double)a.head_dim) : 0.0;
+  if (a.tokens == 0) return cudaSuccess;
+  const int64_t blocks = (a.tokens + kTok - 1) / kTok;
+  kv_append_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, f);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rope(const RopeLaunch& a, cudaStream_t s) {

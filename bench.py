@@ -340,8 +340,11 @@ def long_prefill_arm(wl, args, timer, peaks, peak_src):
 def chunked_arm(wl, args, timer, peaks, peak_src):
     """Chunked prefill: 4 requests, each an 8192-token chunk over a 57344-token
     prefix in a shuffled head-major paged cache.  One step = the paged-prefix
-    call + the causal chunk call + the LSE merge of the two partial results."""
+    call + the causal chunk call + the LSE merge of the two partial results.  Also
+    timed: the serving flow of appending the chunk to the cache, then one paged
+    causal call over prefix + chunk."""
     import attention_tiled_causal_gb300 as atc
+    import synth
     inp = wl.make("cuda")
     C = wl.chunk
     q, k, v = inp["q"], inp["k"], inp["v"]
@@ -373,13 +376,40 @@ def chunked_arm(wl, args, timer, peaks, peak_src):
     ms_p, _ = timer.run(prefix, steps, warmup)
     ms_c, _ = timer.run(chunk, steps, warmup)
     ms_m, _ = timer.run(merge, steps, warmup)
+    merge_bytes = po.numel() * 4 + pl.numel() * 4 + out.numel() * 2 + lse.numel() * 4
+    del po, pl, inp
+
+    # The serving flow: append the chunk's K (rotated) and V to a paged cache that
+    # has room for it, then one paged causal call over prefix + chunk.
+    B, P = wl.batch, wl.prefix
+    table2, npg2 = synth.shuffled_page_table([P + C] * B, wl.seed * 16 + 10)
+    kc2 = synth.randn((wl.hkv, npg2, synth.PAGE, wl.d), wl.seed * 16 + 11, wl.std, device="cuda")
+    vc2 = synth.randn((wl.hkv, npg2, synth.PAGE, wl.d), wl.seed * 16 + 12, wl.std, device="cuda")
+    k_raw = synth.randn((T, wl.hkv, wl.d), wl.seed * 16 + 2, wl.std, device="cuda")  # unrotated chunk keys
+    qpos = torch.arange(P, P + C, dtype=torch.int32).repeat(B)
+    pages = torch.from_numpy(table2).long()[torch.arange(B).repeat_interleave(C), (qpos // synth.PAGE).long()]
+    slots = (pages * synth.PAGE + (qpos % synth.PAGE).long()).to(torch.int32).cuda()
+    qposd = qpos.cuda()
+    tabled = torch.from_numpy(table2).cuda()
+    klens = torch.full((B,), P + C, dtype=torch.int32, device="cuda")
+
+    def append(ev=()):
+        atc.attn_kv_append_paged(k_raw, v, qposd, slots, kc2, vc2)
+
+    def fused(ev=()):
+        append()
+        atc.attn_prefill(q, kc2, vc2, out, lse, inp_cu_q, qposd, C, page_table=tabled, k_lens=klens, num_pages=npg2)
+
+    inp_cu_q = torch.from_numpy(synth.cu_seqlens([C] * B)).cuda()
+    ms_f, _ = timer.run(fused, steps, warmup)
+    ms_a, _ = timer.run(append, steps, warmup)
     atc.attn_device_status()
+    append_bytes = 2 * 2 * k_raw.numel() * 2  # read K and V, write both into the cache
+    del kc2, vc2, k_raw, q, k, v, out, lse
     peak = peaks["bf16_tflops"]
     fl = wl.flops()
     fl_c = 4.0 * wl.d * wl.hq * wl.batch * (C * (C + 1) // 2)
     fl_p = fl - fl_c
-    merge_bytes = po.numel() * 4 + pl.numel() * 4 + out.numel() * 2 + lse.numel() * 4
-    del inp, q, k, v, po, pl, out, lse
     tf = fl / (ms * 1e-3) / 1e12
     return {"workload": wl.name + " (paged prefix + causal chunk + LSE merge)", "steps": steps, "warmup": warmup,
             "flops": fl, "ms": round(ms, 4), "value": round(tf, 2), "unit": "TFLOP/s", "frac": round(tf / peak, 4),
@@ -388,7 +418,14 @@ def chunked_arm(wl, args, timer, peaks, peak_src):
                              "unit": "TFLOP/s"},
             "causal_chunk": {"ms": round(ms_c, 4), "value": round(fl_c / (ms_c * 1e-3) / 1e12, 2),
                              "unit": "TFLOP/s"},
-            "merge": hbm_line("attn_lse_merge of the two partial results", merge_bytes, ms_m, peaks, peak_src)}
+            "merge": hbm_line("attn_lse_merge of the two partial results", merge_bytes, ms_m, peaks, peak_src),
+            "append_then_one_call": {
+                "what": "attn_kv_append_paged of the chunk (K rotated, K/V scattered into pages) + one paged causal "
+                        "call over prefix + chunk", "ms": round(ms_f, 4),
+                "value": round(fl / (ms_f * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "frac": round(fl / (ms_f * 1e-3) / 1e12 / peak, 4),
+                "append": hbm_line("attn_kv_append_paged (4 x 8192 tokens, 8 KV heads)", append_bytes, ms_a, peaks,
+                                   peak_src)}}
 
 
 def hbm_line(what, nbytes, ms, peaks, peak_src):

@@ -79,6 +79,40 @@ ATTN_API int rope_apply(void *x, attn_dtype_t dtype, int64_t tokens, int heads, 
                int64_t stride_token, const int32_t *positions, double base, void *stream);
 
 /*
+ * attn_kv_append_paged -- write a chunk of new tokens' keys and values into the
+ * head-major paged KV cache, rotating the keys (RoPE at their absolute
+ * positions) on the way.
+ *
+ * Defined by: SGLang page, section 2.1 (every new token is given a cache slot
+ * through a token-to-slot table before attention runs) and section 2.2 (a
+ * prefill chunk's K/V join the cache, where the next chunk and the decode
+ * steps read them); Ulysses page, section 2.3 (the cache is split by KV head)
+ * and section 3.2 (keys are rotated at their absolute positions).  The
+ * rotation is rope_apply's, bit for bit.
+ *
+ *  k_new, v_new  [tokens][num_kv_heads][head_dim] bf16, packed, 16-byte aligned;
+ *                k_new holds unrotated keys and is not modified.
+ *  positions     [tokens] int32 absolute position of each key (its RoPE angle).
+ *  slots         [tokens] int32 cache slot of each token, page * page_size + offset
+ *                in [0, num_pages * page_size); -1 skips the token (padding).
+ *  k_cache, v_cache  [num_kv_heads][num_pages][page_size][head_dim] bf16: token t
+ *                of KV head g goes to row g * num_pages * page_size + slots[t].
+ *  k_rot_out     NULL, or [tokens][num_kv_heads][head_dim] bf16 that also receives
+ *                the rotated keys (the chunk's own causal attention can read them
+ *                contiguously).  Skipped tokens are not written here either.
+ *  base          RoPE base (> 0), or 0 to copy the keys unrotated.
+ *  head_dim      head_dim/2 a multiple of 8, at most 256.
+ * Errors: argument errors return before launch.  A slot >= num_pages *
+ * page_size or < -1 is not written; the kernel records it and
+ * attn_device_status() reports ATTN_ERR_DEVICE.  Two tokens with the same slot
+ * race; the caller assigns distinct slots.
+ */
+ATTN_API int attn_kv_append_paged(const void *k_new, const void *v_new, const int32_t *positions,
+                                  const int32_t *slots, int64_t tokens, int num_kv_heads, int head_dim,
+                                  void *k_cache, void *v_cache, int64_t num_pages, int page_size,
+                                  void *k_rot_out, double base, void *stream);
+
+/*
  * attn_prefill -- exact causal GQA attention, FlashAttention-style tiled.
  *
  * Computes, for every query row of every sequence and every query head h in

@@ -53,6 +53,8 @@ def _load():
         lib.oracle_decode_paged.argtypes = [P, P, P, P, P, I32, I32, I32, I64, I32, I32, I32, D, P, P]
         lib.oracle_decode_paged.restype = I32
         lib.oracle_lse_merge.argtypes = [P, P, I32, I64, I32, P, P]
+        lib.oracle_kv_append.argtypes = [P, P, P, P, I64, I32, I32, P, P, I64, D]
+        lib.oracle_kv_append.restype = I32
         lib.oracle_num_threads.restype = I32
         lib.oracle_set_num_threads.argtypes = [I32]
         _lib = lib
@@ -163,3 +165,20 @@ def lse_merge(part_o, part_lse):
     lse = np.empty(lead)
     _load().oracle_lse_merge(_p(po), _p(pl), P, n, d, _p(out), _p(lse))
     return out, lse
+
+
+def kv_append(k_new, v_new, pos, slots, k_cache, v_cache, base: float = 10000.0):
+    """New tokens' keys (rotated at `pos`, rounded to bf16) and values into copies of
+    the head-major paged caches [heads][num_pages][page_size][d] at `slots`
+    (page * page_size + offset; -1 skips).  Returns (k_cache, v_cache, n_bad_slots)."""
+    k_new, v_new = _f64(k_new), _f64(v_new)
+    T, H, d = k_new.shape
+    kc, vc = np.array(k_cache, dtype=np.float64, copy=True), np.array(v_cache, dtype=np.float64, copy=True)
+    rows = kc.shape[1] * kc.shape[2]
+    pos = _i32(pos if pos is not None else np.zeros(T, np.int32))
+    slots = _i32(slots)
+    bad = _load().oracle_kv_append(_p(k_new), _p(v_new), _p(pos), _p(slots), T, H, d, _p(kc), _p(vc), rows,
+                                   float(base))
+    if bad < 0:
+        raise MemoryError("oracle_kv_append: out of memory")
+    return kc, vc, bad

@@ -203,6 +203,47 @@ int oracle_gather_pages(const double *cache, const int32_t *page_table, int max_
     return 0;
 }
 
+/* Append new tokens to the head-major paged cache (SGLang page, sections 2.1
+ * and 2.2: each new token is given a cache slot, page * page_size + offset,
+ * and its K/V are written there before attention reads them; Ulysses page,
+ * section 2.3: one pool per KV head; section 3.2: keys rotated at their
+ * absolute positions).
+ *   k_new, v_new [tokens][heads][d]; pos [tokens]; slots [tokens]
+ *   k_cache, v_cache [heads][rows][d], rows = num_pages * page_size
+ * Key rows are rotated (when base > 0) and rounded to bf16, as the path stores
+ * them; value rows are copied.  Slot -1 skips a token.  Returns the number of
+ * tokens whose slot lies outside [-1, rows); those are skipped too. */
+int oracle_kv_append(const double *k_new, const double *v_new, const int32_t *pos, const int32_t *slots,
+                     int64_t tokens, int heads, int d, double *k_cache, double *v_cache, int64_t rows,
+                     double base)
+{
+    int bad = 0;
+    double *krow = malloc((size_t)d * sizeof(double));
+    if (!krow) return -1;
+    for (int64_t t = 0; t < tokens; ++t) {
+        const int64_t s = slots[t];
+        if (s == -1) continue;
+        if (s < -1 || s >= rows) { ++bad; continue; }
+        for (int h = 0; h < heads; ++h) {
+            const double *src = k_new + (t * heads + h) * (int64_t)d;
+            for (int i = 0; i < d; ++i) krow[i] = src[i];
+            if (base > 0.0) {
+                oracle_rope(krow, 1, 1, d, pos + t, base);
+                oracle_round_bf16(krow, d);
+            }
+            double *kd = k_cache + ((int64_t)h * rows + s) * d;
+            double *vd = v_cache + ((int64_t)h * rows + s) * d;
+            const double *vs = v_new + (t * heads + h) * (int64_t)d;
+            for (int i = 0; i < d; ++i) {
+                kd[i] = krow[i];
+                vd[i] = vs[i];
+            }
+        }
+    }
+    free(krow);
+    return bad;
+}
+
 /* Decode: q [B][hq][d] (already rotated, at position ctx_b - 1) against the
  * ctx_b cached tokens of request b.  out [B][hq][d], lse [B][hq]. */
 int oracle_decode_paged(const double *q, const double *k_cache, const double *v_cache,

@@ -102,3 +102,28 @@ def test_rope_and_merge_reject_bad_arguments(lib):
     assert lib.rope_apply(16, 0, 0, 2, 128, 256, 16, 1e4, None) == 0          # nothing to do
     assert lib.attn_lse_merge(16, 16, 0, 4, 2, 128, 0, 0, 0, 0, 0, 0, 16, 0, None, None) == ERR_ARG
     assert lib.attn_lse_merge(16, 16, 2, 0, 2, 128, 0, 0, 0, 0, 0, 0, 16, 0, None, None) == 0
+
+
+def test_kv_append_rejects_bad_arguments(lib):
+    base = dict(kn=16, vn=16, pos=16, slots=16, T=4, H=8, d=128, kc=16, vc=16, pages=10, page=64, ko=None,
+                rope_base=1e4, stream=None)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        f = lib.attn_kv_append_paged
+        f.argtypes = [C.c_void_p] * 4 + [C.c_int64, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int64, C.c_int,
+                                         C.c_void_p, C.c_double, C.c_void_p]
+        return f(*a.values())
+
+    assert call(d=100) == ERR_SHAPE          # half of 100 is not a multiple of 8
+    assert call(d=512) == ERR_SHAPE
+    assert call(rope_base=-1.0) == ERR_ARG
+    assert call(T=-1) == ERR_ARG
+    assert call(slots=None) == ERR_ARG
+    assert call(pos=None) == ERR_ARG         # rotation needs positions
+    assert call(pages=0) == ERR_ARG
+    assert call(kc=24) == ERR_ALIGN
+    assert call(ko=8) == ERR_ALIGN
+    assert call(T=0) == 0
+    assert call(H=0) == 0

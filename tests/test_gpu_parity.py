@@ -463,3 +463,134 @@ def test_prefill_tc_is_deterministic_across_runs():
     for _ in range(3):
         o, l = _run_prefill(q, k, v, pos, cu, lens)
         assert torch.equal(o, first[0]) and torch.equal(l, first[1])
+
+
+# ------------------------------------------------------------------ append to the paged cache
+
+def _slots_for(table, b, positions, page=64):
+    return np.array([table[b, p // page] * page + p % page for p in positions], np.int32)
+
+
+def _append_inputs(prefix, chunk, hkv, d, seed, pad=0):
+    table, num_pages = synth.shuffled_page_table([p + c for p, c in zip(prefix, chunk)], seed)
+    kc0 = synth.randn((hkv, num_pages, 64, d), seed + 1, 0.7071)
+    vc0 = synth.randn((hkv, num_pages, 64, d), seed + 2, 0.7071)
+    T = sum(chunk) + pad
+    kn = synth.randn((T, hkv, d), seed + 3, 0.7071)
+    vn = synth.randn((T, hkv, d), seed + 4, 0.7071)
+    pos, slots = [], []
+    for b, (p, c) in enumerate(zip(prefix, chunk)):
+        pp = np.arange(p, p + c, dtype=np.int32)
+        pos.append(pp)
+        slots.append(_slots_for(table, b, pp))
+    pos.append(np.zeros(pad, np.int32))
+    slots.append(np.full(pad, -1, np.int32))
+    return table, num_pages, kc0, vc0, kn, vn, np.concatenate(pos), np.concatenate(slots)
+
+
+def test_kv_append_matches_oracle_and_rope_apply():
+    """A 3-request chunk plus 3 padding tokens (slot -1), appended after prefixes of
+    64, 130 and 0 tokens through a shuffled page table.  Values land bit-exactly,
+    keys within one bf16 ulp of the oracle's rounded rotation and bit-identical
+    to rope_apply; every other cache row is untouched."""
+    hkv, d = 8, 128
+    table, num_pages, kc0, vc0, kn, vn, pos, slots = _append_inputs([64, 130, 0], [100, 1, 260], hkv, d, 95, pad=3)
+    T = kn.shape[0]
+    kc, vc = kc0.to(DEV), vc0.to(DEV)
+    ko = torch.full((T, hkv, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    posd, slotd = torch.from_numpy(pos).to(DEV), torch.from_numpy(slots).to(DEV)
+    atc.attn_kv_append_paged(kn.to(DEV), vn.to(DEV), posd, slotd, kc, vc, k_rot_out=ko)
+    atc.attn_device_status()
+    wk, wv, bad = oracle.kv_append(synth.as_f64(kn), synth.as_f64(vn), pos, slots, synth.as_f64(kc0),
+                                   synth.as_f64(vc0))
+    assert bad == 0
+    np.testing.assert_array_equal(synth.as_f64(vc.cpu()), wv)
+    got = synth.as_f64(kc.cpu()).reshape(hkv, -1, d)
+    want = wk.reshape(hkv, -1, d)
+    written = np.zeros(got.shape[1], bool)
+    written[slots[slots >= 0]] = True
+    np.testing.assert_array_equal(got[:, ~written], want[:, ~written])
+    diff = np.abs(got[:, written] - want[:, written])
+    bound = np.abs(want[:, written]) * 2.0 ** -7 + 2e-6
+    assert (diff <= bound).all()
+    assert (diff > 0).mean() < 0.01
+    kr = kn.to(DEV).clone()
+    atc.rope_apply(kr, posd)
+    valid = torch.from_numpy(slots >= 0).to(DEV)
+    assert torch.equal(ko[valid], kr[valid])
+    assert torch.isnan(ko[~valid].float()).all()
+    rows = torch.from_numpy(slots[slots >= 0].astype(np.int64)).to(DEV)
+    assert torch.equal(kc.reshape(hkv, -1, d)[:, rows].permute(1, 0, 2), kr[valid])
+
+
+def test_kv_append_reports_slot_outside_the_cache():
+    """A slot past the cache is not written; the device records it and the host
+    reports it.  The other tokens are written (base 0: a plain copy)."""
+    hkv, d = 2, 128
+    kc = torch.zeros((hkv, 2, 64, d), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    kn = synth.randn((3, hkv, d), 540, 0.7071).to(DEV)
+    vn = synth.randn((3, hkv, d), 541, 0.7071).to(DEV)
+    slots = torch.tensor([5, 128, 7], dtype=torch.int32, device=DEV)  # 128 = num_pages * page_size
+    atc.attn_kv_append_paged(kn, vn, None, slots, kc, vc, base=0.0)
+    with pytest.raises(atc.AttnError) as e:
+        atc.attn_device_status(clear=True)
+    assert e.value.status == 6
+    atc.attn_device_status(clear=True)
+    flat_k, flat_v = kc.reshape(hkv, -1, d), vc.reshape(hkv, -1, d)
+    assert torch.equal(flat_k[:, 5], kn[0]) and torch.equal(flat_k[:, 7], kn[2])
+    assert torch.equal(flat_v[:, 5], vn[0]) and torch.equal(flat_v[:, 7], vn[2])
+    written = torch.zeros(flat_k.shape[1], dtype=torch.bool, device=DEV)
+    written[[5, 7]] = True
+    assert (flat_k[:, ~written] == 0).all() and (flat_v[:, ~written] == 0).all()
+
+
+def test_chunked_prefill_through_append_is_one_paged_call():
+    """Chunked prefill as a serving engine runs it: append the chunk's K/V to the
+    paged cache, then one paged causal call over prefix + chunk (cached token j
+    sits at position j).  Matches the oracle over the gathered keys, and the
+    two-call (paged prefix + contiguous chunk) + LSE merge path."""
+    prefix, chunk, hq, hkv, d = [100, 300], [150, 64], 16, 2, 128
+    table, num_pages, kc0, vc0, kn, vn, pos, slots = _append_inputs(prefix, chunk, hkv, d, 550)
+    T = kn.shape[0]
+    q = synth.randn((T, hq, d), 556, 0.7071)
+    posd, slotd = torch.from_numpy(pos).to(DEV), torch.from_numpy(slots).to(DEV)
+    cu_q = torch.from_numpy(synth.cu_seqlens(chunk)).to(DEV)
+    tabled = torch.from_numpy(table).to(DEV)
+    kc, vc = kc0.to(DEV), vc0.to(DEV)
+    qd = q.to(DEV)
+    atc.rope_apply(qd, posd)
+    kr = torch.empty((T, hkv, d), dtype=torch.bfloat16, device=DEV)
+    atc.attn_kv_append_paged(kn.to(DEV), vn.to(DEV), posd, slotd, kc, vc, k_rot_out=kr)
+    out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((T, hq), dtype=torch.float32, device=DEV)
+    full = torch.tensor([p + c for p, c in zip(prefix, chunk)], dtype=torch.int32, device=DEV)
+    atc.attn_prefill(qd, kc, vc, out, lse, cu_q, posd, max(chunk), page_table=tabled, k_lens=full,
+                     num_pages=num_pages)
+    # the same through the two-call path: paged prefix only, then the contiguous chunk, then a merge
+    po = torch.empty((2, T, hq, d), dtype=torch.float32, device=DEV)
+    pl = torch.empty((2, T, hq), dtype=torch.float32, device=DEV)
+    pre = torch.tensor(prefix, dtype=torch.int32, device=DEV)
+    atc.attn_prefill(qd, kc, vc, po[0], pl[0], cu_q, posd, max(chunk), page_table=tabled, k_lens=pre,
+                     num_pages=num_pages)
+    atc.attn_prefill(qd, kr, vn.to(DEV), po[1], pl[1], cu_q, posd, max(chunk), cu_k=cu_q, k_pos=posd)
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    atc.attn_lse_merge(po, pl, out2, lse2)
+    atc.attn_device_status()
+    # oracle: the appended cache (oracle's own append), gathered in logical order
+    wk, wv, _ = oracle.kv_append(synth.as_f64(kn), synth.as_f64(vn), pos, slots, synth.as_f64(kc0),
+                                 synth.as_f64(vc0))
+    qr = rotated_bf16(q, pos)
+    want_o = np.empty((T, hq, d))
+    want_l = np.empty((T, hq))
+    o0 = 0
+    for b, (p, c) in enumerate(zip(prefix, chunk)):
+        K = np.stack([oracle.gather_pages(wk, table, num_pages, g, b, p + c) for g in range(hkv)], 1)
+        V = np.stack([oracle.gather_pages(wv, table, num_pages, g, b, p + c) for g in range(hkv)], 1)
+        o, l = oracle.attention(qr[o0:o0 + c], np.zeros(c, np.int32), pos[o0:o0 + c], K, V, [0, p + c],
+                                np.arange(p + c, dtype=np.int32), d ** -0.5)
+        want_o[o0:o0 + c], want_l[o0:o0 + c] = o, l
+        o0 += c
+    check(out, lse, want_o, want_l, what="append + one paged call")
+    check(out2, lse2, want_o, want_l, what="two calls + merge")

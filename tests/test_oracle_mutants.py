@@ -23,6 +23,10 @@ MUTANTS = [
     ("decode query position", "ctx, ctx - 1, 1, d,", "ctx, ctx - 2, 1, d,", False),
     ("page slot index", "(j % page)) * (int64_t)d;", "(j / page)) * (int64_t)d;", False),
     ("bf16 ulp", "int q = e - 8;", "int q = e - 9;", False),
+    ("append row of head", "double *kd = k_cache + ((int64_t)h * rows + s) * d;",
+     "double *kd = k_cache + ((int64_t)s * heads + h) * d;", False),
+    ("append rotates values", "const double *vs = v_new + (t * heads + h) * (int64_t)d;",
+     "const double *vs = krow - (int64_t)0 * (t * heads + h);", False),
 ]
 
 

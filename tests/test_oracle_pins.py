@@ -406,3 +406,81 @@ def test_decode_invariant_under_page_permutation_and_request_order():
     o3, l3 = oracle.decode_paged(q[order], kc, vc, table[order], np.array(ctx)[order], num_pages, 0.25)
     np.testing.assert_array_equal(o3, o[order])
     np.testing.assert_array_equal(l3, l[order])
+
+
+# ------------------------------------------------------------ append to the paged cache
+
+def _append_case(seed, T=3, H=2, d=4, pages=3, page=2):
+    rng = np.random.default_rng(seed)
+    kn = rng.normal(0, 1, (T, H, d))
+    vn = rng.normal(0, 1, (T, H, d))
+    kc = np.full((H, pages, page, d), 7.0)
+    vc = np.full((H, pages, page, d), -7.0)
+    return kn, vn, kc, vc
+
+
+def test_kv_append_places_rows_by_slot_and_skips_minus_one():
+    """Hand placement, base 0 (plain copy): slot s of head h is row s of that
+    head's pool; slot -1 leaves the cache alone; every other row keeps its value."""
+    kn, vn, kc, vc = _append_case(90)
+    k2, v2, bad = oracle.kv_append(kn, vn, None, [5, -1, 0], kc, vc, base=0.0)
+    assert bad == 0
+    want_k, want_v = kc.copy(), vc.copy()
+    for h in range(2):
+        want_k[h, 2, 1] = kn[0, h]   # slot 5 = page 2, offset 1
+        want_v[h, 2, 1] = vn[0, h]
+        want_k[h, 0, 0] = kn[2, h]   # slot 0 = page 0, offset 0
+        want_v[h, 0, 0] = vn[2, h]
+    np.testing.assert_array_equal(k2, want_k)
+    np.testing.assert_array_equal(v2, want_v)
+
+
+def test_kv_append_counts_and_skips_out_of_range_slots():
+    kn, vn, kc, vc = _append_case(91)
+    k2, v2, bad = oracle.kv_append(kn, vn, None, [6, -2, 3], kc, vc, base=0.0)
+    assert bad == 2
+    want_k = kc.copy()
+    want_k[:, 1, 1] = kn[2]
+    np.testing.assert_array_equal(k2, want_k)
+    np.testing.assert_array_equal(v2[:, 1, 1], vn[2])
+
+
+def test_kv_append_d2_key_is_bf16_of_plane_rotation():
+    """d = 2: the stored key is the plane rotation of (x, y) by the position
+    (theta_0 = 1), rounded to bf16 by torch's own conversion."""
+    rng = np.random.default_rng(92)
+    T = 6
+    kn = rng.normal(0, 1, (T, 1, 2))
+    vn = rng.normal(0, 1, (T, 1, 2))
+    pos = np.array([0, 1, 5, 17, 1000, 65535], np.int32)
+    kc = np.zeros((1, 2, 4, 2))
+    k2, v2, bad = oracle.kv_append(kn, vn, pos, np.arange(T, dtype=np.int32), kc, kc, base=10000.0)
+    assert bad == 0
+    for t in range(T):
+        x, y, p = kn[t, 0, 0], kn[t, 0, 1], float(pos[t])
+        rot = torch.tensor([x * math.cos(p) - y * math.sin(p), y * math.cos(p) + x * math.sin(p)],
+                           dtype=torch.float64).to(torch.bfloat16).double().numpy()
+        np.testing.assert_array_equal(k2.reshape(-1, 2)[t], rot)
+        np.testing.assert_array_equal(v2.reshape(-1, 2)[t], vn[t, 0])
+
+
+def test_kv_append_then_gather_returns_the_chunk_in_order():
+    """A chunk appended after a prefix through a shuffled page table comes back,
+    token by token, from the page gather of that request."""
+    P, C, H, d, page = 5, 11, 2, 8, 4
+    table, num_pages = synth.shuffled_page_table([P + C], 93, page=page)
+    rng = np.random.default_rng(94)
+    kc = rng.normal(0, 1, (H, num_pages, page, d))
+    vc = rng.normal(0, 1, (H, num_pages, page, d))
+    kn = rng.normal(0, 1, (C, H, d))
+    vn = rng.normal(0, 1, (C, H, d))
+    pos = np.arange(P, P + C, dtype=np.int32)
+    slots = np.array([table[0, p // page] * page + p % page for p in pos], np.int32)
+    k2, v2, bad = oracle.kv_append(kn, vn, pos, slots, kc, vc, base=0.0)
+    assert bad == 0
+    for g in range(H):
+        gk = oracle.gather_pages(k2, table, num_pages, g, 0, P + C)
+        gv = oracle.gather_pages(v2, table, num_pages, g, 0, P + C)
+        np.testing.assert_array_equal(gk[P:], kn[:, g])
+        np.testing.assert_array_equal(gv[P:], vn[:, g])
+        np.testing.assert_array_equal(gk[:P], oracle.gather_pages(kc, table, num_pages, g, 0, P))
