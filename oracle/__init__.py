@@ -55,6 +55,7 @@ def _load():
         lib.oracle_lse_merge.argtypes = [P, P, I32, I64, I32, P, P]
         lib.oracle_kv_append.argtypes = [P, P, P, P, I64, I32, I32, P, P, I64, D]
         lib.oracle_kv_append.restype = I32
+        lib.oracle_dequant_int8.argtypes = [P, P, I64, I32, P]
         lib.oracle_num_threads.restype = I32
         lib.oracle_set_num_threads.argtypes = [I32]
         _lib = lib
@@ -182,3 +183,17 @@ def kv_append(k_new, v_new, pos, slots, k_cache, v_cache, base: float = 10000.0)
     if bad < 0:
         raise MemoryError("oracle_kv_append: out of memory")
     return kc, vc, bad
+
+
+def dequant_int8(codes, scales) -> np.ndarray:
+    """Exact values of an INT8 cache: codes [..., d] int8 times scales [...] fp32
+    (one scale per cached token of a KV head)."""
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    if codes.shape[:-1] != scales.shape:
+        raise ValueError("scales must have the codes' shape without the last axis")
+    d = codes.shape[-1]
+    rows = int(np.prod(codes.shape[:-1]))
+    out = np.empty(codes.shape, dtype=np.float64)
+    _load().oracle_dequant_int8(_p(codes), _p(scales), rows, d, _p(out))
+    return out

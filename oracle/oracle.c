@@ -244,6 +244,18 @@ int oracle_kv_append(const double *k_new, const double *v_new, const int32_t *po
     return bad;
 }
 
+/* INT8 KV cache (Flash Attention page, section 18.12: an INT8 cache halves the
+ * bytes per cached token; Ulysses page, section 5.4: a quantised cache stores
+ * grouped codes with their scales).  Symmetric codes with one scale per (KV
+ * head, cached token): the value is code * scale, computed here exactly.
+ *   codes [rows][d] int8, scales [rows] fp32 -> out [rows][d] */
+void oracle_dequant_int8(const int8_t *codes, const float *scales, int64_t rows, int d, double *out)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int i = 0; i < d; ++i)
+            out[r * d + i] = (double)codes[r * d + i] * (double)scales[r];
+}
+
 /* Decode: q [B][hq][d] (already rotated, at position ctx_b - 1) against the
  * ctx_b cached tokens of request b.  out [B][hq][d], lse [B][hq]. */
 int oracle_decode_paged(const double *q, const double *k_cache, const double *v_cache,

@@ -25,6 +25,7 @@ MUTANTS = [
     ("bf16 ulp", "int q = e - 8;", "int q = e - 9;", False),
     ("append row of head", "double *kd = k_cache + ((int64_t)h * rows + s) * d;",
      "double *kd = k_cache + ((int64_t)s * heads + h) * d;", False),
+    ("int8 scale of the wrong token", "(double)scales[r];", "(double)scales[r > 0 ? r - 1 : r];", False),
     ("append rotates values", "const double *vs = v_new + (t * heads + h) * (int64_t)d;",
      "const double *vs = krow - (int64_t)0 * (t * heads + h);", False),
 ]

@@ -484,3 +484,41 @@ def test_kv_append_then_gather_returns_the_chunk_in_order():
         np.testing.assert_array_equal(gk[P:], kn[:, g])
         np.testing.assert_array_equal(gv[P:], vn[:, g])
         np.testing.assert_array_equal(gk[:P], oracle.gather_pages(kc, table, num_pages, g, 0, P))
+
+
+# ------------------------------------------------------------ INT8 cache values
+
+def test_dequant_int8_hand_values():
+    codes = np.array([[[1, -1, 127, -127], [0, 5, -6, 64]]], np.int8)       # [1 head][2 tokens][d = 4]
+    scales = np.array([[0.5, 0.125]], np.float32)
+    want = np.array([[[0.5, -0.5, 63.5, -63.5], [0.0, 0.625, -0.75, 8.0]]])
+    np.testing.assert_array_equal(oracle.dequant_int8(codes, scales), want)
+
+
+def test_dequant_int8_is_exact_product():
+    """Every value is code * scale exactly: an 8-bit integer times an fp32 scale
+    needs at most 32 significant bits, so fp64 holds it without rounding."""
+    rng = np.random.default_rng(96)
+    codes = rng.integers(-127, 128, (3, 5, 16)).astype(np.int8)
+    scales = rng.uniform(1e-3, 2.0, (3, 5)).astype(np.float32)
+    got = oracle.dequant_int8(codes, scales)
+    from fractions import Fraction
+    for idx in [(0, 0, 0), (1, 2, 3), (2, 4, 15), (0, 3, 7)]:
+        assert Fraction(got[idx]) == Fraction(int(codes[idx])) * Fraction(float(scales[idx[:2]]))
+
+
+def test_decode_over_unit_scale_int8_cache_is_decode_over_the_codes():
+    """With every scale 1 the INT8 cache holds the codes themselves: decode over
+    the dequantised cache equals decode over the codes as numbers."""
+    ctx = [70, 3]
+    q, kc, vc, table, num_pages = _decode_case(97, ctx)
+    rng = np.random.default_rng(98)
+    kq = rng.integers(-127, 128, kc.shape).astype(np.int8)
+    vq = rng.integers(-127, 128, vc.shape).astype(np.int8)
+    ones = np.ones(kc.shape[:-1], np.float32)
+    a = oracle.decode_paged(q / 64.0, oracle.dequant_int8(kq, ones), oracle.dequant_int8(vq, ones), table,
+                            np.array(ctx, np.int32), num_pages, 0.1)
+    b = oracle.decode_paged(q / 64.0, kq.astype(np.float64), vq.astype(np.float64), table,
+                            np.array(ctx, np.int32), num_pages, 0.1)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
