@@ -12,12 +12,14 @@ Entry points (same names as the C ABI):
                                                         new K (rotated) / V into the paged cache
     attn_prefill(q, k, v, out, lse, cu_q, q_pos, ...)   tiled causal GQA attention
     attn_decode_paged(q, k_cache, v_cache, ...)         split-KV decode over a paged cache
+    attn_decode_paged_int8(q, k_codes, v_codes, k_scale, v_scale, ...)   the same over an INT8 cache
     attn_lse_merge(part_out, part_lse, out, lse, ...)   log-sum-exp merge of partials
 """
-from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_device_status,
+from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_decode_paged_int8,
+                       attn_device_status,
                        attn_kv_append_paged, attn_lse_merge, attn_prefill, decode_workspace, lib_path, library,
                        prefill, rope_apply)
 
-__all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_device_status",
+__all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_decode_paged_int8", "attn_device_status",
            "attn_kv_append_paged", "attn_lse_merge", "attn_prefill", "decode_workspace", "lib_path", "library",
            "prefill", "rope_apply"]

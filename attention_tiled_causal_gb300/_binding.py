@@ -50,6 +50,9 @@ def library():
     lib.attn_decode_paged.argtypes = [P, P, P, P, P, I32, I32, I32, I64, I32, I32, I32, I32, F32, P, P, P, I32,
                                       P, P]
     lib.attn_decode_paged.restype = I32
+    lib.attn_decode_paged_int8.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I64, I32, I32, I32, I32, F32, P, P,
+                                           P, I32, P, P]
+    lib.attn_decode_paged_int8.restype = I32
     lib.attn_lse_merge.argtypes = [P, P, I32, I64, I32, I32, I64, I64, I64, I64, I64, I64, P, I32, P, P]
     lib.attn_lse_merge.restype = I32
     _lib = lib
@@ -214,6 +217,37 @@ def attn_decode_paged(q, k_cache, v_cache, page_table, ctx_lens, num_splits: int
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(_i32(ctx_lens, "ctx_lens")), B,
         page_table.shape[1], page, npg, hq, hkv, d, int(num_splits), float(scale), _ptr(part_out),
         _ptr(part_lse), _ptr(out), _dt(out) if out is not None else 0, _ptr(lse), _stream(stream)))
+
+
+def attn_decode_paged_int8(q, k_cache, v_cache, k_scale, v_scale, page_table, ctx_lens, num_splits: int,
+                           part_out, part_lse, out=None, lse=None, scale: Optional[float] = None,
+                           stream=None) -> None:
+    """Split-KV decode over an INT8 cache.  q [B, Hq, d] bf16 (rotated); code caches
+    [Hkv, num_pages, page, d] int8 and scales [Hkv, num_pages, page] fp32 (value =
+    code * scale); page_table [B, max_pages]; ctx_lens [B]; partial workspaces from
+    decode_workspace()."""
+    B, hq, d = q.shape
+    hkv, npg, page, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent cache shapes")
+    if k_cache.dtype != torch.int8 or v_cache.dtype != torch.int8:
+        raise ValueError("code caches must be int8")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t.dtype != torch.float32 or tuple(t.shape) != (hkv, npg, page) or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous float32 [Hkv, num_pages, page] tensor")
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (part_out, "part_out"),
+                 (part_lse, "part_lse")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if tuple(part_out.shape) != (B, hq, num_splits, d) or tuple(part_lse.shape) != (B, hq, num_splits):
+        raise ValueError("workspace shapes must be [B, Hq, splits, d] and [B, Hq, splits]")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    page_table = _i32(page_table, "page_table")
+    _check(library().attn_decode_paged_int8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(page_table),
+        _ptr(_i32(ctx_lens, "ctx_lens")), B, page_table.shape[1], page, npg, hq, hkv, d, int(num_splits),
+        float(scale), _ptr(part_out), _ptr(part_lse), _ptr(out), _dt(out) if out is not None else 0, _ptr(lse),
+        _stream(stream)))
 
 
 def attn_lse_merge(part_out, part_lse, out, lse=None, stream=None) -> None:

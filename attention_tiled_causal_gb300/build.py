@@ -18,7 +18,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattn_gb300.so")
-SOURCES = ["api.cu", "rope.cu", "merge.cu", "prefill_simt.cu", "prefill_tc.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "rope.cu", "merge.cu", "prefill_simt.cu", "prefill_tc.cu", "decode.cu", "decode_noalloc.cu",
+           "decode_int8.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -76,17 +76,22 @@ int get_encode(EncodeTiledFn* fn) {
 }
 
 // bf16 tensor map, 128-byte swizzle, box of 64 elements along the innermost dim.
-int encode_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
-                const cuuint32_t* box) {
+int encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank, const cuuint64_t* dims,
+                 const cuuint64_t* strides_bytes, const cuuint32_t* box) {
   EncodeTiledFn fn;
   int rc = get_encode(&fn);
   if (rc) return rc;
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes,
+  CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
   return ATTN_OK;
+}
+
+int encode_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+                const cuuint32_t* box) {
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box);
 }
 
 // [tokens][heads][128] bf16, box (64 dims, 1 head, 128 tokens).
@@ -103,6 +108,14 @@ int map_pages(CUtensorMap* m, const void* base, int hkv, int64_t num_pages) {
   cuuint64_t strides[1] = {128 * 2};
   cuuint32_t box[2] = {64, 64};
   return encode_bf16(m, base, 2, dims, strides, box);
+}
+
+// head-major paged INT8 cache [hkv][num_pages][64][128] as rows of 128 bytes, box (128 bytes, 64 rows).
+int map_pages_i8(CUtensorMap* m, const void* base, int hkv, int64_t num_pages) {
+  cuuint64_t dims[2] = {128, (cuuint64_t)hkv * (cuuint64_t)num_pages * 64};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, 64};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box);
 }
 
 // ATTN_GB300_FORCE_SIMT=1 routes bf16 prefill to the CUDA-core kernel, so the
@@ -308,6 +321,49 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, c
                       1, num_q_heads * S, S, out, out_dtype == ATTN_FP32 ? 1 : 0, lse};
   e = attn::launch_lse_merge(m, (cudaStream_t)stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode_paged merge launch");
+}
+
+int attn_decode_paged_int8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                           const float* v_scale, const int32_t* page_table, const int32_t* ctx_lens, int batch,
+                           int max_pages, int page_size, int64_t num_pages, int num_q_heads, int num_kv_heads,
+                           int head_dim, int num_splits, float scale, float* part_out, float* part_lse, void* out,
+                           attn_dtype_t out_dtype, float* lse, void* stream) {
+  if (batch < 0) return fail(ATTN_ERR_ARG, "attn_decode_paged_int8: negative batch");
+  if (num_kv_heads <= 0 || num_q_heads != 8 * num_kv_heads)
+    return fail(ATTN_ERR_SHAPE, "attn_decode_paged_int8: needs 8 query heads per KV head (got %d/%d)", num_q_heads,
+                num_kv_heads);
+  if (head_dim != 128) return fail(ATTN_ERR_SHAPE, "attn_decode_paged_int8: head_dim %d (need 128)", head_dim);
+  if (page_size != 64) return fail(ATTN_ERR_SHAPE, "attn_decode_paged_int8: page_size %d (need 64)", page_size);
+  if (num_splits < 1 || num_splits > 256)
+    return fail(ATTN_ERR_ARG, "attn_decode_paged_int8: num_splits %d", num_splits);
+  if (out && out_dtype != ATTN_BF16 && out_dtype != ATTN_FP32)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_paged_int8: out_dtype");
+  if (!(scale > 0.f)) return fail(ATTN_ERR_ARG, "attn_decode_paged_int8: scale must be positive");
+  if (batch == 0) return ATTN_OK;
+  if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !page_table || !ctx_lens || !part_out || !part_lse)
+    return fail(ATTN_ERR_ARG, "attn_decode_paged_int8: null pointer");
+  if (max_pages <= 0 || num_pages <= 0) return fail(ATTN_ERR_ARG, "attn_decode_paged_int8: max_pages/num_pages");
+  if ((int64_t)num_kv_heads * num_pages * page_size > 0x7fffffffLL)
+    return fail(ATTN_ERR_ARG, "attn_decode_paged_int8: cache has more than 2^31-1 rows");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) || !aligned16(v_scale) ||
+      !aligned16(part_out))
+    return fail(ATTN_ERR_ALIGN, "attn_decode_paged_int8: q / caches / scales / part_out must be 16-byte aligned");
+  unsigned* err = nullptr;
+  int rc = device_error_ptr(&err);
+  if (rc) return rc;
+  CUtensorMap tk, tv;
+  if ((rc = map_pages_i8(&tk, k_cache, num_kv_heads, num_pages))) return rc;
+  if ((rc = map_pages_i8(&tv, v_cache, num_kv_heads, num_pages))) return rc;
+  attn::DecodeLaunch a{q, page_table, ctx_lens, batch, max_pages, num_pages, num_q_heads, num_kv_heads, num_splits,
+                       scale, part_out, part_lse, err};
+  cudaError_t e = attn::launch_decode_split_int8(a, k_scale, v_scale, tk, tv, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode_paged_int8 launch");
+  if (!out) return ATTN_OK;
+  const int64_t S = num_splits, d = head_dim;
+  attn::MergeLaunch m{part_out, part_lse, num_splits, batch, num_q_heads, head_dim, d, num_q_heads * S * d, S * d,
+                      1, num_q_heads * S, S, out, out_dtype == ATTN_FP32 ? 1 : 0, lse};
+  e = attn::launch_lse_merge(m, (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode_paged_int8 merge launch");
 }
 
 }  // extern "C"

@@ -22,6 +22,7 @@ enum DeviceError : unsigned {
   DEV_TIMEOUT_DECODE = 0x104,   // decode consumer / producer wait ran out
   DEV_BAD_PAGE = 0x201,         // page-table entry outside [0, num_pages)
   DEV_BAD_SLOT = 0x202,         // cache slot outside [-1, num_pages * page_size)
+  DEV_FP16_RANGE = 0x203,       // a value the INT8 decode feeds the fp16 MMAs exceeds 65504
 };
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait

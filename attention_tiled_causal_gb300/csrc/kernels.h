@@ -85,6 +85,8 @@ struct DecodeLaunch {
 };
 cudaError_t launch_decode_split(const DecodeLaunch& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t s);
+cudaError_t launch_decode_split_int8(const DecodeLaunch& a, const float* k_scale, const float* v_scale,
+                                     const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s);
 
 // Records `msg` as this thread's attn_last_error() text and returns `code`.
 int set_last_error(int code, const char* msg);

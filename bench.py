@@ -428,6 +428,48 @@ def chunked_arm(wl, args, timer, peaks, peak_src):
                                    peak_src)}}
 
 
+def decode_int8_arm(wl, args, timer, peaks, peak_src):
+    """The decode workload over an INT8 cache (codes + one fp32 scale per KV head and
+    token): half the bytes per cached token."""
+    import attention_tiled_causal_gb300 as atc
+    inp = wl.make("cuda")
+    q = inp["q"]
+    po, pl = atc.decode_workspace(wl.batch, wl.hq, wl.splits, wl.d, "cuda")
+    out = torch.empty((wl.batch, wl.hq, wl.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((wl.batch, wl.hq), dtype=torch.float32, device="cuda")
+
+    def step(ev=()):
+        atc.rope_apply(q, inp["q_pos"])
+        if ev:
+            ev[0].record()
+        atc.attn_decode_paged_int8(q, inp["k_cache"], inp["v_cache"], inp["k_scale"], inp["v_scale"],
+                                   inp["page_table"], inp["ctx_lens"], wl.splits, po, pl, out, lse)
+        if ev:
+            ev[1].record()
+
+    ms, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
+    atc.attn_device_status()
+    kv = wl.kv_bytes()
+    part = wl.batch * wl.hq * wl.splits * (wl.d + 1) * 4
+    qb = wl.batch * wl.hq * wl.d * 2
+    outb = wl.batch * wl.hq * (wl.d * 2 + 4)
+    alg_step = kv + qb + 2 * part + outb
+    peak = peaks["hbm_gbs"]
+    achieved = alg_step / (ms_kernel * 1e-3) / 1e9
+    tokens = int(wl.ctx_lens().astype(np.int64).sum())
+    del inp
+    return {
+        "metric": "decode KV-read GB/s", "unit": "GB/s", "value": round(kv / (ms * 1e-3) / 1e9, 1),
+        "ms_per_step": round(ms, 4), "kv_bytes_per_step": kv, "workload": wl.name,
+        "cached_tokens_per_s": round(tokens / (ms * 1e-3), 0),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "attn::dec8::decode_split_int8_kernel + attn::lse_merge_kernel",
+                     "kernel_ms": round(ms_kernel, 4), "peak_source": f"{peak_src} HBM copy"},
+        "gpu_launches_per_step": 3,
+    }
+
+
 def hbm_line(what, nbytes, ms, peaks, peak_src):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"what": what, "bytes": int(nbytes), "ms": round(ms, 4), "value": round(gbs, 1), "unit": "GB/s",
@@ -521,6 +563,15 @@ def main():
             dwl = dataclasses.replace(dwl, batch=args.decode_requests,
                                       name=dwl.name.replace("B32", f"B{args.decode_requests}"))
         dec = decode_arm(dwl, args, timer, peaks, peak_src)
+        torch.cuda.empty_cache()
+        dwl8 = synth.DECODE_INT8
+        if args.decode_requests:
+            import dataclasses
+            dwl8 = dataclasses.replace(dwl8, batch=args.decode_requests,
+                                       name=dwl8.name.replace("B32", f"B{args.decode_requests}"))
+        dec["int8_cache"] = decode_int8_arm(dwl8, args, timer, peaks, peak_src)
+        dec["cached_tokens_per_s"] = round(int(dwl.ctx_lens().astype(np.int64).sum()) / (dec["ms_per_step"] * 1e-3), 0)
+        torch.cuda.empty_cache()
     extra = {}
     if args.workload in ("all", "long"):
         extra["prefill_64k"] = long_prefill_arm(synth.PREFILL_64K, args, timer, peaks, peak_src)
@@ -556,7 +607,9 @@ def main():
                      "warmup": args.warmup, "ms_per_step": dec["ms_per_step"], "higher_is_better": True,
                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                      "config": {"workload": dec["workload"]}, "roofline": dec["roofline"],
-                     "gpu_launches": dec["gpu_launches_per_step"] * args.steps})
+                     "gpu_launches": dec["gpu_launches_per_step"] * args.steps,
+                     "merge": dec["merge"], "cached_tokens_per_s": dec["cached_tokens_per_s"],
+                     "int8_cache": dec["int8_cache"]})
     if res:
         line["rope"] = res["rope"]
     if dec and res:

@@ -225,6 +225,30 @@ ATTN_API int attn_decode_paged_noalloc(const void *q, const void *k_cache, const
                                        attn_dtype_t out_dtype, float *lse, void *stream);
 
 /*
+ * attn_decode_paged_int8 -- attn_decode_paged over an INT8 KV cache.
+ *
+ * Defined by: the same attention as attn_decode_paged, over cached values
+ * code * scale.  An INT8 cache halves the bytes per cached token ("Flash
+ * Attention and distributed parallelism", section 18.12); a quantised cache
+ * keeps grouped codes with their scales (Ulysses page, section 5.4).  Here the
+ * codes are symmetric int8 and the group is one (KV head, cached token).
+ *
+ *  k_cache, v_cache  [num_kv_heads][num_pages][page_size][head_dim] int8 codes.
+ *  k_scale, v_scale  [num_kv_heads][num_pages][page_size] fp32, 16-byte aligned:
+ *                    the cached value is code * scale.
+ *  Everything else as attn_decode_paged (head_dim 128, page_size 64, 8 query
+ *  heads per KV head; same workspace, merge and outputs).
+ * The group contraction runs with fp16 operands: a rotated query element or a
+ * softmax weight times v_scale beyond 65504 in magnitude is recorded as a
+ * device error (attn_device_status reports ATTN_ERR_DEVICE).
+ */
+ATTN_API int attn_decode_paged_int8(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                                    const float *v_scale, const int32_t *page_table, const int32_t *context_lens,
+                                    int batch, int max_pages, int page_size, int64_t num_pages, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int num_splits, float scale, float *part_out,
+                                    float *part_lse, void *out, attn_dtype_t out_dtype, float *lse, void *stream);
+
+/*
  * attn_lse_merge -- combine partial attention results over disjoint key sets.
  *
  *   LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s

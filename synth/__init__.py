@@ -48,6 +48,26 @@ def randn(shape, seed: int, std: float = 1.0, dtype=torch.bfloat16, device="cpu"
     return out.view(*shape)
 
 
+def randint8(shape, seed: int, device="cpu") -> torch.Tensor:
+    """Uniform integers in [-127, 127] as int8 (the symmetric code range of an
+    INT8 cache), seeded like `randn`."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    dev = torch.device(device)
+    out = torch.empty(n, dtype=torch.int8, device=dev)
+    g = torch.Generator(device=dev).manual_seed(int(seed))
+    for s in range(0, n, _CHUNK):
+        e = min(n, s + _CHUNK)
+        out[s:e] = torch.randint(-127, 128, (e - s,), generator=g, dtype=torch.int16, device=dev).to(torch.int8)
+    return out.view(*shape)
+
+
+def uniform(shape, seed: int, lo: float, hi: float, device="cpu") -> torch.Tensor:
+    """U[lo, hi) fp32 samples of `shape`, seeded like `randn`."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(int(seed))
+    return torch.rand(tuple(shape), generator=g, dtype=torch.float32, device=dev).mul_(hi - lo).add_(lo)
+
+
 def as_f64(t: torch.Tensor) -> np.ndarray:
     """Exact fp64 copy of a bf16/fp32 tensor (every bf16/fp32 value is an fp64 value)."""
     return t.to(torch.float64).numpy()
@@ -208,6 +228,7 @@ class Decode:
     kv_std: float = 1.0
     base: float = 10000.0
     ctx_fixed: Optional[list] = None
+    int8: bool = False  # INT8 cache: int8 codes + one fp32 scale per (KV head, token)
 
     @property
     def scale(self) -> float:
@@ -220,19 +241,30 @@ class Decode:
         return rng.integers(self.ctx_lo, self.ctx_hi + 1, size=self.batch).astype(np.int32)
 
     def kv_bytes(self) -> int:
-        return int(self.ctx_lens().astype(np.int64).sum()) * self.hkv * self.d * 2 * 2
+        """Cache bytes one decode step reads: K and V of every cached token of every KV
+        head (bf16: 2 bytes per value; INT8: 1 byte per value + a 4-byte scale per row)."""
+        per_row = self.d + 4 if self.int8 else 2 * self.d
+        return int(self.ctx_lens().astype(np.int64).sum()) * self.hkv * per_row * 2
 
     def make(self, device="cpu"):
         ctx = self.ctx_lens()
         table, num_pages = shuffled_page_table(ctx, self.seed * 16 + 8)
-        kc = randn((self.hkv, max(num_pages, 1), PAGE, self.d), self.seed * 16 + 4, self.kv_std, device=device)
-        vc = randn((self.hkv, max(num_pages, 1), PAGE, self.d), self.seed * 16 + 5, self.kv_std, device=device)
+        shape = (self.hkv, max(num_pages, 1), PAGE, self.d)
         q = randn((self.batch, self.hq, self.d), self.seed * 16 + 1, self.q_std, device=device)
         qpos = (ctx - 1).astype(np.int32)
-        return dict(q=q, k_cache=kc, v_cache=vc,
-                    page_table=torch.from_numpy(table).to(device), num_pages=num_pages,
-                    ctx_lens=torch.from_numpy(ctx).to(device),
-                    q_pos=torch.from_numpy(qpos).to(device))
+        out = dict(q=q, page_table=torch.from_numpy(table).to(device), num_pages=num_pages,
+                   ctx_lens=torch.from_numpy(ctx).to(device), q_pos=torch.from_numpy(qpos).to(device))
+        if self.int8:
+            # codes uniform in [-127, 127] (std 73.3); scales near 1/73.3 so the
+            # cached values have about unit variance, like the bf16 workload
+            out["k_cache"] = randint8(shape, self.seed * 16 + 4, device)
+            out["v_cache"] = randint8(shape, self.seed * 16 + 5, device)
+            out["k_scale"] = uniform(shape[:-1], self.seed * 16 + 10, 0.8 / 73.3, 1.2 / 73.3, device)
+            out["v_scale"] = uniform(shape[:-1], self.seed * 16 + 11, 0.8 / 73.3, 1.2 / 73.3, device)
+        else:
+            out["k_cache"] = randn(shape, self.seed * 16 + 4, self.kv_std, device=device)
+            out["v_cache"] = randn(shape, self.seed * 16 + 5, self.kv_std, device=device)
+        return out
 
 
 TINY = Prefill("tiny causal GQA: B1 S64 (4x16-token segments) 8/2 heads d64 fp32",
@@ -249,5 +281,7 @@ CHUNKED = ChunkedPaged("chunked prefill: B4 x (57344 paged prefix + 8192 chunk) 
                        rows_per_head=512)
 DECODE = Decode("paged decode: B32 ctx U[16384,131072] 64/8 heads d128, 16 splits",
                 batch=32, ctx_lo=16384, ctx_hi=131072, hq=64, hkv=8, d=128, splits=16, seed=1239)
+DECODE_INT8 = Decode("paged decode, INT8 cache: B32 ctx U[16384,131072] 64/8 heads d128, 16 splits",
+                     batch=32, ctx_lo=16384, ctx_hi=131072, hq=64, hkv=8, d=128, splits=16, seed=1239, int8=True)
 
-WORKLOADS = [TINY, PREFILL_8K, PREFILL_64K, CHUNKED, DECODE]
+WORKLOADS = [TINY, PREFILL_8K, PREFILL_64K, CHUNKED, DECODE, DECODE_INT8]

@@ -127,3 +127,22 @@ def test_kv_append_rejects_bad_arguments(lib):
     assert call(ko=8) == ERR_ALIGN
     assert call(T=0) == 0
     assert call(H=0) == 0
+
+
+def test_decode_int8_rejects_bad_arguments(lib):
+    base = dict(q=16, kc=16, vc=16, ks=16, vs=16, table=16, ctx=16, batch=2, max_pages=4, page=64, num_pages=8,
+                hq=64, hkv=8, d=128, splits=16, scale=0.1, po=16, pl=16, out=16, odt=0, lse=None, stream=None)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return lib.attn_decode_paged_int8(*a.values())
+
+    assert call(hq=32) == ERR_SHAPE
+    assert call(d=64) == ERR_SHAPE
+    assert call(page=32) == ERR_SHAPE
+    assert call(splits=0) == ERR_ARG
+    assert call(ks=None) == ERR_ARG
+    assert call(vs=8) == ERR_ALIGN
+    assert call(kc=24) == ERR_ALIGN
+    assert call(batch=0) == 0

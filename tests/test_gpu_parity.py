@@ -594,3 +594,86 @@ def test_chunked_prefill_through_append_is_one_paged_call():
         o0 += c
     check(out, lse, want_o, want_l, what="append + one paged call")
     check(out2, lse2, want_o, want_l, what="two calls + merge")
+
+
+# ------------------------------------------------------------------ decode over an INT8 cache
+
+def _decode_int8(wl, inp, splits):
+    g = {k: (t.to(DEV) if torch.is_tensor(t) else t) for k, t in inp.items()}
+    q = g["q"].clone()
+    atc.rope_apply(q, g["q_pos"])
+    po, pl = atc.decode_workspace(wl.batch, wl.hq, splits, wl.d, DEV)
+    out = torch.empty((wl.batch, wl.hq, wl.d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((wl.batch, wl.hq), dtype=torch.float32, device=DEV)
+    atc.attn_decode_paged_int8(q, g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"],
+                               g["ctx_lens"], splits, po, pl, out, lse)
+    return out, lse
+
+
+def _decode_int8_oracle(wl, inp):
+    """The oracle's decode over the exact cache values code * scale."""
+    qr = rotated_bf16(inp["q"], inp["q_pos"].numpy())
+    kc = oracle.dequant_int8(inp["k_cache"].numpy(), inp["k_scale"].numpy())
+    vc = oracle.dequant_int8(inp["v_cache"].numpy(), inp["v_scale"].numpy())
+    return oracle.decode_paged(qr, kc, vc, inp["page_table"].numpy(), inp["ctx_lens"].numpy(), inp["num_pages"],
+                               wl.scale)
+
+
+@pytest.mark.parametrize("splits", [1, 4, 16])
+def test_decode_int8_matches_oracle(splits):
+    ctx = [1, 63, 64, 65, 700, 2049, 130, 0]
+    wl = synth.Decode("decode int8 small", batch=len(ctx), ctx_lo=0, ctx_hi=0, hq=16, hkv=2, d=128, splits=splits,
+                      seed=560 + splits, ctx_fixed=ctx, int8=True)
+    inp = wl.make()
+    out, lse = _decode_int8(wl, inp, splits)
+    atc.attn_device_status()
+    want_o, want_l = _decode_int8_oracle(wl, inp)
+    check(out, lse, want_o, want_l, what=f"int8 decode splits={splits}")
+    assert torch.all(out[-1] == 0) and torch.all(lse[-1] == -math.inf)  # empty context
+
+
+def test_decode_int8_64_8_heads_long_contexts():
+    ctx = [9000, 131, 4097]
+    wl = synth.Decode("decode int8 64/8", batch=3, ctx_lo=0, ctx_hi=0, hq=64, hkv=8, d=128, splits=16, seed=570,
+                      ctx_fixed=ctx, int8=True)
+    inp = wl.make()
+    out, lse = _decode_int8(wl, inp, 16)
+    atc.attn_device_status()
+    want_o, want_l = _decode_int8_oracle(wl, inp)
+    check(out, lse, want_o, want_l, what="int8 decode 64/8")
+
+
+def test_decode_int8_power_of_two_scales_match_bf16_decode():
+    """With every scale 2^-6 the cached values code / 64 are exact in bf16 (at most
+    8 significant bits): the INT8 path and the bf16 path decode the same numbers."""
+    ctx = [300, 77]
+    wl = synth.Decode("decode int8 pow2", batch=2, ctx_lo=0, ctx_hi=0, hq=16, hkv=2, d=128, splits=4, seed=580,
+                      ctx_fixed=ctx, int8=True)
+    inp = wl.make()
+    inp["k_scale"] = torch.full_like(inp["k_scale"], 2.0 ** -6)
+    inp["v_scale"] = torch.full_like(inp["v_scale"], 2.0 ** -6)
+    o8, l8 = _decode_int8(wl, inp, 4)
+    bf = dict(inp, k_cache=(inp["k_cache"].float() * 2.0 ** -6).to(torch.bfloat16),
+              v_cache=(inp["v_cache"].float() * 2.0 ** -6).to(torch.bfloat16))
+    assert torch.equal(bf["k_cache"].float(), inp["k_cache"].float() / 64.0)  # exact
+    o16, l16, _, _ = _decode(wl, bf, 4)
+    atc.attn_device_status()
+    check(o8, l8, o16.float().cpu().numpy(), l16.cpu().numpy(), what="int8 vs bf16 path on code / 64")
+
+
+def test_decode_int8_value_beyond_fp16_is_reported():
+    """A query element beyond the fp16 range is caught on the device and reported."""
+    ctx = [100]
+    wl = synth.Decode("decode int8 range", batch=1, ctx_lo=0, ctx_hi=0, hq=8, hkv=1, d=128, splits=2, seed=590,
+                      ctx_fixed=ctx, int8=True)
+    inp = wl.make()
+    g = {k: (t.to(DEV) if torch.is_tensor(t) else t) for k, t in inp.items()}
+    q = g["q"].clone()
+    q[0, 3, 17] = 1.0e6
+    po, pl = atc.decode_workspace(1, 8, 2, 128, DEV)
+    atc.attn_decode_paged_int8(q, g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"],
+                               g["ctx_lens"], 2, po, pl)
+    with pytest.raises(atc.AttnError) as e:
+        atc.attn_device_status(clear=True)
+    assert e.value.status == 6
+    atc.attn_device_status(clear=True)
