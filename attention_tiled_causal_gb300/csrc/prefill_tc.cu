@@ -63,7 +63,7 @@ constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 32 + 1024;
 // sub-partitions, so 3 warps per sub-partition launch with at most 168
 // registers each; every role fits in that without spilling.
 constexpr int NTHREADS = 384;
-constexpr int WARP_TMA = 8, WARP_MMA_S = 9, WARP_MMA_PV = 10;
+constexpr int WARP_TMA = 8, WARP_MMA_S = 9, WARP_MMA_PV = 10, WARP_IDLE = 11;
 constexpr int REGS_LAUNCH = 168;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
@@ -93,15 +93,35 @@ struct Params {
   float scale;
 };
 
-// Number of keys with position <= qp among k_pos[0..n), positions non-decreasing.
-__device__ int upper_bound_pos(const int32_t* k_pos, int n, int qp) {
-  int lo = 0, hi = n;
+// Number of keys with position <= qp among k_pos[0..n), positions
+// non-decreasing, computed by one whole warp (every lane gets the result).
+// First a guess that is exact when the positions are consecutive integers (one
+// round of loads to check it), then, if the guess fails, a 32-way search: each
+// round the lanes probe 32 evenly spaced keys of the open interval and a ballot
+// keeps the segment where the positions pass qp (8192 keys: three rounds).
+__device__ int count_le_warp(const int32_t* k_pos, int n, int qp, int lane) {
+  if (n <= 0) return 0;
+  const int first = __ldg(k_pos);
+  if (first > qp) return 0;
+  const int64_t g = (int64_t)qp - first + 1;  // the count if positions are consecutive
+  if (g >= n) {
+    if (__ldg(k_pos + n - 1) <= qp) return n;
+  } else if (__ldg(k_pos + g - 1) <= qp && __ldg(k_pos + g) > qp) {
+    return (int)g;
+  }
+  int lo = 1, hi = n;  // the count lies in [lo, hi]: k_pos[lo-1] <= qp, k_pos[hi] > qp or hi = n
   while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (k_pos[mid] <= qp)
-      lo = mid + 1;
-    else
-      hi = mid;
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool le = idx < hi && __ldg(k_pos + idx) <= qp;
+    const int c = __popc(__ballot_sync(0xffffffffu, le));  // lanes 0..c-1 passed (positions are sorted)
+    if (c > 0) {
+      const int nlo = lo + (c - 1) * step + 1;
+      hi = min(hi, lo + c * step);
+      lo = nlo;
+    } else {
+      hi = min(hi, lo);
+    }
   }
   return lo;
 }
@@ -170,6 +190,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   sm.nfull = sm.nkv + 2;
 
   if (threadIdx.x == 0) {
+    ATTN_TC_TRACE(26, 0);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.q_full[t], 1);
       mbar_init(&sm.s_full[t], 1);
@@ -182,9 +203,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.kv_empty[i], 1);
     }
     fence_mbar_init();
+  }
+  if (warp == WARP_MMA_S) tmem_alloc(sm.tmem_slot, TMEM_COLS);
+  __syncthreads();
+  // The Q tiles do not depend on the K/V extent: their loads start at once and
+  // the extent search below runs under their latency.
+  if (warp == WARP_TMA && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    for (int t = 0; t < 2; ++t) {
+      if (q0 + t * BM >= Sq) continue;
+      mbar_arrive_expect_tx(&sm.q_full[t], TILE);
+      for (int hf = 0; hf < 2; ++hf)
+        tma_load_3d(smem + OFF_Q + t * TILE + hf * HALF, &tm_q, &sm.q_full[t], hf * 64, h, q_beg + q0 + t * BM);
+    }
+  }
+  if (warp == WARP_IDLE) {
     // Per query tile: K/V tiles needed (keys up to the tile's last position) and
     // leading tiles visible in full to every row (keys up to its first position);
     // only tiles in between need the per-element mask.
+    if (lane == 0) ATTN_TC_TRACE(26, 0);
     for (int t = 0; t < 2; ++t) {
       const int r0 = q0 + t * BM;
       int nk = 0, nk_first = 0;
@@ -192,37 +231,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!p.causal) {
           nk = nk_first = Sk;
         } else {
-          const int qp_last = p.q_pos[q_beg + min(r0 + BM, Sq) - 1];
-          const int qp_first = p.q_pos[q_beg + r0];
-          nk = PAGED ? max(0, min(Sk, qp_last + 1)) : upper_bound_pos(p.k_pos + k_beg, Sk, qp_last);
-          nk_first = PAGED ? max(0, min(Sk, qp_first + 1)) : upper_bound_pos(p.k_pos + k_beg, Sk, qp_first);
+          const int qp_last = __ldg(p.q_pos + q_beg + min(r0 + BM, Sq) - 1);
+          const int qp_first = __ldg(p.q_pos + q_beg + r0);
+          nk = PAGED ? max(0, min(Sk, qp_last + 1)) : count_le_warp(p.k_pos + k_beg, Sk, qp_last, lane);
+          nk_first = PAGED ? max(0, min(Sk, qp_first + 1)) : count_le_warp(p.k_pos + k_beg, Sk, qp_first, lane);
         }
       }
-      sm.nkv[t] = (nk + BN - 1) / BN;
-      sm.nfull[t] = nk_first / BN;
+      if (lane == 0) {
+        sm.nkv[t] = (nk + BN - 1) / BN;
+        sm.nfull[t] = nk_first / BN;
+      }
     }
+    if (lane == 0) ATTN_TC_TRACE(27, 0);
   }
-  if (warp == WARP_MMA_S) tmem_alloc(sm.tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
+  if (threadIdx.x == 0) ATTN_TC_TRACE(28, 0);
   const int nkv_a = sm.nkv[0], nkv_b = sm.nkv[1];
   const int nkv = max(nkv_a, nkv_b);
 
   if (warp >= 8) {
    if (warp == WARP_TMA) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && nkv > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      for (int t = 0; t < 2; ++t) {
-        if (sm.nkv[t] == 0) continue;
-        mbar_arrive_expect_tx(&sm.q_full[t], TILE);
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(smem + OFF_Q + t * TILE + hf * HALF, &tm_q, &sm.q_full[t], hf * 64, h, q_beg + q0 + t * BM);
-      }
+    if (lane == 0) {
       const int32_t* table = PAGED ? p.page_table + (int64_t)b * p.max_pages : nullptr;
       int issued = 0;
       for (int i = 0; i < 2 * nkv; ++i) {
@@ -259,9 +292,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         issued = i + 1;
       }
-      // Leave no copy in flight: wait (bounded) for the last slots issued.
+      // Leave no copy in flight: wait (bounded) for the last slots issued and
+      // for the Q tiles (loaded even when a tile turns out to need no keys).
       for (int i = max(0, issued - NSLOT); i < issued; ++i)
         mbar_wait(&sm.kv_full[i % NSLOT], (i / NSLOT) & 1, nullptr, 0);
+      for (int t = 0; t < 2; ++t)
+        if (q0 + t * BM < Sq) mbar_wait(&sm.q_full[t], 0, nullptr, 0);
     }
   } else if (warp == WARP_MMA_S || warp == WARP_MMA_PV) {
     // ------------------------------------------------------------ MMA issuers
@@ -552,6 +588,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) ATTN_TC_TRACE(29, 0);
   if (warp == WARP_MMA_S) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
