@@ -12,12 +12,13 @@
 //  * Warp 8 (one thread) is the TMA producer: Q tiles once, then K_j and V_j
 //    tiles (128 tokens x 128 dims, two 128-byte-swizzled boxes each) into a
 //    3-slot shared-memory ring, each slot guarded by full/empty mbarriers.
+//    The Q tiles and K_0 are requested before the CTA knows how many key
+//    tiles it needs; warp 11 works that out meanwhile.
 //  * Warps 9 and 10 issue tcgen05.mma, each as a converged warp with one
 //    elected lane: warp 9 the scores S_t = Q_t K_j^T into TMEM (M = 128,
 //    N = 128, K = 16 per instruction, bf16 in, fp32 accumulate), warp 10 the
 //    updates O_t += P_t V_j into a second TMEM accumulator.  tcgen05.commit
 //    arrives on mbarriers when the tensor core is done.
-//  * Warp 11 idles (the block is three whole warpgroups).
 //  * Warps 0-3 (tile A) and 4-7 (tile B) are the softmax warpgroups: thread r
 //    of a warpgroup owns query row r (TMEM lane r), loads its 128 scores with
 //    tcgen05.ld, applies the absolute-position causal mask (Ulysses page,
@@ -91,24 +92,26 @@ struct Params {
   int64_t num_pages;
   int max_pages, hq, hkv, h_lo, causal, out_f32;
   float scale;
+  int wave;  // CTAs resident at once (one per SM): the CTA `wave` launches later likely follows this one
 };
 
 // Number of keys with position <= qp among k_pos[0..n), positions
-// non-decreasing, computed by one whole warp (every lane gets the result).
-// First a guess that is exact when the positions are consecutive integers (one
-// round of loads to check it), then, if the guess fails, a 32-way search: each
-// round the lanes probe 32 evenly spaced keys of the open interval and a ballot
-// keeps the segment where the positions pass qp (8192 keys: three rounds).
-__device__ int count_le_warp(const int32_t* k_pos, int n, int qp, int lane) {
+// non-decreasing (first = k_pos[0]), if a guess that is exact for consecutive
+// positions checks out (one thread, one round of loads); -1 otherwise.
+__device__ int count_le_guess(const int32_t* k_pos, int n, int first, int qp) {
   if (n <= 0) return 0;
-  const int first = __ldg(k_pos);
   if (first > qp) return 0;
   const int64_t g = (int64_t)qp - first + 1;  // the count if positions are consecutive
-  if (g >= n) {
-    if (__ldg(k_pos + n - 1) <= qp) return n;
-  } else if (__ldg(k_pos + g - 1) <= qp && __ldg(k_pos + g) > qp) {
-    return (int)g;
-  }
+  if (g >= n) return __ldg(k_pos + n - 1) <= qp ? n : -1;
+  return (__ldg(k_pos + g - 1) <= qp && __ldg(k_pos + g) > qp) ? (int)g : -1;
+}
+
+// The same count by one whole warp (every lane gets the result): a 32-way
+// search; each round the lanes probe 32 evenly spaced keys of the open
+// interval and a ballot keeps the segment where the positions pass qp
+// (8192 keys: three rounds).
+__device__ int count_le_warp(const int32_t* k_pos, int n, int qp, int lane) {
+  if (n <= 0 || __ldg(k_pos) > qp) return 0;
   int lo = 1, hi = n;  // the count lies in [lo, hi]: k_pos[lo-1] <= qp, k_pos[hi] > qp or hi = n
   while (lo < hi) {
     const int step = (hi - lo + 31) / 32;
@@ -189,7 +192,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   sm.nkv = (int*)(sm.tmem_slot + 4);
   sm.nfull = sm.nkv + 2;
 
-  if (threadIdx.x == 0) {
+  if (warp == WARP_IDLE) {
+    // Per query tile: K/V tiles needed (keys up to the tile's last position) and
+    // leading tiles visible in full to every row (keys up to its first position);
+    // only tiles in between need the per-element mask.  Lane c < 4 handles count
+    // c (tile c / 2; its last row if c is even, its first row if odd), so the
+    // four counts' loads are in flight together.  It touches no barrier, so it
+    // runs before the barriers are even set up.
+    const int c = lane & 3, t = c >> 1;
+    const int r0 = q0 + t * BM;
+    const bool rows = r0 < Sq;
+    int qp = 0, cnt = 0;
+    if (rows && p.causal) {
+      qp = __ldg(p.q_pos + q_beg + ((c & 1) ? r0 : min(r0 + BM, Sq) - 1));
+      const int first = (!PAGED && Sk > 0) ? __ldg(p.k_pos + k_beg) : 0;  // in flight with qp
+      cnt = PAGED ? max(0, min(Sk, qp + 1)) : count_le_guess(p.k_pos + k_beg, Sk, first, qp);
+    } else if (rows) {
+      cnt = Sk;
+    }
+    for (int cc = 0; cc < 4; ++cc) {  // the rare counts whose guess failed, by the whole warp
+      const int got = __shfl_sync(0xffffffffu, cnt, cc);
+      if (got < 0) {
+        const int v = count_le_warp(p.k_pos + k_beg, Sk, __shfl_sync(0xffffffffu, qp, cc), lane);
+        if (c == cc) cnt = v;
+      }
+    }
+    const int cnt_first = __shfl_sync(0xffffffffu, cnt, lane | 1);  // the same tile's first-row count
+    if (lane == 0 || lane == 2) {
+      sm.nkv[t] = (cnt + BN - 1) / BN;
+      sm.nfull[t] = cnt_first / BN;
+    }
+    if (lane == 0) ATTN_TC_TRACE(27, 0);
+  }
+  if (warp == WARP_MMA_S) tmem_alloc(sm.tmem_slot, TMEM_COLS);
+  // K or V tile j into ring slot `slot` (TMA, completion on kv_full[slot]).
+  const int32_t* table = PAGED ? p.page_table + (int64_t)b * p.max_pages : nullptr;
+  auto load_kv = [&](int slot, bool is_v, int j) {
+    const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+    uint8_t* dst = smem + OFF_KV + slot * TILE;
+    ATTN_TC_TRACE(20 + (is_v ? 1 : 0), j);
+    mbar_arrive_expect_tx(&sm.kv_full[slot], TILE);
+    if (!PAGED) {
+      for (int hf = 0; hf < 2; ++hf) tma_load_3d(dst + hf * HALF, tm, &sm.kv_full[slot], hf * 64, g, k_beg + j * BN);
+    } else {
+      for (int pp = 0; pp < 2; ++pp) {  // two 64-token pages per tile
+        const int lp = j * 2 + pp;
+        int pid = lp < p.max_pages ? table[lp] : -1;
+        if (pid < 0 || pid >= p.num_pages) {
+          if (lp * 64 < Sk) record_error(p.err, DEV_BAD_PAGE);
+          pid = 0;  // tokens past Sk are masked; keep the byte count whole
+        }
+        const int row0 = (int)(((int64_t)g * p.num_pages + pid) * 64);
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_2d(dst + hf * HALF + pp * (HALF / 2), tm, &sm.kv_full[slot], hf * 64, row0);
+      }
+    }
+  };
+  // The producer sets the barriers up itself and requests the Q tiles and K_0
+  // at once: none of them depends on the K/V extent, which warp 11 may still
+  // be working out.  K_0 is load 0 of the ring whenever any key is visible; if
+  // none is, the producer still waits for it before exiting.  The __syncthreads
+  // below publishes the initialised barriers to every other role.
+  const bool k0_early = Sk > 0;
+  if (warp == WARP_TMA && lane == 0) {
     ATTN_TC_TRACE(26, 0);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.q_full[t], 1);
@@ -203,12 +268,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.kv_empty[i], 1);
     }
     fence_mbar_init();
-  }
-  if (warp == WARP_MMA_S) tmem_alloc(sm.tmem_slot, TMEM_COLS);
-  __syncthreads();
-  // The Q tiles do not depend on the K/V extent: their loads start at once and
-  // the extent search below runs under their latency.
-  if (warp == WARP_TMA && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -218,31 +277,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int hf = 0; hf < 2; ++hf)
         tma_load_3d(smem + OFF_Q + t * TILE + hf * HALF, &tm_q, &sm.q_full[t], hf * 64, h, q_beg + q0 + t * BM);
     }
-  }
-  if (warp == WARP_IDLE) {
-    // Per query tile: K/V tiles needed (keys up to the tile's last position) and
-    // leading tiles visible in full to every row (keys up to its first position);
-    // only tiles in between need the per-element mask.
-    if (lane == 0) ATTN_TC_TRACE(26, 0);
-    for (int t = 0; t < 2; ++t) {
-      const int r0 = q0 + t * BM;
-      int nk = 0, nk_first = 0;
-      if (r0 < Sq) {
-        if (!p.causal) {
-          nk = nk_first = Sk;
-        } else {
-          const int qp_last = __ldg(p.q_pos + q_beg + min(r0 + BM, Sq) - 1);
-          const int qp_first = __ldg(p.q_pos + q_beg + r0);
-          nk = PAGED ? max(0, min(Sk, qp_last + 1)) : count_le_warp(p.k_pos + k_beg, Sk, qp_last, lane);
-          nk_first = PAGED ? max(0, min(Sk, qp_first + 1)) : count_le_warp(p.k_pos + k_beg, Sk, qp_first, lane);
-        }
-      }
-      if (lane == 0) {
-        sm.nkv[t] = (nk + BN - 1) / BN;
-        sm.nfull[t] = nk_first / BN;
-      }
+    if (k0_early) load_kv(0, false, 0);
+    // Q comes from HBM and its latency opens every CTA.  Blocks start in
+    // launch order as SMs free up, so the block `wave` places later in that
+    // order will likely start on some SM when a block of this wave ends: bring
+    // its Q tiles into L2 now.
+    const int64_t L = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+    const int64_t Ln = L + p.wave;
+    if (p.wave > 0 && Ln < (int64_t)gridDim.x * gridDim.y * gridDim.z) {
+      const int xn = (int)(Ln % gridDim.x), yn = (int)((Ln / gridDim.x) % gridDim.y);
+      const int bn = (int)(Ln / ((int64_t)gridDim.x * gridDim.y));
+      const int qbn = __ldg(p.cu_q + bn), sqn = __ldg(p.cu_q + bn + 1) - qbn;
+      const int q0n = (gridDim.y - 1 - yn) * 2 * BM;
+      for (int t = 0; t < 2; ++t)
+        if (q0n + t * BM < sqn)
+          for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_3d(&tm_q, hf * 64, p.h_lo + xn, qbn + q0n + t * BM);
     }
-    if (lane == 0) ATTN_TC_TRACE(27, 0);
   }
   tc_fence_before();
   __syncthreads();
@@ -256,9 +306,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
    if (warp == WARP_TMA) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int32_t* table = PAGED ? p.page_table + (int64_t)b * p.max_pages : nullptr;
-      int issued = 0;
-      for (int i = 0; i < 2 * nkv; ++i) {
+      int issued = k0_early ? 1 : 0;
+      for (int i = issued; i < 2 * nkv; ++i) {
         // load i of the ring order (see ring_pos_k / ring_pos_v)
         bool is_v;
         int j;
@@ -271,25 +320,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const int slot = i % NSLOT;
         if (i >= NSLOT && !mbar_wait(&sm.kv_empty[slot], ((i / NSLOT) - 1) & 1, p.err, DEV_TIMEOUT_TMA)) break;
-        const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-        uint8_t* dst = smem + OFF_KV + slot * TILE;
-        ATTN_TC_TRACE(20 + (is_v ? 1 : 0), j);
-        mbar_arrive_expect_tx(&sm.kv_full[slot], TILE);
-        if (!PAGED) {
-          for (int hf = 0; hf < 2; ++hf) tma_load_3d(dst + hf * HALF, tm, &sm.kv_full[slot], hf * 64, g, k_beg + j * BN);
-        } else {
-          for (int pp = 0; pp < 2; ++pp) {  // two 64-token pages per tile
-            const int lp = j * 2 + pp;
-            int pid = lp < p.max_pages ? table[lp] : -1;
-            if (pid < 0 || pid >= p.num_pages) {
-              if (lp * 64 < Sk) record_error(p.err, DEV_BAD_PAGE);
-              pid = 0;  // tokens past Sk are masked; keep the byte count whole
-            }
-            const int row0 = (int)(((int64_t)g * p.num_pages + pid) * 64);
-            for (int hf = 0; hf < 2; ++hf)
-              tma_load_2d(dst + hf * HALF + pp * (HALF / 2), tm, &sm.kv_full[slot], hf * 64, row0);
-          }
-        }
+        load_kv(slot, is_v, j);
         issued = i + 1;
       }
       // Leave no copy in flight: wait (bounded) for the last slots issued and
@@ -643,6 +674,15 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, con
   p.causal = a.causal;
   p.out_f32 = a.out_f32;
   p.scale = a.scale;
+  {
+    static int sms[64] = {};
+    if (dev < 64 && sms[dev] == 0) {
+      int n = 0;
+      if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
+      sms[dev] = n;
+    }
+    p.wave = dev < 64 ? sms[dev] : 0;
+  }
   const int pairs = (a.max_seqlen_q + 2 * tc::BM - 1) / (2 * tc::BM);
   dim3 grid(a.h_hi - a.h_lo, pairs, a.batch);
   if (paged)
