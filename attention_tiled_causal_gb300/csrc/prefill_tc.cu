@@ -428,20 +428,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok) break;
       tc_fence_after();
       if (row == 0) ATTN_TC_TRACE(10 + t, j);
-      // Scores: two halves of 64 columns; the second load overlaps the first
-      // half's max.
-      // Scores: one row of S_t (128 fp32) per thread.
+      if (lane == 0) ATTN_TC_TRACE(48 + warp, j);
+      // Scores: one row of S_t (128 fp32) per thread, in one TMEM load.
       float s[128];
       float mx[8];
       {
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+        uint32_t sr[128];
+        tmem_ld128(tS, sr);
         tmem_wait_ld();
+        tmem_regs_ready128(sr);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_regs_ready(sr[c]);
-#pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
       }
       tc_fence_before();
       mbar_arrive(&sm.s_free[t]);  // S_t may now be overwritten by S_t(j+1)
@@ -518,6 +515,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ok) break;
         tc_fence_after();
       }
+      if (row == 0) ATTN_TC_TRACE(32 + t, j);
       // P = exp2(S * scale*log2e - m*scale*log2e), bf16, into the swizzled K-major
       // tile.  The affine step and the row sum run on fp32 pairs.
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nmbx2 = f2_pack(-mb, -mb);
@@ -571,6 +569,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       mbar_arrive(&sm.p_full[t]);
       if (row == 0) ATTN_TC_TRACE(18 + t, j);
+      if (lane == 0) ATTN_TC_TRACE(40 + warp, j);
     }
 
     // epilogue: O / l to global memory, LSE = scale * m + ln l
