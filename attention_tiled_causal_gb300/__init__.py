@@ -8,6 +8,8 @@ PyTorch provides device memory and streams.
 
 Entry points (same names as the C ABI):
     rope_apply(x, positions, base)                      RoPE at absolute positions, in place
+    rope_table(positions, head_dim, base)               cos/sin table for on-the-fly rotation
+    attn_prefill(..., q_rope_cs=table)                  attention with the query's RoPE fused in
     attn_kv_append_paged(k_new, v_new, positions, slots, k_cache, v_cache)
                                                         new K (rotated) / V into the paged cache
     attn_prefill(q, k, v, out, lse, cu_q, q_pos, ...)   tiled causal GQA attention
@@ -18,8 +20,8 @@ Entry points (same names as the C ABI):
 from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_decode_paged_int8,
                        attn_device_status,
                        attn_kv_append_paged, attn_lse_merge, attn_prefill, decode_workspace, lib_path, library,
-                       prefill, rope_apply)
+                       prefill, rope_apply, rope_table)
 
 __all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_decode_paged_int8", "attn_device_status",
            "attn_kv_append_paged", "attn_lse_merge", "attn_prefill", "decode_workspace", "lib_path", "library",
-           "prefill", "rope_apply"]
+           "prefill", "rope_apply", "rope_table"]

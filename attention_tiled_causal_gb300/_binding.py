@@ -42,6 +42,11 @@ def library():
     lib.attn_device_status.restype = I32
     lib.rope_apply.argtypes = [P, I32, I64, I32, I32, I64, P, F64, P]
     lib.rope_apply.restype = I32
+    lib.rope_table.argtypes = [P, I64, I32, F64, P, P]
+    lib.rope_table.restype = I32
+    lib.attn_prefill_rope_q.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, I64, I32, P, P, I64, P, P, I32, I32,
+                                        I64, I32, I32, I32, I32, I32, F32, I32, P, P]
+    lib.attn_prefill_rope_q.restype = I32
     lib.attn_kv_append_paged.argtypes = [P, P, P, P, I64, I32, I32, P, P, I64, I32, P, F64, P]
     lib.attn_kv_append_paged.restype = I32
     lib.attn_prefill.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, I64, I32, P, P, I64, P, P, I32, I32, I64,
@@ -144,14 +149,29 @@ def attn_kv_append_paged(k_new, v_new, positions, slots, k_cache, v_cache, *, k_
                                           _stream(stream)))
 
 
+def rope_table(positions, head_dim: int, base: float = 10000.0, out=None, stream=None) -> torch.Tensor:
+    """cos and sin of every RoPE angle at absolute `positions` [tokens]: a float32
+    [tokens, head_dim/2, 2] table, the numbers rope_apply rotates with."""
+    positions = _i32(positions, "positions")
+    T = positions.numel()
+    if out is None:
+        out = torch.empty((T, head_dim // 2, 2), dtype=torch.float32, device=positions.device)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (T, head_dim // 2, 2) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 [tokens, head_dim/2, 2] tensor")
+    _check(library().rope_table(_ptr(positions), T, int(head_dim), float(base), _ptr(out), _stream(stream)))
+    return out
+
+
 def attn_prefill(q, k, v, out, lse, cu_q, q_pos, max_seqlen_q: int, *, cu_k=None, k_pos=None,
                  page_table=None, k_lens=None, num_pages: int = 0, h_lo: int = 0,
                  h_hi: Optional[int] = None, scale: Optional[float] = None, causal: bool = True,
-                 stream=None) -> None:
+                 q_rope_cs=None, stream=None) -> None:
     """Tiled causal GQA attention.  q [Tq, Hq, d]; contiguous k/v [Tk, Hkv, d] with
     cu_k/k_pos, or head-major paged caches [Hkv, num_pages, page, d] with
     page_table [B, max_pages] and k_lens [B].  Writes out [Tq, Hq, d] and lse [Tq, Hq]
-    (if given) for query heads [h_lo, h_hi)."""
+    (if given) for query heads [h_lo, h_hi).  With q_rope_cs (from rope_table over
+    q_pos) q holds unrotated queries and the kernel rotates them itself
+    (attn_prefill_rope_q)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
         if not t.is_contiguous():
             raise ValueError(f"{n} must be contiguous")
@@ -175,12 +195,18 @@ def attn_prefill(q, k, v, out, lse, cu_q, q_pos, max_seqlen_q: int, *, cu_k=None
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     cu_q = _i32(cu_q, "cu_q")
     B = cu_q.numel() - 1
-    _check(library().attn_prefill(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _dt(out), _ptr(lse), _dt(q), B, _ptr(cu_q),
-        _ptr(_i32(q_pos, "q_pos")), Tq, int(max_seqlen_q), _ptr(_i32(cu_k, "cu_k")),
-        _ptr(_i32(k_pos, "k_pos")), total_k, _ptr(_i32(page_table, "page_table")),
-        _ptr(_i32(k_lens, "k_lens")), max_pages, page, int(num_pages), hq, hkv, d, int(h_lo),
-        int(h_hi), float(scale), 1 if causal else 0, _stream(stream)))
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(out), _dt(out), _ptr(lse), _dt(q), B, _ptr(cu_q),
+            _ptr(_i32(q_pos, "q_pos")), Tq, int(max_seqlen_q), _ptr(_i32(cu_k, "cu_k")),
+            _ptr(_i32(k_pos, "k_pos")), total_k, _ptr(_i32(page_table, "page_table")),
+            _ptr(_i32(k_lens, "k_lens")), max_pages, page, int(num_pages), hq, hkv, d, int(h_lo),
+            int(h_hi), float(scale), 1 if causal else 0]
+    if q_rope_cs is None:
+        _check(library().attn_prefill(*args, _stream(stream)))
+    else:
+        if q_rope_cs.dtype != torch.float32 or tuple(q_rope_cs.shape) != (Tq, d // 2, 2) \
+                or not q_rope_cs.is_contiguous():
+            raise ValueError("q_rope_cs must be a contiguous float32 [Tq, d/2, 2] table (rope_table)")
+        _check(library().attn_prefill_rope_q(*args, _ptr(q_rope_cs), _stream(stream)))
 
 
 def prefill(q, k, v, cu_q, q_pos, max_seqlen_q: int, out_dtype=None, with_lse: bool = True, **kw):

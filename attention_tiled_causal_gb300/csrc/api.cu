@@ -198,12 +198,16 @@ int attn_kv_append_paged(const void* k_new, const void* v_new, const int32_t* po
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_kv_append_paged launch");
 }
 
-int attn_prefill(const void* q, const void* k, const void* v, void* out, attn_dtype_t out_dtype, float* lse,
+}  // extern "C"
+
+namespace {
+
+int prefill_impl(const void* q, const void* k, const void* v, void* out, attn_dtype_t out_dtype, float* lse,
                  attn_dtype_t dtype, int batch, const int32_t* cu_q, const int32_t* q_pos, int64_t total_q,
                  int max_seqlen_q, const int32_t* cu_k, const int32_t* k_pos, int64_t total_k,
                  const int32_t* page_table, const int32_t* k_lens, int max_pages, int page_size, int64_t num_pages,
                  int num_q_heads, int num_kv_heads, int head_dim, int h_lo, int h_hi, float scale, int causal,
-                 void* stream) {
+                 const float* q_rope_cs, void* stream) {
   if (batch < 0 || max_seqlen_q < 0 || total_q < 0) return fail(ATTN_ERR_ARG, "attn_prefill: negative size");
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
     return fail(ATTN_ERR_SHAPE, "attn_prefill: num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads,
@@ -245,10 +249,13 @@ int attn_prefill(const void* q, const void* k, const void* v, void* out, attn_dt
   a.max_pages = max_pages; a.page_size = page_size; a.num_pages = num_pages;
   a.hq = num_q_heads; a.hkv = num_kv_heads; a.d = head_dim; a.h_lo = h_lo; a.h_hi = h_hi;
   a.scale = scale; a.causal = causal ? 1 : 0;
+  a.q_rope_cs = q_rope_cs;
   int rc = device_error_ptr(&a.err);
   if (rc) return rc;
 
   const bool tc = dtype == ATTN_BF16 && head_dim == 128 && (!paged || page_size == 64) && !force_simt();
+  if (q_rope_cs && !tc)
+    return fail(ATTN_ERR_UNSUPPORTED, "attn_prefill_rope_q: fused RoPE needs bf16, head_dim 128 (tensor-core path)");
   cudaError_t e;
   if (tc) {
     CUtensorMap tq, tk, tv;
@@ -265,6 +272,45 @@ int attn_prefill(const void* q, const void* k, const void* v, void* out, attn_dt
     e = attn::launch_prefill_simt(a, (cudaStream_t)stream);
   }
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_prefill launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_prefill(const void* q, const void* k, const void* v, void* out, attn_dtype_t out_dtype, float* lse,
+                 attn_dtype_t dtype, int batch, const int32_t* cu_q, const int32_t* q_pos, int64_t total_q,
+                 int max_seqlen_q, const int32_t* cu_k, const int32_t* k_pos, int64_t total_k,
+                 const int32_t* page_table, const int32_t* k_lens, int max_pages, int page_size, int64_t num_pages,
+                 int num_q_heads, int num_kv_heads, int head_dim, int h_lo, int h_hi, float scale, int causal,
+                 void* stream) {
+  return prefill_impl(q, k, v, out, out_dtype, lse, dtype, batch, cu_q, q_pos, total_q, max_seqlen_q, cu_k, k_pos,
+                      total_k, page_table, k_lens, max_pages, page_size, num_pages, num_q_heads, num_kv_heads,
+                      head_dim, h_lo, h_hi, scale, causal, nullptr, stream);
+}
+
+int attn_prefill_rope_q(const void* q, const void* k, const void* v, void* out, attn_dtype_t out_dtype, float* lse,
+                        attn_dtype_t dtype, int batch, const int32_t* cu_q, const int32_t* q_pos, int64_t total_q,
+                        int max_seqlen_q, const int32_t* cu_k, const int32_t* k_pos, int64_t total_k,
+                        const int32_t* page_table, const int32_t* k_lens, int max_pages, int page_size,
+                        int64_t num_pages, int num_q_heads, int num_kv_heads, int head_dim, int h_lo, int h_hi,
+                        float scale, int causal, const float* q_rope_cs, void* stream) {
+  if (!q_rope_cs) return fail(ATTN_ERR_ARG, "attn_prefill_rope_q: null RoPE table");
+  if (!aligned16(q_rope_cs)) return fail(ATTN_ERR_ALIGN, "attn_prefill_rope_q: RoPE table must be 16-byte aligned");
+  return prefill_impl(q, k, v, out, out_dtype, lse, dtype, batch, cu_q, q_pos, total_q, max_seqlen_q, cu_k, k_pos,
+                      total_k, page_table, k_lens, max_pages, page_size, num_pages, num_q_heads, num_kv_heads,
+                      head_dim, h_lo, h_hi, scale, causal, q_rope_cs, stream);
+}
+
+int rope_table(const int32_t* positions, int64_t tokens, int head_dim, double base, float* cs_out, void* stream) {
+  if (tokens < 0 || head_dim <= 0) return fail(ATTN_ERR_ARG, "rope_table: negative size");
+  if (head_dim % 2 || head_dim > 256) return fail(ATTN_ERR_SHAPE, "rope_table: head_dim %d (even, <= 256)", head_dim);
+  if (!(base > 0.0)) return fail(ATTN_ERR_ARG, "rope_table: base must be positive");
+  if (tokens == 0) return ATTN_OK;
+  if (!positions || !cs_out) return fail(ATTN_ERR_ARG, "rope_table: null pointer");
+  if (!aligned16(cs_out)) return fail(ATTN_ERR_ALIGN, "rope_table: cs_out must be 16-byte aligned");
+  cudaError_t e = attn::launch_rope_table(cs_out, tokens, head_dim, positions, base, (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "rope_table launch");
 }
 
 int attn_lse_merge(const float* part_out, const float* part_lse, int n_parts, int64_t rows, int heads, int head_dim,

@@ -345,6 +345,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// One RoPE pair rotation, x1' = x1 cos - x2 sin, x2' = x2 cos + x1 sin, with
+// the rounding of every step fixed (one product, then one fused multiply-add)
+// so that every kernel that rotates gets the same bits.
+__device__ __forceinline__ void rope_rotate(float x1, float x2, float cs, float sn, float& y1, float& y2) {
+  y1 = __fmaf_rn(x1, cs, -__fmul_rn(x2, sn));
+  y2 = __fmaf_rn(x2, cs, __fmul_rn(x1, sn));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

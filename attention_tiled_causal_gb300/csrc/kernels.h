@@ -18,6 +18,8 @@ struct RopeLaunch {
   double base;
 };
 cudaError_t launch_rope(const RopeLaunch& a, cudaStream_t s);
+cudaError_t launch_rope_table(float* cs_out, int64_t tokens, int head_dim, const int32_t* positions, double base,
+                              cudaStream_t s);
 
 struct AppendLaunch {
   const void* k_new;
@@ -65,6 +67,7 @@ struct PrefillLaunch {
   float scale;
   int causal;
   unsigned* err;
+  const float* q_rope_cs = nullptr;  // tcgen05 kernel only: [total_q][d/2][2] cos, sin; rotate Q on the fly
 };
 // CUDA-core kernel: any supported dtype / head_dim / page size.
 cudaError_t launch_prefill_simt(const PrefillLaunch& a, cudaStream_t s);

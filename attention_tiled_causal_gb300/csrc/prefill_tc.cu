@@ -58,7 +58,7 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_KV = OFF_Q + 2 * TILE;
 constexpr int OFF_P = OFF_KV + NSLOT * TILE;
 constexpr int OFF_BAR = OFF_P + 2 * TILE;
-constexpr int NBAR = 16;
+constexpr int NBAR = 18;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 32 + 1024;
 // 12 warps = 3 warpgroups.  The register file is split across the SM's four
 // sub-partitions, so 3 warps per sub-partition launch with at most 168
@@ -79,6 +79,7 @@ struct Smem {
   uint64_t* s_free;    // [2]  softmax -> MMA: S_t read out of TMEM (128 arrivals)
   uint64_t* p_full;    // [2]  softmax -> MMA: P_t written, O_t rescaled (128 arrivals)
   uint64_t* o_done;    // [2]  MMA -> softmax: O_t += P_t V_j finished
+  uint64_t* q_rot;     // [2]  softmax -> MMA: Q_t rotated in place (128 arrivals; only when RoPE is fused)
   uint32_t* tmem_slot;
   int* nkv;            // [2]  K/V tiles each query tile needs
   int* nfull;          // [2]  leading K/V tiles every row of the query tile sees in full
@@ -93,6 +94,7 @@ struct Params {
   int max_pages, hq, hkv, h_lo, causal, out_f32;
   float scale;
   int wave;  // CTAs resident at once (one per SM): the CTA `wave` launches later likely follows this one
+  const float4* q_cs;  // NULL, or [total_q][32] float4: (cos, sin) of the 64 RoPE angles of each query row
 };
 
 // Number of keys with position <= qp among k_pos[0..n), positions
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   sm.s_free = bars + 10;
   sm.p_full = bars + 12;
   sm.o_done = bars + 14;
+  sm.q_rot = bars + 16;
   sm.tmem_slot = (uint32_t*)(bars + NBAR);
   sm.nkv = (int*)(sm.tmem_slot + 4);
   sm.nfull = sm.nkv + 2;
@@ -262,6 +265,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.s_free[t], 128);
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_done[t], 1);
+      mbar_init(&sm.q_rot[t], 128);
     }
     for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&sm.kv_full[i], 1);
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (warp == WARP_MMA_S) {
         bool ok = true;
         for (int t = 0; t < 2 && ok; ++t)
-          if (sm.nkv[t] > 0) ok = wait(&sm.q_full[t], 0);
+          if (sm.nkv[t] > 0) ok = wait(p.q_cs ? &sm.q_rot[t] : &sm.q_full[t], 0);
         tc_fence_after();
         ATTN_TC_TRACE(0, 0);
         const uint64_t dQ = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
@@ -423,7 +427,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
 
-    for (int j = 0; j < nkv_t; ++j) {
+    if (p.q_cs && nkv_t > 0) {
+      // RoPE of the query, fused: the warp rotates its 32 rows of Q_t in shared
+      // memory with the same cos/sin and the same rounding as rope_apply, so the
+      // scores are those of rope_apply followed by this kernel, bit for bit.
+      // Lane l takes pairs 2l and 2l+1 (dims 2l, 2l+1 with partners 64+2l,
+      // 65+2l) of every row, so each table load reads one row's 512 bytes
+      // contiguously across the warp; the loads are issued before Q lands.
+      const int r_first = wq * 32;
+      const int nrows = max(0, min(32, Sq - (q0 + t * BM + r_first)));
+      const float4* src = p.q_cs + (int64_t)(q_beg + q0 + t * BM + r_first) * 32 + lane;
+      float4 tab[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nrows) tab[i] = __ldg(src + i * 32);
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[t], 0, p.err, DEV_TIMEOUT_SOFTMAX));
+      if (ok) {
+        const int chunk = lane >> 2, within = (lane & 3) * 4;  // dims 2l, 2l+1: chunk l/4, bytes 4(l%4)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i >= nrows) break;
+          const int rr = r_first + i;
+          uint8_t* qrow = smem + OFF_Q + t * TILE + (rr >> 3) * 1024 + (rr & 7) * 128 + ((chunk ^ (rr & 7)) << 4) +
+                          within;
+          uint32_t* p1 = reinterpret_cast<uint32_t*>(qrow);
+          uint32_t* p2 = reinterpret_cast<uint32_t*>(qrow + HALF);
+          const uint32_t u1 = *p1, u2 = *p2;
+          float y0, y1, z0, z1;
+          rope_rotate(__uint_as_float(u1 << 16), __uint_as_float(u2 << 16), tab[i].x, tab[i].y, y0, z0);
+          rope_rotate(__uint_as_float(u1 & 0xffff0000u), __uint_as_float(u2 & 0xffff0000u), tab[i].z, tab[i].w, y1,
+                      z1);
+          *p1 = pack_bf16x2(y0, y1);
+          *p2 = pack_bf16x2(z0, z1);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.q_rot[t]);
+    }
+
+    for (int j = 0; j < nkv_t && ok; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, p.err, DEV_TIMEOUT_SOFTMAX));
       if (!ok) break;
       tc_fence_after();
@@ -673,6 +715,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, con
   p.causal = a.causal;
   p.out_f32 = a.out_f32;
   p.scale = a.scale;
+  p.q_cs = reinterpret_cast<const float4*>(a.q_rope_cs);
   {
     static int sms[64] = {};
     if (dev < 64 && sms[dev] == 0) {

@@ -83,8 +83,10 @@ __global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t to
     for (int e = 0; e < V; ++e) {
       const float cs = cs_s[tt][c * V + e], sn = sn_s[tt][c * V + e];
       const float x1 = to_f(a1[e]), x2 = to_f(a2[e]);
-      from_f(x1 * cs - x2 * sn, b1[e]);
-      from_f(x2 * cs + x1 * sn, b2[e]);
+      float y1, y2;
+      rope_rotate(x1, x2, cs, sn, y1, y2);
+      from_f(y1, b1[e]);
+      from_f(y2, b2[e]);
     }
     *reinterpret_cast<uint4*>(p1) = w1;
     *reinterpret_cast<uint4*>(p2) = w2;
@@ -146,8 +148,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const In
       for (int e = 0; e < V; ++e) {
         const float cs = cs_s[tt][c * V + e], sn = sn_s[tt][c * V + e];
         const float x1 = to_f(a1[e]), x2 = to_f(a2[e]);
-        from_f(x1 * cs - x2 * sn, b1[e]);
-        from_f(x2 * cs + x1 * sn, b2[e]);
+        float y1, y2;
+        rope_rotate(x1, x2, cs, sn, y1, y2);
+        from_f(y1, b1[e]);
+        from_f(y2, b2[e]);
       }
       u1 = w1;
       u2 = w2;
@@ -181,6 +185,32 @@ cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s) {
   if (a.tokens == 0) return cudaSuccess;
   const int64_t blocks = (a.tokens + kTok - 1) / kTok;
   kv_append_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, f);
+  return cudaGetLastError();
+}
+
+// cos and sin of every (token, pair) angle, interleaved [tokens][d/2][2] fp32:
+// the same numbers rope_kernel rotates with, for kernels that rotate on the fly.
+__global__ void __launch_bounds__(256) rope_table_kernel(float2* __restrict__ cs_out, int64_t tokens, int d,
+                                                         const int32_t* __restrict__ pos, const InvFreq f) {
+  __shared__ float cs_s[kTok][128], sn_s[kTok][128];
+  const int half = d / 2;
+  const int64_t t0 = (int64_t)blockIdx.x * kTok;
+  angle_tables(cs_s, sn_s, t0, tokens, half, pos, f);
+  for (int i = threadIdx.x; i < kTok * half; i += blockDim.x) {
+    const int tt = i / half, ii = i % half;
+    const int64_t t = t0 + tt;
+    if (t < tokens) cs_out[t * half + ii] = make_float2(cs_s[tt][ii], sn_s[tt][ii]);
+  }
+}
+
+cudaError_t launch_rope_table(float* cs_out, int64_t tokens, int head_dim, const int32_t* positions, double base,
+                              cudaStream_t s) {
+  InvFreq f;
+  const int half = head_dim / 2;
+  for (int i = 0; i < half; ++i) f.v[i] = pow(base, -2.0 * (double)i / (double)head_dim);
+  if (tokens == 0) return cudaSuccess;
+  const int64_t blocks = (tokens + kTok - 1) / kTok;
+  rope_table_kernel<<<(unsigned)blocks, 256, 0, s>>>((float2*)cs_out, tokens, head_dim, positions, f);
   return cudaGetLastError();
 }
 

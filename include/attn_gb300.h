@@ -79,6 +79,16 @@ ATTN_API int rope_apply(void *x, attn_dtype_t dtype, int64_t tokens, int heads, 
                int64_t stride_token, const int32_t *positions, double base, void *stream);
 
 /*
+ * rope_table -- the cos and sin of every RoPE angle, for kernels that rotate on
+ * the fly: cs_out[t][i] = (cos a, sin a), a = positions[t] * base^(-2i/head_dim),
+ * i < head_dim/2, as fp32 pairs [tokens][head_dim/2][2] (16-byte aligned).  The
+ * numbers are exactly those rope_apply rotates with (Ulysses page, sections
+ * 3.2 and 5.3: absolute positions).  head_dim even, <= 256; base > 0.
+ */
+ATTN_API int rope_table(const int32_t *positions, int64_t tokens, int head_dim, double base, float *cs_out,
+                        void *stream);
+
+/*
  * attn_kv_append_paged -- write a chunk of new tokens' keys and values into the
  * head-major paged KV cache, rotating the keys (RoPE at their absolute
  * positions) on the way.
@@ -161,6 +171,24 @@ ATTN_API int attn_prefill(const void *q, const void *k, const void *v, void *out
                  const int32_t *page_table, const int32_t *k_lens, int max_pages, int page_size,
                  int64_t num_pages, int num_q_heads, int num_kv_heads, int head_dim, int h_lo,
                  int h_hi, float scale, int causal, void *stream);
+
+/*
+ * attn_prefill_rope_q -- attn_prefill with the query's RoPE fused in: q holds
+ * UNROTATED queries, and the kernel rotates each query row in on-chip memory,
+ * with the cos/sin of q_rope_cs ([total_q][head_dim/2][2] fp32 from rope_table
+ * over q_pos, 16-byte aligned), before its scores.  The result equals
+ * rope_apply(q) followed by attn_prefill bit for bit; q itself is not
+ * modified.  Keys must already be rotated (rope_apply or attn_kv_append_paged).
+ * Only the tensor-core path takes it (bf16, head_dim 128); other shapes return
+ * ATTN_ERR_UNSUPPORTED.  All other arguments as attn_prefill.
+ */
+ATTN_API int attn_prefill_rope_q(const void *q, const void *k, const void *v, void *out, attn_dtype_t out_dtype,
+                                 float *lse, attn_dtype_t dtype, int batch, const int32_t *cu_q,
+                                 const int32_t *q_pos, int64_t total_q, int max_seqlen_q, const int32_t *cu_k,
+                                 const int32_t *k_pos, int64_t total_k, const int32_t *page_table,
+                                 const int32_t *k_lens, int max_pages, int page_size, int64_t num_pages,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int h_lo, int h_hi, float scale,
+                                 int causal, const float *q_rope_cs, void *stream);
 
 /*
  * attn_decode_paged -- split-KV decode over a head-major paged KV cache.

@@ -146,3 +146,19 @@ def test_decode_int8_rejects_bad_arguments(lib):
     assert call(vs=8) == ERR_ALIGN
     assert call(kc=24) == ERR_ALIGN
     assert call(batch=0) == 0
+
+
+def test_rope_table_and_fused_prefill_reject_bad_arguments(lib):
+    assert lib.rope_table(16, 4, 127, 1e4, 16, None) == ERR_SHAPE     # odd head_dim
+    assert lib.rope_table(16, 4, 128, 0.0, 16, None) == ERR_ARG       # base
+    assert lib.rope_table(None, 4, 128, 1e4, 16, None) == ERR_ARG
+    assert lib.rope_table(16, 4, 128, 1e4, 8, None) == ERR_ALIGN
+    assert lib.rope_table(16, 0, 128, 1e4, None, None) == 0
+    a = dict(q=16, k=16, v=16, out=16, out_dtype=0, lse=None, dtype=0, batch=1, cu_q=16, q_pos=16, total_q=4,
+             max_seqlen_q=4, cu_k=16, k_pos=16, total_k=4, page_table=None, k_lens=None, max_pages=0,
+             page_size=0, num_pages=0, hq=8, hkv=2, d=128, h_lo=0, h_hi=8, scale=0.1, causal=1)
+    f = lib.attn_prefill_rope_q
+    assert f(*a.values(), None, None) == ERR_ARG      # no table
+    assert f(*a.values(), 8, None) == ERR_ALIGN       # misaligned table
+    a["d"] = 96
+    assert f(*a.values(), 16, None) == ERR_SHAPE      # prefill's own checks still apply

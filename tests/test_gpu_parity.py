@@ -677,3 +677,81 @@ def test_decode_int8_value_beyond_fp16_is_reported():
         atc.attn_device_status(clear=True)
     assert e.value.status == 6
     atc.attn_device_status(clear=True)
+
+
+# ------------------------------------------------------------------ query RoPE fused into prefill
+
+def test_rope_table_matches_the_angles():
+    T, d = 700, 128
+    pos = np.sort(np.random.default_rng(4).integers(0, 131072, T)).astype(np.int32)
+    pos[:3] = [0, 1, 131071]
+    tab = atc.rope_table(torch.from_numpy(pos).to(DEV), d).cpu().numpy().astype(np.float64)
+    ang = pos[:, None].astype(np.float64) * (10000.0 ** (-2.0 * np.arange(d // 2) / d))[None, :]
+    assert np.abs(tab[..., 0] - np.cos(ang)).max() < 2e-6
+    assert np.abs(tab[..., 1] - np.sin(ang)).max() < 2e-6
+    np.testing.assert_array_equal(tab[0, :, 0], 1.0)   # position 0: cos 1, sin 0
+    np.testing.assert_array_equal(tab[0, :, 1], 0.0)
+
+
+@pytest.mark.parametrize("lens,hq,hkv,starts", CASES)
+def test_prefill_fused_query_rope_equals_rope_apply_then_prefill(lens, hq, hkv, starts):
+    """The kernel rotates the unrotated queries itself, with rope_apply's cos/sin
+    and rounding: outputs and LSE are bit-identical, and q is left unrotated."""
+    q, k, v, pos, cu = _bf16_case(lens, hq, hkv, starts, 600 + hq + len(lens))
+    out_ref, lse_ref = _run_prefill(q, k, v, pos, cu, lens)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    posd, cud = torch.from_numpy(pos).to(DEV), torch.from_numpy(cu).to(DEV)
+    atc.rope_apply(kd, posd)
+    tab = atc.rope_table(posd, q.shape[2])
+    out = torch.full(q.shape, float("nan"), dtype=q.dtype, device=DEV)
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    atc.attn_prefill(qd, kd, vd, out, lse, cud, posd, max(lens), cu_k=cud, k_pos=posd, q_rope_cs=tab)
+    atc.attn_device_status()
+    assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
+    assert torch.equal(qd.cpu(), q)  # the caller's q is not modified
+    want_o, want_l = _oracle_prefill(q, k, v, pos, cu, lens, 128 ** -0.5)
+    check(out, lse, want_o, want_l, what=f"fused query RoPE {lens}")
+
+
+def test_prefill_fused_query_rope_head_slices_and_paged_source():
+    """Head slices of the fused call equal the all-heads call; the paged source
+    (chunk over a cached prefix) takes the fused rotation too."""
+    lens = [600]
+    q, k, v, pos, cu = _bf16_case(lens, 64, 8, [0], 610)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    posd, cud = torch.from_numpy(pos).to(DEV), torch.from_numpy(cu).to(DEV)
+    atc.rope_apply(kd, posd)
+    tab = atc.rope_table(posd, 128)
+    full_o, full_l = atc.prefill(qd, kd, vd, cud, posd, 600, cu_k=cud, k_pos=posd, q_rope_cs=tab)
+    for lo, hi in ((16, 32), (56, 64)):
+        o, l = atc.prefill(qd, kd, vd, cud, posd, 600, cu_k=cud, k_pos=posd, q_rope_cs=tab, h_lo=lo, h_hi=hi)
+        assert torch.equal(o[:, lo:hi], full_o[:, lo:hi]) and torch.equal(l[:, lo:hi], full_l[:, lo:hi])
+    # paged: the chunk's queries over a cache that holds prefix + chunk
+    prefix, chunk, hq2, hkv2, d = [100, 300], [150, 64], 16, 2, 128
+    table, num_pages, kc0, vc0, kn, vn, ppos, slots = _append_inputs(prefix, chunk, hkv2, d, 620)
+    T = kn.shape[0]
+    q2 = synth.randn((T, hq2, d), 626, 0.7071).to(DEV)
+    pposd = torch.from_numpy(ppos).to(DEV)
+    kc, vc = kc0.to(DEV), vc0.to(DEV)
+    atc.attn_kv_append_paged(kn.to(DEV), vn.to(DEV), pposd, torch.from_numpy(slots).to(DEV), kc, vc)
+    cu_q = torch.from_numpy(synth.cu_seqlens(chunk)).to(DEV)
+    klens = torch.tensor([p + c for p, c in zip(prefix, chunk)], dtype=torch.int32, device=DEV)
+    tabled = torch.from_numpy(table).to(DEV)
+    o_f, l_f = atc.prefill(q2, kc, vc, cu_q, pposd, max(chunk), page_table=tabled, k_lens=klens,
+                           num_pages=num_pages, q_rope_cs=atc.rope_table(pposd, d))
+    q2r = q2.clone()
+    atc.rope_apply(q2r, pposd)
+    o_r, l_r = atc.prefill(q2r, kc, vc, cu_q, pposd, max(chunk), page_table=tabled, k_lens=klens,
+                           num_pages=num_pages)
+    atc.attn_device_status()
+    assert torch.equal(o_f, o_r) and torch.equal(l_f, l_r)
+
+
+def test_prefill_fused_query_rope_needs_the_tensor_core_path():
+    q = torch.zeros((8, 8, 64), dtype=torch.float32, device=DEV)
+    pos = torch.arange(8, dtype=torch.int32, device=DEV)
+    cu = torch.tensor([0, 8], dtype=torch.int32, device=DEV)
+    with pytest.raises(atc.AttnError) as e:
+        atc.prefill(q, q[:, :2].contiguous(), q[:, :2].contiguous(), cu, pos, 8, cu_k=cu, k_pos=pos,
+                    q_rope_cs=atc.rope_table(pos, 64))
+    assert e.value.status == 4
