@@ -56,6 +56,8 @@ def _load():
         lib.oracle_kv_append.argtypes = [P, P, P, P, I64, I32, I32, P, P, I64, D]
         lib.oracle_kv_append.restype = I32
         lib.oracle_dequant_int8.argtypes = [P, P, I64, I32, P]
+        lib.oracle_kv_append_int8.argtypes = [P, P, P, P, I64, I32, I32, P, P, P, P, I64, D]
+        lib.oracle_kv_append_int8.restype = I32
         lib.oracle_num_threads.restype = I32
         lib.oracle_set_num_threads.argtypes = [I32]
         _lib = lib
@@ -197,3 +199,22 @@ def dequant_int8(codes, scales) -> np.ndarray:
     out = np.empty(codes.shape, dtype=np.float64)
     _load().oracle_dequant_int8(_p(codes), _p(scales), rows, d, _p(out))
     return out
+
+
+def kv_append_int8(k_new, v_new, pos, slots, k_codes, v_codes, k_scale, v_scale, base: float = 10000.0):
+    """kv_append into an INT8 cache: keys rotated at `pos` and rounded to bf16, then
+    every key and value row quantised (scale = max|x| / 127 in fp32, codes rounded
+    to nearest even).  Returns copies (k_codes, v_codes, k_scale, v_scale, n_bad)."""
+    k_new, v_new = _f64(k_new), _f64(v_new)
+    T, H, d = k_new.shape
+    kc = np.array(k_codes, dtype=np.int8, copy=True)
+    vc = np.array(v_codes, dtype=np.int8, copy=True)
+    ks = np.array(k_scale, dtype=np.float32, copy=True)
+    vs = np.array(v_scale, dtype=np.float32, copy=True)
+    rows = kc.shape[1] * kc.shape[2]
+    pos = _i32(pos if pos is not None else np.zeros(T, np.int32))
+    bad = _load().oracle_kv_append_int8(_p(k_new), _p(v_new), _p(pos), _p(_i32(slots)), T, H, d, _p(kc), _p(vc),
+                                        _p(ks), _p(vs), rows, float(base))
+    if bad < 0:
+        raise MemoryError("oracle_kv_append_int8: out of memory")
+    return kc, vc, ks, vs, bad

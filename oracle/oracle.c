@@ -256,6 +256,62 @@ void oracle_dequant_int8(const int8_t *codes, const float *scales, int64_t rows,
             out[r * d + i] = (double)codes[r * d + i] * (double)scales[r];
 }
 
+/* Symmetric INT8 quantisation of one cache row (the reading taken of the
+ * Flash Attention page, section 18.12, and the Ulysses page, section 5.4:
+ * grouped codes with a scale, the group being one (KV head, token) row).  In
+ * fp32, as the path decides it: scale = max|x| / 127, code = x / scale rounded
+ * to the nearest integer (ties to even), clamped to [-127, 127]; an all-zero
+ * row has scale 0 and codes 0.  x holds d values that are exact in fp32. */
+static void quant_row_int8(const double *x, int d, int8_t *codes, float *scale)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < d; ++i) {
+        float a = fabsf((float)x[i]);
+        if (a > amax) amax = a;
+    }
+    float s = amax / 127.0f;
+    *scale = s;
+    for (int i = 0; i < d; ++i) {
+        if (s == 0.0f) { codes[i] = 0; continue; }
+        float q = rintf((float)x[i] / s);
+        if (q > 127.0f) q = 127.0f;
+        if (q < -127.0f) q = -127.0f;
+        codes[i] = (int8_t)q;
+    }
+}
+
+/* oracle_kv_append for an INT8 cache: keys rotated (base > 0) and rounded to
+ * bf16, as the bf16 cache would hold them, then each key and value row is
+ * quantised by quant_row_int8 into codes [heads][rows][d] and scales
+ * [heads][rows].  Slot -1 skips a token; returns the number of tokens whose
+ * slot lies outside [-1, rows), which are skipped too. */
+int oracle_kv_append_int8(const double *k_new, const double *v_new, const int32_t *pos, const int32_t *slots,
+                          int64_t tokens, int heads, int d, int8_t *k_codes, int8_t *v_codes, float *k_scale,
+                          float *v_scale, int64_t rows, double base)
+{
+    int bad = 0;
+    double *krow = malloc((size_t)d * sizeof(double));
+    if (!krow) return -1;
+    for (int64_t t = 0; t < tokens; ++t) {
+        const int64_t s = slots[t];
+        if (s == -1) continue;
+        if (s < -1 || s >= rows) { ++bad; continue; }
+        for (int h = 0; h < heads; ++h) {
+            const double *src = k_new + (t * heads + h) * (int64_t)d;
+            for (int i = 0; i < d; ++i) krow[i] = src[i];
+            if (base > 0.0) {
+                oracle_rope(krow, 1, 1, d, pos + t, base);
+                oracle_round_bf16(krow, d);
+            }
+            const int64_t r = (int64_t)h * rows + s;
+            quant_row_int8(krow, d, k_codes + r * d, k_scale + r);
+            quant_row_int8(v_new + (t * heads + h) * (int64_t)d, d, v_codes + r * d, v_scale + r);
+        }
+    }
+    free(krow);
+    return bad;
+}
+
 /* Decode: q [B][hq][d] (already rotated, at position ctx_b - 1) against the
  * ctx_b cached tokens of request b.  out [B][hq][d], lse [B][hq]. */
 int oracle_decode_paged(const double *q, const double *k_cache, const double *v_cache,

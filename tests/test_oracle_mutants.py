@@ -26,6 +26,8 @@ MUTANTS = [
     ("append row of head", "double *kd = k_cache + ((int64_t)h * rows + s) * d;",
      "double *kd = k_cache + ((int64_t)s * heads + h) * d;", False),
     ("int8 scale of the wrong token", "(double)scales[r];", "(double)scales[r > 0 ? r - 1 : r];", False),
+    ("int8 scale over 128", "float s = amax / 127.0f;", "float s = amax / 128.0f;", False),
+    ("int8 rounding toward zero", "float q = rintf((float)x[i] / s);", "float q = truncf((float)x[i] / s);", False),
     ("append rotates values", "const double *vs = v_new + (t * heads + h) * (int64_t)d;",
      "const double *vs = krow - (int64_t)0 * (t * heads + h);", False),
 ]

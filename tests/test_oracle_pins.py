@@ -522,3 +522,66 @@ def test_decode_over_unit_scale_int8_cache_is_decode_over_the_codes():
                             np.array(ctx, np.int32), num_pages, 0.1)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------------ INT8 append (quantisation)
+
+def _q_case(rows_k, rows_v=None):
+    """One token, one head: k_new / v_new rows given explicitly; 1 page of 2 slots."""
+    k = np.asarray(rows_k, np.float64)[None, None, :]
+    v = np.asarray(rows_v if rows_v is not None else rows_k, np.float64)[None, None, :]
+    d = k.shape[-1]
+    z8 = np.zeros((1, 1, 2, d), np.int8)
+    zs = np.zeros((1, 1, 2), np.float32)
+    return k, v, z8, zs
+
+
+def test_int8_append_hand_quantisation():
+    """max|x| = 2.54 -> scale 0.02 (fp32); 2.54 -> 127, -1.27 -> -63.5 -> -64 (ties to even),
+    0.01 -> 0.5 -> 0, 0.03 -> 1.5 -> 2."""
+    row = [2.54, -1.27, 0.01, 0.03]
+    k, v, z8, zs = _q_case(row)
+    kc, vc, ks, vs, bad = oracle.kv_append_int8(k, v, None, [1], z8, z8, zs, zs, base=0.0)
+    s = np.float32(2.54) / np.float32(127.0)
+    assert ks[0, 0, 1] == s and vs[0, 0, 1] == s
+    want = [int(np.rint(np.float32(x) / s)) for x in row]
+    assert want[0] == 127
+    np.testing.assert_array_equal(kc[0, 0, 1], want)
+    np.testing.assert_array_equal(vc[0, 0, 1], want)
+    np.testing.assert_array_equal(kc[0, 0, 0], 0)  # slot 0 untouched
+    assert bad == 0
+
+
+def test_int8_append_zero_row_and_error_bound():
+    k, v, z8, zs = _q_case([0.0, 0.0, 0.0, 0.0], [0.5, -0.25, 3.0, 1e-3])
+    kc, vc, ks, vs, _ = oracle.kv_append_int8(k, v, None, [0], z8, z8, zs, zs, base=0.0)
+    assert ks[0, 0, 0] == 0 and (kc[0, 0, 0] == 0).all()
+    # any row: |code * scale - x| <= scale / 2, and the largest |x| maps to +-127
+    rng = np.random.default_rng(99)
+    for _ in range(50):
+        row = rng.normal(0, rng.uniform(0.01, 10), 16).astype(np.float32).astype(np.float64)
+        k, v, z8, zs = _q_case(row)
+        kc, vc, ks, vs, _ = oracle.kv_append_int8(k, v, None, [0], z8, z8, zs, zs, base=0.0)
+        s = float(ks[0, 0, 0])
+        back = kc[0, 0, 0].astype(np.float64) * s
+        # half a step, plus the fp32 rounding of x / scale near a .5 boundary (a few ulps of x)
+        assert (np.abs(back - row) <= s / 2 + np.abs(row) * 2.0 ** -22).all()
+        assert np.abs(kc[0, 0, 0]).max() == 127
+
+
+def test_int8_append_keys_are_quantised_bf16_rotations():
+    """With rotation, the key codes are the quantisation of what the bf16 append
+    stores: the two appends agree after dequantisation within half a step."""
+    rng = np.random.default_rng(100)
+    T, H, d = 5, 2, 8
+    kn = rng.normal(0, 1, (T, H, d))
+    vn = rng.normal(0, 1, (T, H, d))
+    pos = np.array([0, 3, 77, 1000, 65535], np.int32)
+    slots = np.arange(T, dtype=np.int32)
+    z = np.zeros((H, 2, 4, d))
+    kb, vb, _ = oracle.kv_append(kn, vn, pos, slots, z, z)
+    kc, vc, ks, vs, _ = oracle.kv_append_int8(kn, vn, pos, slots, np.zeros((H, 2, 4, d), np.int8),
+                                              np.zeros((H, 2, 4, d), np.int8), np.zeros((H, 2, 4), np.float32),
+                                              np.zeros((H, 2, 4), np.float32))
+    kd = oracle.dequant_int8(kc, ks)
+    assert np.all(np.abs(kd - kb) <= ks[..., None].astype(np.float64) / 2 + np.abs(kb) * 2.0 ** -22)
