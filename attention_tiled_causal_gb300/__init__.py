@@ -12,6 +12,7 @@ Entry points (same names as the C ABI):
     attn_prefill(..., q_rope_cs=table)                  attention with the query's RoPE fused in
     attn_kv_append_paged(k_new, v_new, positions, slots, k_cache, v_cache)
                                                         new K (rotated) / V into the paged cache
+    attn_kv_append_paged_int8(..., k_scale, v_scale)    the same into an INT8 cache (quantising)
     attn_prefill(q, k, v, out, lse, cu_q, q_pos, ...)   tiled causal GQA attention
     attn_decode_paged(q, k_cache, v_cache, ...)         split-KV decode over a paged cache
     attn_decode_paged_int8(q, k_codes, v_codes, k_scale, v_scale, ...)   the same over an INT8 cache
@@ -19,9 +20,9 @@ Entry points (same names as the C ABI):
 """
 from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_decode_paged_int8,
                        attn_device_status,
-                       attn_kv_append_paged, attn_lse_merge, attn_prefill, decode_workspace, lib_path, library,
+                       attn_kv_append_paged, attn_kv_append_paged_int8, attn_lse_merge, attn_prefill, decode_workspace, lib_path, library,
                        prefill, rope_apply, rope_table)
 
 __all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_decode_paged_int8", "attn_device_status",
-           "attn_kv_append_paged", "attn_lse_merge", "attn_prefill", "decode_workspace", "lib_path", "library",
+           "attn_kv_append_paged", "attn_kv_append_paged_int8", "attn_lse_merge", "attn_prefill", "decode_workspace", "lib_path", "library",
            "prefill", "rope_apply", "rope_table"]

@@ -47,6 +47,8 @@ def library():
     lib.attn_prefill_rope_q.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, I64, I32, P, P, I64, P, P, I32, I32,
                                         I64, I32, I32, I32, I32, I32, F32, I32, P, P]
     lib.attn_prefill_rope_q.restype = I32
+    lib.attn_kv_append_paged_int8.argtypes = [P, P, P, P, I64, I32, I32, P, P, P, P, I64, I32, P, F64, P]
+    lib.attn_kv_append_paged_int8.restype = I32
     lib.attn_kv_append_paged.argtypes = [P, P, P, P, I64, I32, I32, P, P, I64, I32, P, F64, P]
     lib.attn_kv_append_paged.restype = I32
     lib.attn_prefill.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, I64, I32, P, P, I64, P, P, I32, I32, I64,
@@ -160,6 +162,41 @@ def rope_table(positions, head_dim: int, base: float = 10000.0, out=None, stream
         raise ValueError("out must be a contiguous float32 [tokens, head_dim/2, 2] tensor")
     _check(library().rope_table(_ptr(positions), T, int(head_dim), float(base), _ptr(out), _stream(stream)))
     return out
+
+
+def attn_kv_append_paged_int8(k_new, v_new, positions, slots, k_cache, v_cache, k_scale, v_scale, *,
+                              k_rot_out=None, base: float = 10000.0, stream=None) -> None:
+    """attn_kv_append_paged into an INT8 cache: code caches [Hkv, num_pages, page, 128]
+    int8 and scales [Hkv, num_pages, page] fp32; keys rotated and rounded to bf16,
+    then every row quantised (scale = max|x| / 127)."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        if not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{n} must be contiguous bf16")
+    T, hkv, d = k_new.shape
+    if tuple(v_new.shape) != (T, hkv, d):
+        raise ValueError("v_new must have k_new's shape")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        if t.dtype != torch.int8 or not t.is_contiguous() or t.dim() != 4 or t.shape[0] != hkv or t.shape[3] != d:
+            raise ValueError(f"{n} must be a contiguous int8 [Hkv, num_pages, page, d] tensor")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != tuple(k_cache.shape[:3]):
+            raise ValueError(f"{n} must be a contiguous float32 [Hkv, num_pages, page] tensor")
+    if k_rot_out is not None and (tuple(k_rot_out.shape) != (T, hkv, d) or not k_rot_out.is_contiguous()
+                                  or k_rot_out.dtype != torch.bfloat16):
+        raise ValueError("k_rot_out must be contiguous bf16 shaped like k_new")
+    slots = _i32(slots, "slots")
+    if slots.numel() != T:
+        raise ValueError("slots must hold one entry per token")
+    pos_ptr = None
+    if base > 0:
+        positions = _i32(positions, "positions")
+        if positions.numel() != T:
+            raise ValueError("positions must hold one entry per token")
+        pos_ptr = _ptr(positions)
+    _check(library().attn_kv_append_paged_int8(
+        _ptr(k_new), _ptr(v_new), pos_ptr, _ptr(slots), T, hkv, d, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), k_cache.shape[1], k_cache.shape[2], _ptr(k_rot_out) if k_rot_out is not None else None,
+        float(base), _stream(stream)))
 
 
 def attn_prefill(q, k, v, out, lse, cu_q, q_pos, max_seqlen_q: int, *, cu_k=None, k_pos=None,

@@ -198,6 +198,30 @@ int attn_kv_append_paged(const void* k_new, const void* v_new, const int32_t* po
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_kv_append_paged launch");
 }
 
+int attn_kv_append_paged_int8(const void* k_new, const void* v_new, const int32_t* positions, const int32_t* slots,
+                              int64_t tokens, int num_kv_heads, int head_dim, void* k_cache, void* v_cache,
+                              float* k_scale, float* v_scale, int64_t num_pages, int page_size, void* k_rot_out,
+                              double base, void* stream) {
+  if (tokens < 0 || num_kv_heads < 0 || num_pages < 0 || page_size <= 0)
+    return fail(ATTN_ERR_ARG, "attn_kv_append_paged_int8: negative size");
+  if (head_dim != 128) return fail(ATTN_ERR_SHAPE, "attn_kv_append_paged_int8: head_dim %d (need 128)", head_dim);
+  if (!(base >= 0.0)) return fail(ATTN_ERR_ARG, "attn_kv_append_paged_int8: base must be >= 0 (0 = no rotation)");
+  if (tokens == 0 || num_kv_heads == 0) return ATTN_OK;
+  if (!k_new || !v_new || !slots || !k_cache || !v_cache || !k_scale || !v_scale || (base > 0.0 && !positions))
+    return fail(ATTN_ERR_ARG, "attn_kv_append_paged_int8: null pointer");
+  if (num_pages == 0) return fail(ATTN_ERR_ARG, "attn_kv_append_paged_int8: empty cache");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
+      !aligned16(v_scale) || (k_rot_out && !aligned16(k_rot_out)))
+    return fail(ATTN_ERR_ALIGN, "attn_kv_append_paged_int8: tensors must be 16-byte aligned");
+  unsigned* err = nullptr;
+  int rc = device_error_ptr(&err);
+  if (rc) return rc;
+  attn::AppendLaunch a{k_new, v_new, positions, slots, tokens, num_kv_heads, head_dim, k_cache, v_cache,
+                       num_pages * (int64_t)page_size, k_rot_out, base, err, k_scale, v_scale};
+  cudaError_t e = attn::launch_kv_append_int8(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_kv_append_paged_int8 launch");
+}
+
 }  // extern "C"
 
 namespace {

@@ -34,8 +34,11 @@ struct AppendLaunch {
   void* k_rot_out;
   double base;  // 0: copy keys unrotated
   unsigned* err;
+  float* k_scale = nullptr;  // INT8 cache: per-row scales (k_cache / v_cache then hold int8 codes)
+  float* v_scale = nullptr;
 };
 cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s);
+cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s);
 
 struct MergeLaunch {
   const float* part_out;

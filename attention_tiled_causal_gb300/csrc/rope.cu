@@ -188,6 +188,108 @@ cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// One cache row of 128 values (4 per lane of a warp) quantised to symmetric
+// int8: scale = max|x| / 127, code = x / scale rounded to the nearest integer
+// (ties to even) and clamped to [-127, 127], all in fp32; an all-zero row gets
+// scale 0 and codes 0.  The 128 codes go to dst (4 bytes per lane).
+__device__ __forceinline__ void quant_store_int8(const float (&x)[4], int lane, int8_t* dst, float* scale_dst) {
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float sc = amax / 127.0f;
+  uint32_t packed = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float q = sc == 0.0f ? 0.0f : rintf(x[e] / sc);
+    q = fminf(fmaxf(q, -127.0f), 127.0f);
+    packed |= (uint32_t)(uint8_t)(int8_t)(int)q << (8 * e);
+  }
+  *reinterpret_cast<uint32_t*>(dst + 4 * lane) = packed;
+  if (lane == 0) *scale_dst = sc;
+}
+
+// kv_append_kernel for an INT8 cache: one warp per (token, KV head), lane l
+// holding dims 4l..4l+3.  A key is rotated exactly as rope_kernel rotates it
+// (its RoPE partner sits 16 lanes away) and rounded to bf16 -- the value a
+// bf16 cache would hold -- before both rows are quantised.
+__global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendLaunch a, const InvFreq f) {
+  __shared__ float cs_s[kTok][128], sn_s[kTok][128];
+  __shared__ int64_t slot_s[kTok];
+  const int64_t t0 = (int64_t)blockIdx.x * kTok;
+  if (threadIdx.x < kTok) {
+    const int64_t t = t0 + threadIdx.x;
+    int64_t sl = -1;
+    if (t < a.tokens) {
+      sl = __ldg(a.slots + t);
+      if (sl < -1 || sl >= a.cache_rows) {
+        record_error(a.err, DEV_BAD_SLOT);
+        sl = -1;
+      }
+    }
+    slot_s[threadIdx.x] = sl;
+  }
+  const bool rotate = a.base > 0.0;
+  if (rotate) angle_tables(cs_s, sn_s, t0, a.tokens, 64, a.positions, f);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
+  const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
+  int8_t* kc = (int8_t*)a.k_cache;
+  int8_t* vc = (int8_t*)a.v_cache;
+  __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
+  for (int w = warp; w < kTok * a.heads; w += blockDim.x / 32) {
+    const int tt = w / a.heads, h = w % a.heads;
+    const int64_t sl = slot_s[tt];
+    if (sl < 0) continue;
+    const int64_t t = t0 + tt;
+    const int64_t src = (t * a.heads + h) * 128 + 4 * lane;
+    const int64_t row = (int64_t)h * a.cache_rows + sl;
+    float x[4];
+    {
+      const uint2 w2 = __ldg(reinterpret_cast<const uint2*>(kn + src));
+      x[0] = __uint_as_float(w2.x << 16), x[1] = __uint_as_float(w2.x & 0xffff0000u);
+      x[2] = __uint_as_float(w2.y << 16), x[3] = __uint_as_float(w2.y & 0xffff0000u);
+    }
+    if (rotate) {
+      const int i0 = 4 * (lane & 15);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float xp = __shfl_xor_sync(0xffffffffu, x[e], 16);
+        float y1, y2;
+        if (lane < 16)
+          rope_rotate(x[e], xp, cs_s[tt][i0 + e], sn_s[tt][i0 + e], y1, y2);
+        else
+          rope_rotate(xp, x[e], cs_s[tt][i0 + e], sn_s[tt][i0 + e], y1, y2);
+        x[e] = __bfloat162float(__float2bfloat16_rn(lane < 16 ? y1 : y2));
+      }
+      if (ko) {
+        uint2 o2;
+        o2.x = pack_bf16x2(x[0], x[1]);
+        o2.y = pack_bf16x2(x[2], x[3]);
+        *reinterpret_cast<uint2*>(ko + src) = o2;
+      }
+    } else if (ko) {
+      *reinterpret_cast<uint2*>(ko + src) = __ldg(reinterpret_cast<const uint2*>(kn + src));
+    }
+    quant_store_int8(x, lane, kc + row * 128, a.k_scale + row);
+    {
+      const uint2 w2 = __ldg(reinterpret_cast<const uint2*>(vn + src));
+      x[0] = __uint_as_float(w2.x << 16), x[1] = __uint_as_float(w2.x & 0xffff0000u);
+      x[2] = __uint_as_float(w2.y << 16), x[3] = __uint_as_float(w2.y & 0xffff0000u);
+    }
+    quant_store_int8(x, lane, vc + row * 128, a.v_scale + row);
+  }
+}
+
+cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s) {
+  InvFreq f;
+  for (int i = 0; i < 64; ++i) f.v[i] = a.base > 0.0 ? pow(a.base, -2.0 * (double)i / 128.0) : 0.0;
+  if (a.tokens == 0) return cudaSuccess;
+  const int64_t blocks = (a.tokens + kTok - 1) / kTok;
+  kv_append_int8_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, f);
+  return cudaGetLastError();
+}
+
 // cos and sin of every (token, pair) angle, interleaved [tokens][d/2][2] fp32:
 // the same numbers rope_kernel rotates with, for kernels that rotate on the fly.
 __global__ void __launch_bounds__(256) rope_table_kernel(float2* __restrict__ cs_out, int64_t tokens, int d,

@@ -405,7 +405,20 @@ def chunked_arm(wl, args, timer, peaks, peak_src):
     ms_a, _ = timer.run(append, steps, warmup)
     atc.attn_device_status()
     append_bytes = 2 * 2 * k_raw.numel() * 2  # read K and V, write both into the cache
-    del kc2, vc2, k_raw, q, k, v, out, lse
+    del kc2, vc2
+    # the same chunk into an INT8 cache (codes + one fp32 scale per row)
+    kc8 = torch.zeros((wl.hkv, npg2, synth.PAGE, wl.d), dtype=torch.int8, device="cuda")
+    vc8 = torch.zeros_like(kc8)
+    ks8 = torch.zeros((wl.hkv, npg2, synth.PAGE), dtype=torch.float32, device="cuda")
+    vs8 = torch.zeros_like(ks8)
+
+    def append8(ev=()):
+        atc.attn_kv_append_paged_int8(k_raw, v, qposd, slots, kc8, vc8, ks8, vs8)
+
+    ms_a8, _ = timer.run(append8, steps, warmup)
+    atc.attn_device_status()
+    append8_bytes = 2 * k_raw.numel() * 2 + 2 * (k_raw.numel() + k_raw.numel() // wl.d * 4)
+    del kc8, vc8, ks8, vs8, k_raw, q, k, v, out, lse
     peak = peaks["bf16_tflops"]
     fl = wl.flops()
     fl_c = 4.0 * wl.d * wl.hq * wl.batch * (C * (C + 1) // 2)
@@ -425,7 +438,9 @@ def chunked_arm(wl, args, timer, peaks, peak_src):
                 "value": round(fl / (ms_f * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "frac": round(fl / (ms_f * 1e-3) / 1e12 / peak, 4),
                 "append": hbm_line("attn_kv_append_paged (4 x 8192 tokens, 8 KV heads)", append_bytes, ms_a, peaks,
-                                   peak_src)}}
+                                   peak_src),
+                "append_int8": hbm_line("attn_kv_append_paged_int8 (the same chunk into an INT8 cache)",
+                                        append8_bytes, ms_a8, peaks, peak_src)}}
 
 
 def decode_int8_arm(wl, args, timer, peaks, peak_src):

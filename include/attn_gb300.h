@@ -123,6 +123,26 @@ ATTN_API int attn_kv_append_paged(const void *k_new, const void *v_new, const in
                                   void *k_rot_out, double base, void *stream);
 
 /*
+ * attn_kv_append_paged_int8 -- attn_kv_append_paged into an INT8 cache (the
+ * cache attn_decode_paged_int8 reads).  Keys are rotated exactly as
+ * attn_kv_append_paged rotates them and rounded to bf16; then every key and
+ * value row of 128 values is quantised to symmetric int8 in fp32: scale =
+ * max|x| / 127, code = x / scale rounded to nearest (ties to even), clamped
+ * to [-127, 127]; an all-zero row gets scale 0 ("Flash Attention and
+ * distributed parallelism", section 18.12; Ulysses page, section 5.4).
+ *
+ *  k_cache, v_cache  [num_kv_heads][num_pages][page_size][128] int8 codes.
+ *  k_scale, v_scale  [num_kv_heads][num_pages][page_size] fp32 (16-byte aligned).
+ *  k_rot_out         NULL, or the rotated bf16 keys [tokens][num_kv_heads][128].
+ *  Everything else as attn_kv_append_paged (head_dim must be 128).
+ */
+ATTN_API int attn_kv_append_paged_int8(const void *k_new, const void *v_new, const int32_t *positions,
+                                       const int32_t *slots, int64_t tokens, int num_kv_heads, int head_dim,
+                                       void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                                       int64_t num_pages, int page_size, void *k_rot_out, double base,
+                                       void *stream);
+
+/*
  * attn_prefill -- exact causal GQA attention, FlashAttention-style tiled.
  *
  * Computes, for every query row of every sequence and every query head h in

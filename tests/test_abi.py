@@ -162,3 +162,19 @@ def test_rope_table_and_fused_prefill_reject_bad_arguments(lib):
     assert f(*a.values(), 8, None) == ERR_ALIGN       # misaligned table
     a["d"] = 96
     assert f(*a.values(), 16, None) == ERR_SHAPE      # prefill's own checks still apply
+
+
+def test_kv_append_int8_rejects_bad_arguments(lib):
+    base = dict(kn=16, vn=16, pos=16, slots=16, T=4, H=8, d=128, kc=16, vc=16, ks=16, vs=16, pages=10, page=64,
+                ko=None, rope_base=1e4, stream=None)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return lib.attn_kv_append_paged_int8(*a.values())
+
+    assert call(d=64) == ERR_SHAPE
+    assert call(rope_base=-1.0) == ERR_ARG
+    assert call(ks=None) == ERR_ARG
+    assert call(vs=8) == ERR_ALIGN
+    assert call(T=0) == 0

@@ -755,3 +755,77 @@ def test_prefill_fused_query_rope_needs_the_tensor_core_path():
         atc.prefill(q, q[:, :2].contiguous(), q[:, :2].contiguous(), cu, pos, 8, cu_k=cu, k_pos=pos,
                     q_rope_cs=atc.rope_table(pos, 64))
     assert e.value.status == 4
+
+
+# ------------------------------------------------------------------ append into an INT8 cache
+
+def _int8_cache(hkv, num_pages, seed):
+    kc = synth.randint8((hkv, num_pages, 64, 128), seed)
+    vc = synth.randint8((hkv, num_pages, 64, 128), seed + 1)
+    ks = synth.uniform((hkv, num_pages, 64), seed + 2, 0.01, 0.02)
+    vs = synth.uniform((hkv, num_pages, 64), seed + 3, 0.01, 0.02)
+    return kc, vc, ks, vs
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+def test_kv_append_int8_matches_oracle(rotate):
+    """Codes and scales as the oracle decides them in fp32.  Unrotated rows and all
+    value rows are bit-exact; rotated key codes follow the bf16 rotation, which
+    may differ from the oracle's by one ulp in rare elements, so their codes are
+    within one step and almost all equal.  Other cache rows stay untouched."""
+    hkv, d = 8, 128
+    table, num_pages, _, _, kn, vn, pos, slots = _append_inputs([64, 130, 0], [100, 1, 260], hkv, d, 640, pad=3)
+    kc0, vc0, ks0, vs0 = _int8_cache(hkv, num_pages, 650)
+    kc, vc, ks, vs = kc0.to(DEV), vc0.to(DEV), ks0.to(DEV), vs0.to(DEV)
+    base = 10000.0 if rotate else 0.0
+    ko = torch.empty(kn.shape, dtype=torch.bfloat16, device=DEV)
+    atc.attn_kv_append_paged_int8(kn.to(DEV), vn.to(DEV), torch.from_numpy(pos).to(DEV),
+                                  torch.from_numpy(slots).to(DEV), kc, vc, ks, vs, k_rot_out=ko, base=base)
+    atc.attn_device_status()
+    wkc, wvc, wks, wvs, bad = oracle.kv_append_int8(synth.as_f64(kn), synth.as_f64(vn), pos, slots, kc0.numpy(),
+                                                    vc0.numpy(), ks0.numpy(), vs0.numpy(), base=base)
+    assert bad == 0
+    np.testing.assert_array_equal(vc.cpu().numpy(), wvc)
+    np.testing.assert_array_equal(vs.cpu().numpy(), wvs)
+    gk, gs = kc.cpu().numpy().astype(np.int32), ks.cpu().numpy()
+    if not rotate:
+        np.testing.assert_array_equal(gk, wkc)
+        np.testing.assert_array_equal(gs, wks)
+        assert torch.equal(ko[torch.from_numpy(slots >= 0).to(DEV)], kn.to(DEV)[torch.from_numpy(slots >= 0).to(DEV)])
+    else:
+        diff = np.abs(gk - wkc.astype(np.int32))
+        assert diff.max() <= 1 and (diff > 0).mean() < 0.01
+        assert np.allclose(gs, wks, rtol=2 ** -7, atol=0)
+        # the bf16 rotated keys it also wrote are rope_apply's, bit for bit
+        kr = kn.to(DEV).clone()
+        atc.rope_apply(kr, torch.from_numpy(pos).to(DEV))
+        valid = torch.from_numpy(slots >= 0).to(DEV)
+        assert torch.equal(ko[valid], kr[valid])
+
+
+def test_decode_over_int8_append_matches_oracle():
+    """Serving flow on an INT8 cache: the chunk appended (rotated, quantised), then
+    the decode of the last position of each request over the whole cache."""
+    hkv, hq, d = 2, 16, 128
+    prefix, chunk = [300, 64], [40, 1]
+    table, num_pages, _, _, kn, vn, pos, slots = _append_inputs(prefix, chunk, hkv, d, 660)
+    kc0, vc0, ks0, vs0 = _int8_cache(hkv, num_pages, 670)
+    kc, vc, ks, vs = kc0.to(DEV), vc0.to(DEV), ks0.to(DEV), vs0.to(DEV)
+    atc.attn_kv_append_paged_int8(kn.to(DEV), vn.to(DEV), torch.from_numpy(pos).to(DEV),
+                                  torch.from_numpy(slots).to(DEV), kc, vc, ks, vs)
+    ctx = np.array([p + c for p, c in zip(prefix, chunk)], np.int32)
+    q = synth.randn((2, hq, d), 680, 0.7071)
+    qpos = (ctx - 1).astype(np.int32)
+    qr = q.to(DEV).clone()
+    atc.rope_apply(qr, torch.from_numpy(qpos).to(DEV))
+    po, pl = atc.decode_workspace(2, hq, 4, d, DEV)
+    out = torch.empty((2, hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((2, hq), dtype=torch.float32, device=DEV)
+    atc.attn_decode_paged_int8(qr, kc, vc, ks, vs, torch.from_numpy(table).to(DEV), torch.from_numpy(ctx).to(DEV),
+                               4, po, pl, out, lse)
+    atc.attn_device_status()
+    wkc, wvc, wks, wvs, _ = oracle.kv_append_int8(synth.as_f64(kn), synth.as_f64(vn), pos, slots, kc0.numpy(),
+                                                  vc0.numpy(), ks0.numpy(), vs0.numpy())
+    want_o, want_l = oracle.decode_paged(rotated_bf16(q, qpos), oracle.dequant_int8(wkc, wks),
+                                         oracle.dequant_int8(wvc, wvs), table, ctx, num_pages, d ** -0.5)
+    check(out, lse, want_o, want_l, what="decode over the INT8 append")
