@@ -478,7 +478,9 @@ def decode_int8_arm(wl, args, timer, peaks, peak_src):
         "ms_per_step": round(ms, 4), "kv_bytes_per_step": kv, "workload": wl.name,
         "cached_tokens_per_s": round(tokens / (ms * 1e-3), 0),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic("decode_int8_paged_b32.md", "decode_int8.cu"),
+                     "traffic_scope": "decode_split_int8_kernel (ncu, scaled from a 4-request capture); merge not included",
                      "kernel": "attn::dec8::decode_split_int8_kernel + attn::lse_merge_kernel",
                      "kernel_ms": round(ms_kernel, 4), "peak_source": f"{peak_src} HBM copy"},
         "gpu_launches_per_step": 3,
