@@ -9,8 +9,8 @@
 // Structure as the bf16 split kernel: one CTA per (split s, KV head g, request
 // b); a producer thread streams pages through a 6-stage ring (TMA for the code
 // blocks, 128-byte swizzled; a bulk copy for the two 256-byte scale rows); four
-// consumer warps take 16 tokens each and keep online-softmax states that are
-// merged at the end.  The group contraction runs on mma.sync m16n8k16 with
+// consumer warps take 16 tokens of each page, two pages per iteration, and keep
+// online-softmax states that are merged at the end.  The group contraction runs on mma.sync m16n8k16 with
 // fp16 operands, because an int8 code becomes an fp16 value exactly with two
 // integer instructions and one packed subtract (0x6400 | (code + 128) is the
 // fp16 number 1024 + code + 128), and fp16 holds the bf16 query and the
@@ -197,41 +197,57 @@ __global__ void __launch_bounds__(NTHREADS, 2)
   const int key = kb + (mat & 1) * 8 + rr;  // ldmatrix row this lane addresses
   bool ok = true;
 
-  for (int i = 0; i < npg; ++i) {
-    const int st = i % NST;
-    ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (i / NST) & 1, a.err, DEV_TIMEOUT_DECODE));
+  // Two pages per iteration: 32 tokens of this warp, whose score chains are
+  // independent, under one online-softmax update.  An odd last page runs alone.
+  for (int i = 0; i < npg; i += 2) {
+    const bool two = i + 1 < npg;
+    const int st0 = i % NST, st1 = (i + 1) % NST;
+    ok = __all_sync(0xffffffffu, mbar_wait(&full[st0], (i / NST) & 1, a.err, DEV_TIMEOUT_DECODE) &&
+                                     (!two || mbar_wait(&full[st1], ((i + 1) / NST) & 1, a.err, DEV_TIMEOUT_DECODE)));
     if (!ok) break;
-    const uint32_t kst = sbase + st * STAGE_BYTES;
-    const uint32_t vst = kst + OFF_V;
-    const float* kss = (const float*)(smem + st * STAGE_BYTES + OFF_KS);
-    const float* vss = (const float*)(smem + st * STAGE_BYTES + OFF_VS);
-    // S = q Kcode^T for tokens kb..kb+15 (two n-tiles of 8 tokens), two k-steps per ldmatrix
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // S = q Kcode^T: n-tiles (page 0, tokens 0-7), (page 0, 8-15), (page 1, 0-7), (page 1, 8-15)
+    float sc[4][4];
 #pragma unroll
-    for (int ks = 0; ks < 8; ks += 2) {
-      uint32_t r0, r1, r2, r3;  // (n-tile 0, ks), (n-tile 1, ks), (n-tile 0, ks+1), (n-tile 1, ks+1)
-      ldsm_x4(kst + code_off(key, ks + (mat >> 1)), r0, r1, r2, r3);
-      r0 ^= 0x80808080u;
-      r1 ^= 0x80808080u;
-      r2 ^= 0x80808080u;
-      r3 ^= 0x80808080u;
-      mma_f16(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, codes_to_half2(r0, 0x5140), codes_to_half2(r0, 0x7362));
-      mma_f16(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, codes_to_half2(r1, 0x5140), codes_to_half2(r1, 0x7362));
-      mma_f16(sc[0], qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, codes_to_half2(r2, 0x5140), codes_to_half2(r2, 0x7362));
-      mma_f16(sc[1], qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, codes_to_half2(r3, 0x5140), codes_to_half2(r3, 0x7362));
+    for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+    for (int pg = 0; pg < 2; ++pg) {
+      if (pg == 1 && !two) break;
+      const uint32_t kst = sbase + (pg ? st1 : st0) * STAGE_BYTES;
+#pragma unroll
+      for (int ks = 0; ks < 8; ks += 2) {
+        uint32_t r0, r1, r2, r3;  // (n-tile 0, ks), (n-tile 1, ks), (n-tile 0, ks+1), (n-tile 1, ks+1)
+        ldsm_x4(kst + code_off(key, ks + (mat >> 1)), r0, r1, r2, r3);
+        r0 ^= 0x80808080u;
+        r1 ^= 0x80808080u;
+        r2 ^= 0x80808080u;
+        r3 ^= 0x80808080u;
+        mma_f16(sc[2 * pg], qa[ks][0], 0u, qa[ks][1], 0u, codes_to_half2(r0, 0x5140), codes_to_half2(r0, 0x7362));
+        mma_f16(sc[2 * pg + 1], qa[ks][0], 0u, qa[ks][1], 0u, codes_to_half2(r1, 0x5140),
+                codes_to_half2(r1, 0x7362));
+        mma_f16(sc[2 * pg], qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, codes_to_half2(r2, 0x5140),
+                codes_to_half2(r2, 0x7362));
+        mma_f16(sc[2 * pg + 1], qa[ks + 1][0], 0u, qa[ks + 1][1], 0u, codes_to_half2(r3, 0x5140),
+                codes_to_half2(r3, 0x7362));
+      }
     }
-    // K scales, mask of tokens past the context, online softmax for head row grp
-    const int tok0 = (p_beg + i) * PAGE + kb + 2 * tig;
+    // K scales, mask of tokens past the context (and of a missing second page),
+    // online softmax for head row grp
     float mx = -INFINITY;
 #pragma unroll
-    for (int n = 0; n < 2; ++n) {
-      const float2 ksc = *reinterpret_cast<const float2*>(kss + kb + n * 8 + 2 * tig);
-      sc[n][0] *= ksc.x;
-      sc[n][1] *= ksc.y;
+    for (int pg = 0; pg < 2; ++pg) {
+      const float* kss = (const float*)(smem + (pg ? st1 : st0) * STAGE_BYTES + OFF_KS);
+      const int tok0 = (p_beg + i + pg) * PAGE + kb + 2 * tig;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        if (tok0 + n * 8 + e >= ctx) sc[n][e] = -INFINITY;
-        mx = fmaxf(mx, sc[n][e]);
+      for (int n = 0; n < 2; ++n) {
+        float2 ksc = make_float2(0.f, 0.f);
+        if (pg == 0 || two) ksc = *reinterpret_cast<const float2*>(kss + kb + n * 8 + 2 * tig);
+        sc[2 * pg + n][0] *= ksc.x;
+        sc[2 * pg + n][1] *= ksc.y;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if ((pg == 1 && !two) || tok0 + n * 8 + e >= ctx) sc[2 * pg + n][e] = -INFINITY;
+          mx = fmaxf(mx, sc[2 * pg + n][e]);
+        }
       }
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -239,13 +255,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     const float m_new = fmaxf(m, mx);
     const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2((m - m_new) * sl2);
     const float mb = (m_new == -INFINITY) ? 0.f : m_new * sl2;
-    float p[2][2];
+    float p[4][2];
+    l *= alpha;
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         p[n][e] = fast_exp2(fmaf(sc[n][e], sl2, -mb));
-        l = (n == 0 && e == 0) ? l * alpha + p[n][e] : l + p[n][e];
+        l += p[n][e];
       }
     m = m_new;
 #pragma unroll
@@ -253,33 +270,44 @@ __global__ void __launch_bounds__(NTHREADS, 2)
       o[n][0] *= alpha;
       o[n][1] *= alpha;
     }
-    // O += (P v_scale) Vcode: A = weighted P (rows = heads, k = the warp's 16 tokens)
-    uint32_t pa0, pa2;
-    {
-      const float2 v0 = *reinterpret_cast<const float2*>(vss + kb + 2 * tig);
-      const float2 v1 = *reinterpret_cast<const float2*>(vss + kb + 8 + 2 * tig);
-      const float w00 = p[0][0] * v0.x, w01 = p[0][1] * v0.y, w10 = p[1][0] * v1.x, w11 = p[1][1] * v1.y;
-      if (!(fabsf(w00) <= kHalfMax && fabsf(w01) <= kHalfMax && fabsf(w10) <= kHalfMax && fabsf(w11) <= kHalfMax))
-        record_error(a.err, DEV_FP16_RANGE);
-      pa0 = pack_half2(w00, w01);
-      pa2 = pack_half2(w10, w11);
-    }
+    // O += (P v_scale) Vcode, page by page: A = weighted P (rows = heads, k = the page's 16 tokens)
 #pragma unroll
-    for (int c = 0; c < 8; c += 2) {
-      uint32_t r0, r1, r2, r3;  // (tokens 0-7, chunk c), (tokens 8-15, c), (0-7, c+1), (8-15, c+1)
-      ldsm_x4_t(vst + code_off(key, c + (mat >> 1)), r0, r1, r2, r3);
-      r0 ^= 0x80808080u;
-      r1 ^= 0x80808080u;
-      r2 ^= 0x80808080u;
-      r3 ^= 0x80808080u;
-      // even dims 16c + 2n use bytes 0 and 2 of each register, odd dims bytes 1 and 3
-      mma_f16(o[2 * c], pa0, 0u, pa2, 0u, codes_to_half2(r0, 0x5240), codes_to_half2(r1, 0x5240));
-      mma_f16(o[2 * c + 1], pa0, 0u, pa2, 0u, codes_to_half2(r0, 0x5341), codes_to_half2(r1, 0x5341));
-      mma_f16(o[2 * c + 2], pa0, 0u, pa2, 0u, codes_to_half2(r2, 0x5240), codes_to_half2(r3, 0x5240));
-      mma_f16(o[2 * c + 3], pa0, 0u, pa2, 0u, codes_to_half2(r2, 0x5341), codes_to_half2(r3, 0x5341));
+    for (int pg = 0; pg < 2; ++pg) {
+      if (pg == 1 && !two) break;
+      const uint32_t vst = sbase + (pg ? st1 : st0) * STAGE_BYTES + OFF_V;
+      const float* vss = (const float*)(smem + (pg ? st1 : st0) * STAGE_BYTES + OFF_VS);
+      uint32_t pa0, pa2;
+      {
+        const float2 v0 = *reinterpret_cast<const float2*>(vss + kb + 2 * tig);
+        const float2 v1 = *reinterpret_cast<const float2*>(vss + kb + 8 + 2 * tig);
+        const float w00 = p[2 * pg][0] * v0.x, w01 = p[2 * pg][1] * v0.y;
+        const float w10 = p[2 * pg + 1][0] * v1.x, w11 = p[2 * pg + 1][1] * v1.y;
+        if (!(fabsf(w00) <= kHalfMax && fabsf(w01) <= kHalfMax && fabsf(w10) <= kHalfMax &&
+              fabsf(w11) <= kHalfMax))
+          record_error(a.err, DEV_FP16_RANGE);
+        pa0 = pack_half2(w00, w01);
+        pa2 = pack_half2(w10, w11);
+      }
+#pragma unroll
+      for (int c = 0; c < 8; c += 2) {
+        uint32_t r0, r1, r2, r3;  // (tokens 0-7, chunk c), (tokens 8-15, c), (0-7, c+1), (8-15, c+1)
+        ldsm_x4_t(vst + code_off(key, c + (mat >> 1)), r0, r1, r2, r3);
+        r0 ^= 0x80808080u;
+        r1 ^= 0x80808080u;
+        r2 ^= 0x80808080u;
+        r3 ^= 0x80808080u;
+        // even dims 16c + 2n use bytes 0 and 2 of each register, odd dims bytes 1 and 3
+        mma_f16(o[2 * c], pa0, 0u, pa2, 0u, codes_to_half2(r0, 0x5240), codes_to_half2(r1, 0x5240));
+        mma_f16(o[2 * c + 1], pa0, 0u, pa2, 0u, codes_to_half2(r0, 0x5341), codes_to_half2(r1, 0x5341));
+        mma_f16(o[2 * c + 2], pa0, 0u, pa2, 0u, codes_to_half2(r2, 0x5240), codes_to_half2(r3, 0x5240));
+        mma_f16(o[2 * c + 3], pa0, 0u, pa2, 0u, codes_to_half2(r2, 0x5341), codes_to_half2(r3, 0x5341));
+      }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    if (lane == 0) {
+      mbar_arrive(&empty[st0]);
+      if (two) mbar_arrive(&empty[st1]);
+    }
   }
 
   // ---------------- merge the four warps' states through shared memory
