@@ -206,6 +206,59 @@ class Timer:
         return tot / steps, (sub / steps if inner else None)
 
 
+def pipelined_e2e(atc, host_in, host_out, dev, pos, cu, seq, steps, warmup):
+    """End-to-end time per step through the public API as a serving loop runs it:
+    every step uploads its Q/K/V from pinned host memory, runs RoPE + attention and
+    downloads O and LSE, on three streams with two sets of device buffers, so the
+    upload of step i+1 and the download of step i-1 overlap the compute of step i.
+    Returns ms per step (CUDA events from the first upload to the last download)."""
+    hq_, hk_, hv_ = host_in
+    ho, hl = host_out
+    q0, k0, v0, out0, lse0 = dev
+    bufs = [(q0, k0, v0, out0, lse0),
+            tuple(torch.empty_like(t) for t in (q0, k0, v0, out0, lse0))]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    cmp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n, first):
+        for i in range(n):
+            b = i % 2
+            q, k, v, out, lse = bufs[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2 or not first:
+                    s_in.wait_event(cmp_done[b])  # this buffer's previous inputs are consumed
+                q.copy_(hq_, non_blocking=True)
+                k.copy_(hk_, non_blocking=True)
+                v.copy_(hv_, non_blocking=True)
+                in_done[b].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(in_done[b])
+                if i >= 2 or not first:
+                    s_cmp.wait_event(out_done[b])  # this buffer's previous outputs are read back
+                atc.rope_apply(q, pos)
+                atc.rope_apply(k, pos)
+                atc.attn_prefill(q, k, v, out, lse, cu, pos, seq, cu_k=cu, k_pos=pos)
+                cmp_done[b].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(cmp_done[b])
+                ho.copy_(out, non_blocking=True)
+                hl.copy_(lse, non_blocking=True)
+                out_done[b].record(s_out)
+
+    run(warmup, True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    with torch.cuda.stream(s_cmp):
+        s_cmp.wait_event(e0)
+    run(steps, False)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def prefill_arm(wl, args, timer, peaks, peak_src):
     import attention_tiled_causal_gb300 as atc
     inp = wl.make("cuda")
@@ -239,7 +292,9 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
         ho.copy_(out, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
-    ms_e2e, _ = timer.run(e2e_step, args.steps, args.warmup)
+    ms_e2e_serial, _ = timer.run(e2e_step, args.steps, args.warmup)
+    ms_e2e = pipelined_e2e(atc, (hq_, hk_, hv_), (ho, hl), (q, k, v, out, lse), pos, cu, wl.seq, args.steps,
+                           args.warmup)
     # RoPE alone (S1), an HBM stream: read + write of Q and of K
     ms_rope, _ = timer.run(lambda ev=(): (atc.rope_apply(q, pos), atc.rope_apply(k, pos)), args.steps, args.warmup)
     rope_bytes = 2 * (q.numel() + k.numel()) * q.element_size()
@@ -255,7 +310,12 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
                      "kernel": "attn::tc::prefill_tc_kernel", "kernel_ms": round(ms_kernel, 4),
                      "peak_source": f"{peak_src} bf16 dense (burst)"},
         "e2e": {"value": round(flops / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4),
+                "schedule": "three streams, double-buffered: step i+1's upload and step i-1's download overlap "
+                            "step i's compute; inputs (168 MB) exceed L2",
+                "serial": {"value": round(flops / (ms_e2e_serial * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                           "ms_per_step": round(ms_e2e_serial, 4),
+                           "schedule": "upload, compute and download of each step in turn on one stream"}},
         "launches_per_step": launches,
         "rope": hbm_line("rope_apply (Q and K of the 8K prefill)", rope_bytes, ms_rope, peaks, peak_src),
         "inputs": (q, k, v, pos, cu),

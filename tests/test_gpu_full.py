@@ -152,3 +152,33 @@ def test_decode_b32_16_splits_on_sampled_requests():
                                      ctx[b:b + 1], n, w.scale)
         check(out[b:b + 1], lse[b:b + 1], wo, wl, f"decode request {b} (ctx {ctx[b]})")
         del kc, vc
+
+
+def test_decode_int8_b32_16_splits_on_sampled_requests():
+    """The INT8-cache decode at the full 32-request size (4.59 GB of codes and
+    scales), checked on six requests against the oracle's decode over the exact
+    cached values code * scale."""
+    w = synth.DECODE_INT8
+    inp = w.make(DEV)
+    q_raw = inp["q"].cpu()
+    q = inp["q"].clone()
+    atc.rope_apply(q, inp["q_pos"])
+    po, pl = atc.decode_workspace(w.batch, w.hq, w.splits, w.d, DEV)
+    out = torch.empty((w.batch, w.hq, w.d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((w.batch, w.hq), dtype=torch.float32, device=DEV)
+    atc.attn_decode_paged_int8(q, inp["k_cache"], inp["v_cache"], inp["k_scale"], inp["v_scale"], inp["page_table"],
+                               inp["ctx_lens"], w.splits, po, pl, out, lse)
+    atc.attn_device_status()
+    ctx = inp["ctx_lens"].cpu().numpy()
+    table = inp["page_table"].cpu().numpy()
+    qpos = inp["q_pos"].cpu().numpy()
+    picks = [int(np.argmax(ctx)), int(np.argmin(ctx))] + list(np.random.default_rng(6).choice(w.batch, 4, False))
+    for b in dict.fromkeys(picks):
+        n = (int(ctx[b]) + 63) // 64
+        pages = torch.from_numpy(table[b, :n].astype(np.int64)).to(DEV)
+        kc = oracle.dequant_int8(inp["k_cache"][:, pages].cpu().numpy(), inp["k_scale"][:, pages].cpu().numpy())
+        vc = oracle.dequant_int8(inp["v_cache"][:, pages].cpu().numpy(), inp["v_scale"][:, pages].cpu().numpy())
+        ident = np.arange(n, dtype=np.int32)[None, :]
+        wo, wl = oracle.decode_paged(rot(q_raw[b:b + 1], qpos[b:b + 1]), kc, vc, ident, ctx[b:b + 1], n, w.scale)
+        check(out[b:b + 1], lse[b:b + 1], wo, wl, f"INT8 decode request {b} (ctx {ctx[b]})")
+        del kc, vc
