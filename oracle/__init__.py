@@ -58,6 +58,8 @@ def _load():
         lib.oracle_dequant_int8.argtypes = [P, P, I64, I32, P]
         lib.oracle_kv_append_int8.argtypes = [P, P, P, P, I64, I32, I32, P, P, P, P, I64, D]
         lib.oracle_kv_append_int8.restype = I32
+        lib.oracle_round_e4m3.argtypes = [P, I64]
+        lib.oracle_quant_e4m3.argtypes = [P, I64, I64, P, P]
         lib.oracle_num_threads.restype = I32
         lib.oracle_set_num_threads.argtypes = [I32]
         _lib = lib
@@ -218,3 +220,29 @@ def kv_append_int8(k_new, v_new, pos, slots, k_codes, v_codes, k_scale, v_scale,
     if bad < 0:
         raise MemoryError("oracle_kv_append_int8: out of memory")
     return kc, vc, ks, vs, bad
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Nearest e4m3 values (ties to even, saturating at +-448)."""
+    out = np.array(x, dtype=np.float64, copy=True)
+    _load().oracle_round_e4m3(_p(out), out.size)
+    return out
+
+
+def quant_e4m3(x, group_axes):
+    """Quantise x to e4m3 with one fp32 scale per group: a group is one index of
+    the leading `group_axes` axes of x (after moving them to the front, in
+    order); scale = max|x| / 448, value = e4m3(x / scale) decided in fp32.
+    Returns (values with x's shape, scales with the group axes' shape)."""
+    x = _f64(x)
+    axes = list(group_axes)
+    rest = [a for a in range(x.ndim) if a not in axes]
+    xt = np.ascontiguousarray(np.transpose(x, axes + rest))
+    gshape = xt.shape[:len(axes)]
+    groups = int(np.prod(gshape))
+    n = int(np.prod(xt.shape[len(axes):]))
+    codes = np.empty(xt.shape, dtype=np.float64)
+    scales = np.empty(gshape, dtype=np.float32)
+    _load().oracle_quant_e4m3(_p(xt), groups, n, _p(codes), _p(scales))
+    inv = np.argsort(axes + rest)
+    return np.transpose(codes, inv), scales

@@ -312,6 +312,51 @@ int oracle_kv_append_int8(const double *k_new, const double *v_new, const int32_
     return bad;
 }
 
+/* ---------------------------------------------------------------- FP8 (e4m3) */
+
+/* The nearest e4m3 value (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * no infinities, largest finite 448, subnormal spacing 2^-9), ties to even;
+ * finite values beyond 448 saturate to +-448.  The FP8 path of the Flash
+ * Attention page, section 18.5 (an FP8 mode with block quantisation). */
+static double round_e4m3(double x)
+{
+    if (x != x || x == 0.0) return x;
+    double a = fabs(x);
+    int e;
+    (void)frexp(a, &e);          /* a = m * 2^e, 0.5 <= m < 1: binade [2^(e-1), 2^e) */
+    int q = (e - 1) - 3;         /* 3 mantissa bits */
+    if (q < -9) q = -9;          /* subnormal spacing */
+    double r = rint(a / ldexp(1.0, q)) * ldexp(1.0, q);
+    if (r > 448.0) r = 448.0;
+    return copysign(r, x);
+}
+
+void oracle_round_e4m3(double *x, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) x[i] = round_e4m3(x[i]);
+}
+
+/* Quantise groups of values to e4m3 with one fp32 scale per group: scale =
+ * max|x| / 448, value = e4m3(x / scale) with x / scale in fp32 (as the path
+ * decides it); an all-zero group gets scale 0 and values 0.  codes receives
+ * the e4m3 VALUES (not their bit patterns).
+ *   x [groups][n] (exact in fp32) -> codes [groups][n], scales [groups] */
+void oracle_quant_e4m3(const double *x, int64_t groups, int64_t n, double *codes, float *scales)
+{
+    for (int64_t g = 0; g < groups; ++g) {
+        const double *xg = x + g * n;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < n; ++i) {
+            float a = fabsf((float)xg[i]);
+            if (a > amax) amax = a;
+        }
+        float s = amax / 448.0f;
+        scales[g] = s;
+        for (int64_t i = 0; i < n; ++i)
+            codes[g * n + i] = s == 0.0f ? 0.0 : round_e4m3((double)((float)xg[i] / s));
+    }
+}
+
 /* Decode: q [B][hq][d] (already rotated, at position ctx_b - 1) against the
  * ctx_b cached tokens of request b.  out [B][hq][d], lse [B][hq]. */
 int oracle_decode_paged(const double *q, const double *k_cache, const double *v_cache,

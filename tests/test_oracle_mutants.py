@@ -28,6 +28,8 @@ MUTANTS = [
     ("int8 scale of the wrong token", "(double)scales[r];", "(double)scales[r > 0 ? r - 1 : r];", False),
     ("int8 scale over 128", "float s = amax / 127.0f;", "float s = amax / 128.0f;", False),
     ("int8 rounding toward zero", "float q = rintf((float)x[i] / s);", "float q = truncf((float)x[i] / s);", False),
+    ("e4m3 four mantissa bits", "int q = (e - 1) - 3;", "int q = (e - 1) - 4;", False),
+    ("e4m3 no saturation", "if (r > 448.0) r = 448.0;", "if (r > 480.0) r = 480.0;", False),
     ("append rotates values", "const double *vs = v_new + (t * heads + h) * (int64_t)d;",
      "const double *vs = krow - (int64_t)0 * (t * heads + h);", False),
 ]

@@ -585,3 +585,49 @@ def test_int8_append_keys_are_quantised_bf16_rotations():
                                               np.zeros((H, 2, 4), np.float32))
     kd = oracle.dequant_int8(kc, ks)
     assert np.all(np.abs(kd - kb) <= ks[..., None].astype(np.float64) / 2 + np.abs(kb) * 2.0 ** -22)
+
+
+# ------------------------------------------------------------ FP8 (e4m3)
+
+def test_round_e4m3_matches_torch_conversion():
+    """Every e4m3 value and every midpoint between neighbours (ties to even),
+    against torch's float8_e4m3fn conversion."""
+    codes = torch.arange(0, 256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float()
+    vals = codes[torch.isfinite(codes)].double().unique().numpy()
+    mids = (vals[:-1] + vals[1:]) / 2
+    rng = np.random.default_rng(101)
+    rand = rng.uniform(-448, 448, 2000) * rng.choice([1, 1e-1, 1e-2, 1e-3], 2000)
+    x = np.concatenate([vals, mids, -mids, rand]).astype(np.float32).astype(np.float64)
+    want = torch.from_numpy(x).float().to(torch.float8_e4m3fn).float().double().numpy()
+    np.testing.assert_array_equal(oracle.round_e4m3(x), want)
+
+
+def test_round_e4m3_saturates_and_keeps_signed_zero():
+    got = oracle.round_e4m3(np.array([448.0, 449.0, 479.0, 1e6, -1e6, 0.0, -0.0, 2.0 ** -10, 2.0 ** -9]))
+    np.testing.assert_array_equal(got[:5], [448.0, 448.0, 448.0, 448.0, -448.0])
+    assert got[5] == 0.0 and np.signbit(got[6])
+    assert got[7] == 0.0 and got[8] == 2.0 ** -9   # 2^-10 is a tie between 0 and 2^-9: even is 0
+
+
+def test_quant_e4m3_groups_and_scale():
+    """One scale per group (max|x| / 448 in fp32): the largest |x| of a group maps
+    to +-448, every value is within half an e4m3 step (relative 2^-4) of x / scale,
+    and a zero group has scale 0."""
+    rng = np.random.default_rng(102)
+    x = rng.normal(0, 1, (3, 5, 32)).astype(np.float32).astype(np.float64)
+    x[2, 4] = 0.0
+    codes, scales = oracle.quant_e4m3(x, [0, 1])
+    assert scales.shape == (3, 5) and scales[2, 4] == 0 and (codes[2, 4] == 0).all()
+    for i in range(3):
+        for j in range(5):
+            if scales[i, j] == 0:
+                continue
+            s = np.float32(np.abs(x[i, j]).max().astype(np.float32) / np.float32(448.0))
+            assert scales[i, j] == s
+            assert np.abs(codes[i, j]).max() == 448.0
+            ref = (x[i, j].astype(np.float32) / s).astype(np.float64)
+            assert np.all(np.abs(codes[i, j] - ref) <= np.maximum(np.abs(ref) * 2.0 ** -4, 2.0 ** -10))
+    # group axes in another order: per column group
+    c2, s2 = oracle.quant_e4m3(x, [2])
+    assert s2.shape == (32,)
+    np.testing.assert_array_equal(s2, (np.abs(x).max(axis=(0, 1)).astype(np.float32) / np.float32(448.0)))
