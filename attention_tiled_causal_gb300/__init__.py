@@ -21,8 +21,8 @@ Entry points (same names as the C ABI):
 from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_decode_paged_int8,
                        attn_device_status,
                        attn_kv_append_paged, attn_kv_append_paged_int8, attn_lse_merge, attn_prefill, decode_workspace, lib_path, library,
-                       prefill, rope_apply, rope_table)
+                       prefill, quant_fp8_heads, quant_fp8_rows, rope_apply, rope_table)
 
 __all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_decode_paged_int8", "attn_device_status",
            "attn_kv_append_paged", "attn_kv_append_paged_int8", "attn_lse_merge", "attn_prefill", "decode_workspace", "lib_path", "library",
-           "prefill", "rope_apply", "rope_table"]
+           "prefill", "quant_fp8_heads", "quant_fp8_rows", "rope_apply", "rope_table"]

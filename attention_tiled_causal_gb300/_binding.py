@@ -47,6 +47,10 @@ def library():
     lib.attn_prefill_rope_q.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, I64, I32, P, P, I64, P, P, I32, I32,
                                         I64, I32, I32, I32, I32, I32, F32, I32, P, P]
     lib.attn_prefill_rope_q.restype = I32
+    lib.quant_fp8_rows.argtypes = [P, I64, I32, I32, P, P, P]
+    lib.quant_fp8_rows.restype = I32
+    lib.quant_fp8_heads.argtypes = [P, I64, I32, I32, P, P, P, I32, I64, P]
+    lib.quant_fp8_heads.restype = I32
     lib.attn_kv_append_paged_int8.argtypes = [P, P, P, P, I64, I32, I32, P, P, P, P, I64, I32, P, F64, P]
     lib.attn_kv_append_paged_int8.restype = I32
     lib.attn_kv_append_paged.argtypes = [P, P, P, P, I64, I32, I32, P, P, I64, I32, P, F64, P]
@@ -197,6 +201,36 @@ def attn_kv_append_paged_int8(k_new, v_new, positions, slots, k_cache, v_cache, 
         _ptr(k_new), _ptr(v_new), pos_ptr, _ptr(slots), T, hkv, d, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
         _ptr(v_scale), k_cache.shape[1], k_cache.shape[2], _ptr(k_rot_out) if k_rot_out is not None else None,
         float(base), _stream(stream)))
+
+
+def quant_fp8_rows(x, stream=None):
+    """e4m3 codes of x [tokens, heads, 128] bf16 with one scale per (token, head) row:
+    returns (codes as torch.float8_e4m3fn [tokens, heads, 128], scales [tokens, heads])."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 3:
+        raise ValueError("x must be a contiguous bf16 [tokens, heads, head_dim] tensor")
+    T, H, d = x.shape
+    codes = torch.empty((T, H, d), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _check(library().quant_fp8_rows(_ptr(x), T, H, d, _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes.view(torch.float8_e4m3fn), scales
+
+
+def quant_fp8_heads(x, transposed: bool = False, stream=None):
+    """e4m3 codes of x [tokens, heads, 128] bf16 with one scale per head: returns (codes,
+    scales [heads]); codes are [tokens, heads, 128], or [heads, 128, t_stride] with
+    t_stride = tokens rounded up to 16 when transposed (the layout the FP8 prefill
+    reads its values in)."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 3:
+        raise ValueError("x must be a contiguous bf16 [tokens, heads, head_dim] tensor")
+    T, H, d = x.shape
+    t_stride = (T + 15) // 16 * 16
+    shape = (H, d, t_stride) if transposed else (T, H, d)
+    codes = torch.zeros(shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty((H,), dtype=torch.float32, device=x.device)
+    scratch = torch.empty((H,), dtype=torch.int32, device=x.device)
+    _check(library().quant_fp8_heads(_ptr(x), T, H, d, _ptr(codes), _ptr(scales), _ptr(scratch),
+                                     1 if transposed else 0, t_stride, _stream(stream)))
+    return codes.view(torch.float8_e4m3fn), scales
 
 
 def attn_prefill(q, k, v, out, lse, cu_q, q_pos, max_seqlen_q: int, *, cu_k=None, k_pos=None,

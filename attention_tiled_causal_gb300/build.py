@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattn_gb300.so")
 SOURCES = ["api.cu", "rope.cu", "merge.cu", "prefill_simt.cu", "prefill_tc.cu", "decode.cu", "decode_noalloc.cu",
-           "decode_int8.cu"]
+           "decode_int8.cu", "quant_fp8.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

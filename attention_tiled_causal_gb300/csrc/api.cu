@@ -222,6 +222,31 @@ int attn_kv_append_paged_int8(const void* k_new, const void* v_new, const int32_
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_kv_append_paged_int8 launch");
 }
 
+int quant_fp8_rows(const void* x, int64_t tokens, int heads, int head_dim, void* codes, float* scales,
+                   void* stream) {
+  if (tokens < 0 || heads < 0) return fail(ATTN_ERR_ARG, "quant_fp8_rows: negative size");
+  if (head_dim != 128) return fail(ATTN_ERR_SHAPE, "quant_fp8_rows: head_dim %d (need 128)", head_dim);
+  if (tokens == 0 || heads == 0) return ATTN_OK;
+  if (!x || !codes || !scales) return fail(ATTN_ERR_ARG, "quant_fp8_rows: null pointer");
+  if (!aligned16(x) || !aligned16(codes)) return fail(ATTN_ERR_ALIGN, "quant_fp8_rows: x / codes not 16-byte aligned");
+  cudaError_t e = attn::launch_quant_fp8_rows(x, tokens * heads, codes, scales, (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "quant_fp8_rows launch");
+}
+
+int quant_fp8_heads(const void* x, int64_t tokens, int heads, int head_dim, void* codes, float* scales,
+                    unsigned* amax_scratch, int transposed, int64_t t_stride, void* stream) {
+  if (tokens < 0 || heads < 0) return fail(ATTN_ERR_ARG, "quant_fp8_heads: negative size");
+  if (head_dim != 128) return fail(ATTN_ERR_SHAPE, "quant_fp8_heads: head_dim %d (need 128)", head_dim);
+  if (transposed && (t_stride < tokens || t_stride % 16))
+    return fail(ATTN_ERR_ARG, "quant_fp8_heads: t_stride must be >= tokens and a multiple of 16");
+  if (tokens == 0 || heads == 0) return ATTN_OK;
+  if (!x || !codes || !scales || !amax_scratch) return fail(ATTN_ERR_ARG, "quant_fp8_heads: null pointer");
+  if (!aligned16(x) || !aligned16(codes)) return fail(ATTN_ERR_ALIGN, "quant_fp8_heads: x / codes not 16-byte aligned");
+  cudaError_t e = attn::launch_quant_fp8_heads(x, tokens, heads, codes, scales, amax_scratch, transposed != 0,
+                                               t_stride, (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "quant_fp8_heads launch");
+}
+
 }  // extern "C"
 
 namespace {

@@ -39,6 +39,9 @@ struct AppendLaunch {
 };
 cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s);
 cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s);
+cudaError_t launch_quant_fp8_rows(const void* x, int64_t rows, void* codes, float* scales, cudaStream_t s);
+cudaError_t launch_quant_fp8_heads(const void* x, int64_t tokens, int heads, void* codes, float* scales,
+                                   unsigned* amax_scratch, bool transposed, int64_t t_stride, cudaStream_t s);
 
 struct MergeLaunch {
   const float* part_out;

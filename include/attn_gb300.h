@@ -143,6 +143,29 @@ ATTN_API int attn_kv_append_paged_int8(const void *k_new, const void *v_new, con
                                        void *stream);
 
 /*
+ * quant_fp8_rows / quant_fp8_heads -- e4m3 codes for the FP8 prefill ("Flash
+ * Attention and distributed parallelism", section 18.5: an FP8 mode with block
+ * quantisation).  A group of values shares one fp32 scale = max|x| / 448; each
+ * value is stored as e4m3(x / scale), rounded to nearest even with x / scale
+ * in fp32 (saturating at +-448); an all-zero group has scale 0 and codes 0.
+ * The value a code stands for is code * scale.
+ *
+ *  quant_fp8_rows:  x [tokens][heads][128] bf16 -> codes [tokens][heads][128]
+ *                   e4m3, scales [tokens][heads] fp32; one group per row (the
+ *                   queries).
+ *  quant_fp8_heads: one group per head over all tokens (keys, values) ->
+ *                   scales [heads]; codes [tokens][heads][128] (transposed = 0)
+ *                   or [heads][128][t_stride] (transposed = 1, t_stride >= tokens
+ *                   and a multiple of 16: the values, whose P V contraction reads
+ *                   V^T rows).  amax_scratch: caller-owned [heads] unsigned.
+ * x and codes 16-byte aligned; head_dim must be 128.
+ */
+ATTN_API int quant_fp8_rows(const void *x, int64_t tokens, int heads, int head_dim, void *codes, float *scales,
+                            void *stream);
+ATTN_API int quant_fp8_heads(const void *x, int64_t tokens, int heads, int head_dim, void *codes, float *scales,
+                             unsigned *amax_scratch, int transposed, int64_t t_stride, void *stream);
+
+/*
  * attn_prefill -- exact causal GQA attention, FlashAttention-style tiled.
  *
  * Computes, for every query row of every sequence and every query head h in

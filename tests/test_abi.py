@@ -43,7 +43,7 @@ def test_only_the_c_abi_is_exported(lib):
     import subprocess
     out = subprocess.run(["nm", "-D", "--defined-only", atc.lib_path()], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
-    ours = {s for s in exported if s.startswith(("attn_", "rope_"))}
+    ours = {s for s in exported if s.startswith(("attn_", "rope_", "quant_"))}
     assert ours == set(declared_functions())
 
 

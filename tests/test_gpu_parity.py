@@ -829,3 +829,29 @@ def test_decode_over_int8_append_matches_oracle():
     want_o, want_l = oracle.decode_paged(rotated_bf16(q, qpos), oracle.dequant_int8(wkc, wks),
                                          oracle.dequant_int8(wvc, wvs), table, ctx, num_pages, d ** -0.5)
     check(out, lse, want_o, want_l, what="decode over the INT8 append")
+
+
+# ------------------------------------------------------------------ FP8 quantisation
+
+def test_quant_fp8_rows_and_heads_match_oracle():
+    """e4m3 codes and fp32 scales exactly as the oracle decides them in fp32, for
+    one group per (token, head) row, per head, and per head with the transposed
+    [heads][128][t_stride] layout of the values."""
+    T, H = 333, 8
+    x = synth.randn((T, H, 128), 700, 0.7071)
+    x[5, 3] = 0                                  # an all-zero row
+    xd = x.to(DEV)
+    c_r, s_r = atc.quant_fp8_rows(xd)
+    c_h, s_h = atc.quant_fp8_heads(xd)
+    c_t, s_t = atc.quant_fp8_heads(xd, transposed=True)
+    atc.attn_device_status()
+    xf = synth.as_f64(x)
+    want_r, ws_r = oracle.quant_e4m3(xf, [0, 1])
+    want_h, ws_h = oracle.quant_e4m3(xf, [1])
+    np.testing.assert_array_equal(c_r.float().cpu().numpy(), want_r)
+    np.testing.assert_array_equal(s_r.cpu().numpy(), ws_r)
+    np.testing.assert_array_equal(c_h.float().cpu().numpy(), want_h)
+    np.testing.assert_array_equal(s_h.cpu().numpy(), ws_h)
+    np.testing.assert_array_equal(s_t.cpu().numpy(), ws_h)
+    assert c_t.shape == (H, 128, 336)
+    np.testing.assert_array_equal(c_t.float().cpu().numpy()[:, :, :T], np.transpose(want_h, (1, 2, 0)))
