@@ -47,6 +47,9 @@ def library():
     lib.attn_prefill_rope_q.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, I64, I32, P, P, I64, P, P, I32, I32,
                                         I64, I32, I32, I32, I32, I32, F32, I32, P, P]
     lib.attn_prefill_rope_q.restype = I32
+    lib.attn_prefill_fp8.argtypes = [P, P, P, P, P, P, I64, P, I32, P, I32, P, P, I64, I32, P, P, I64, I32, I32,
+                                     I32, I32, I32, F32, I32, P]
+    lib.attn_prefill_fp8.restype = I32
     lib.quant_fp8_rows.argtypes = [P, I64, I32, I32, P, P, P]
     lib.quant_fp8_rows.restype = I32
     lib.quant_fp8_heads.argtypes = [P, I64, I32, I32, P, P, P, I32, I64, P]
@@ -225,7 +228,7 @@ def quant_fp8_heads(x, transposed: bool = False, stream=None):
     T, H, d = x.shape
     t_stride = (T + 15) // 16 * 16
     shape = (H, d, t_stride) if transposed else (T, H, d)
-    codes = torch.zeros(shape, dtype=torch.uint8, device=x.device)
+    codes = torch.empty(shape, dtype=torch.uint8, device=x.device)
     scales = torch.empty((H,), dtype=torch.float32, device=x.device)
     scratch = torch.empty((H,), dtype=torch.int32, device=x.device)
     _check(library().quant_fp8_heads(_ptr(x), T, H, d, _ptr(codes), _ptr(scales), _ptr(scratch),
@@ -278,6 +281,41 @@ def attn_prefill(q, k, v, out, lse, cu_q, q_pos, max_seqlen_q: int, *, cu_k=None
                 or not q_rope_cs.is_contiguous():
             raise ValueError("q_rope_cs must be a contiguous float32 [Tq, d/2, 2] table (rope_table)")
         _check(library().attn_prefill_rope_q(*args, _ptr(q_rope_cs), _stream(stream)))
+
+
+def attn_prefill_fp8(q, q_scale, k, k_scale, v_t, v_scale, out, lse, cu_q, q_pos, max_seqlen_q: int, cu_k, k_pos,
+                     *, h_lo: int = 0, h_hi: Optional[int] = None, scale: Optional[float] = None,
+                     causal: bool = True, stream=None) -> None:
+    """Tiled causal GQA attention on e4m3 codes (quant_fp8_rows for q, quant_fp8_heads for
+    k and, transposed, v).  q [Tq, Hq, 128] with q_scale [Tq, Hq]; k [Tk, Hkv, 128] with
+    k_scale [Hkv]; v_t [Hkv, 128, t_stride] with v_scale [Hkv].  Every key sequence must
+    start at a multiple of 16 tokens.  Writes out [Tq, Hq, 128] (bf16 or fp32) and lse."""
+    for t, n in ((q, "q"), (k, "k"), (v_t, "v_t"), (out, "out"), (q_scale, "q_scale"), (k_scale, "k_scale"),
+                 (v_scale, "v_scale")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for t, n in ((q, "q"), (k, "k"), (v_t, "v_t")):
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise ValueError(f"{n} must hold e4m3 codes (float8_e4m3fn or uint8)")
+    for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t.dtype != torch.float32:
+            raise ValueError(f"{n} must be float32")
+    Tq, hq, d = q.shape
+    Tk, hkv, dk = k.shape
+    if dk != d or out.shape != q.shape or tuple(v_t.shape[:2]) != (hkv, d) or v_t.dim() != 3:
+        raise ValueError("inconsistent q/k/v_t/out shapes")
+    if tuple(q_scale.shape) != (Tq, hq) or tuple(k_scale.shape) != (hkv,) or tuple(v_scale.shape) != (hkv,):
+        raise ValueError("q_scale must be [Tq, Hq]; k_scale and v_scale [Hkv]")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (Tq, hq) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 [Tq, Hq] tensor")
+    h_hi = hq if h_hi is None else h_hi
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    cu_q = _i32(cu_q, "cu_q")
+    _check(library().attn_prefill_fp8(
+        _ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(v_t), _ptr(v_scale), v_t.shape[2], _ptr(out),
+        _dt(out), _ptr(lse), cu_q.numel() - 1, _ptr(cu_q), _ptr(_i32(q_pos, "q_pos")), Tq, int(max_seqlen_q),
+        _ptr(_i32(cu_k, "cu_k")), _ptr(_i32(k_pos, "k_pos")), Tk, hq, hkv, d, int(h_lo), int(h_hi), float(scale),
+        1 if causal else 0, _stream(stream)))
 
 
 def prefill(q, k, v, cu_q, q_pos, max_seqlen_q: int, out_dtype=None, with_lse: bool = True, **kw):

@@ -110,6 +110,22 @@ int map_pages(CUtensorMap* m, const void* base, int hkv, int64_t num_pages) {
   return encode_bf16(m, base, 2, dims, strides, box);
 }
 
+// e4m3 codes [tokens][heads][128] as rows of 128 bytes, box (128 bytes, 1 head, 128 tokens).
+int map_tokens_i8(CUtensorMap* m, const void* base, int64_t tokens, int heads) {
+  cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)(tokens > 0 ? tokens : 1)};
+  cuuint64_t strides[2] = {128, (cuuint64_t)heads * 128};
+  cuuint32_t box[3] = {128, 1, 128};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, dims, strides, box);
+}
+
+// transposed e4m3 codes [heads][128][t_stride], box (128 keys, 128 dims, 1 head).
+int map_vt_i8(CUtensorMap* m, const void* base, int64_t t_stride, int heads) {
+  cuuint64_t dims[3] = {(cuuint64_t)t_stride, 128, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)t_stride, (cuuint64_t)t_stride * 128};
+  cuuint32_t box[3] = {128, 128, 1};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, dims, strides, box);
+}
+
 // head-major paged INT8 cache [hkv][num_pages][64][128] as rows of 128 bytes, box (128 bytes, 64 rows).
 int map_pages_i8(CUtensorMap* m, const void* base, int hkv, int64_t num_pages) {
   cuuint64_t dims[2] = {128, (cuuint64_t)hkv * (cuuint64_t)num_pages * 64};
@@ -151,8 +167,15 @@ int attn_device_status(int clear) {
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   }
-  if (v) return fail(ATTN_ERR_DEVICE, "device error 0x%x (%s)", v,
-                     v == 0x201 ? "page id outside the cache" : "pipeline wait timed out");
+  if (v) {
+    // the device codes of common.cuh: 0x10x wait timeouts, 0x20x bad inputs
+    const char* what = v == 0x201   ? "page id outside the cache"
+                       : v == 0x202 ? "cache slot outside the cache"
+                       : v == 0x203 ? "INT8 decode value beyond the fp16 range"
+                       : v == 0x204 ? "FP8 prefill key sequence not starting at a multiple of 16"
+                                    : "pipeline wait timed out";
+    return fail(ATTN_ERR_DEVICE, "device error 0x%x (%s)", v, what);
+  }
   return ATTN_OK;
 }
 
@@ -245,6 +268,52 @@ int quant_fp8_heads(const void* x, int64_t tokens, int heads, int head_dim, void
   cudaError_t e = attn::launch_quant_fp8_heads(x, tokens, heads, codes, scales, amax_scratch, transposed != 0,
                                                t_stride, (cudaStream_t)stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "quant_fp8_heads launch");
+}
+
+int attn_prefill_fp8(const void* q, const float* q_scale, const void* k, const float* k_scale, const void* v_t,
+                     const float* v_scale, int64_t v_t_stride, void* out, attn_dtype_t out_dtype, float* lse,
+                     int batch, const int32_t* cu_q, const int32_t* q_pos, int64_t total_q, int max_seqlen_q,
+                     const int32_t* cu_k, const int32_t* k_pos, int64_t total_k, int num_q_heads, int num_kv_heads,
+                     int head_dim, int h_lo, int h_hi, float scale, int causal, void* stream) {
+  if (batch < 0 || max_seqlen_q < 0 || total_q < 0 || total_k < 0)
+    return fail(ATTN_ERR_ARG, "attn_prefill_fp8: negative size");
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
+    return fail(ATTN_ERR_SHAPE, "attn_prefill_fp8: num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads,
+                num_kv_heads);
+  const int G = num_q_heads / num_kv_heads;
+  if (h_lo < 0 || h_hi > num_q_heads || h_lo > h_hi || h_lo % G || h_hi % G)
+    return fail(ATTN_ERR_SHAPE, "attn_prefill_fp8: head range [%d, %d) must be whole GQA groups of %d", h_lo, h_hi,
+                G);
+  if (head_dim != 128) return fail(ATTN_ERR_SHAPE, "attn_prefill_fp8: head_dim %d (need 128)", head_dim);
+  if (out_dtype != ATTN_BF16 && out_dtype != ATTN_FP32) return fail(ATTN_ERR_UNSUPPORTED, "attn_prefill_fp8: out_dtype");
+  if (!(scale > 0.f)) return fail(ATTN_ERR_ARG, "attn_prefill_fp8: scale must be positive");
+  if (v_t_stride < total_k || v_t_stride % 16)
+    return fail(ATTN_ERR_ARG, "attn_prefill_fp8: v_t_stride must be >= total_k and a multiple of 16");
+  if (batch == 0 || max_seqlen_q == 0 || h_lo == h_hi || total_q == 0) return ATTN_OK;
+  if (!q || !q_scale || !k || !k_scale || !v_t || !v_scale || !out || !cu_q || !q_pos || !cu_k || !k_pos)
+    return fail(ATTN_ERR_ARG, "attn_prefill_fp8: null pointer");
+  if (total_q > 0x7fffffff || total_k > 0x7fffffff) return fail(ATTN_ERR_ARG, "attn_prefill_fp8: more than 2^31-1 tokens");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v_t) || !aligned16(out))
+    return fail(ATTN_ERR_ALIGN, "attn_prefill_fp8: q/k/v_t/out must be 16-byte aligned");
+  attn::PrefillLaunch a;
+  a.q = q; a.k = k; a.v = v_t; a.out = out;
+  a.out_f32 = out_dtype == ATTN_FP32;
+  a.lse = lse;
+  a.in_f32 = 0;
+  a.batch = batch; a.cu_q = cu_q; a.q_pos = q_pos; a.max_seqlen_q = max_seqlen_q;
+  a.cu_k = cu_k; a.k_pos = k_pos; a.page_table = nullptr; a.k_lens = nullptr;
+  a.max_pages = 0; a.page_size = 0; a.num_pages = 0;
+  a.hq = num_q_heads; a.hkv = num_kv_heads; a.d = head_dim; a.h_lo = h_lo; a.h_hi = h_hi;
+  a.scale = scale; a.causal = causal ? 1 : 0;
+  a.fp8 = 1; a.q_scale = q_scale; a.k_scale = k_scale; a.v_scale = v_scale;
+  int rc = device_error_ptr(&a.err);
+  if (rc) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = map_tokens_i8(&tq, q, total_q, num_q_heads))) return rc;
+  if ((rc = map_tokens_i8(&tk, k, total_k, num_kv_heads))) return rc;
+  if ((rc = map_vt_i8(&tv, v_t, v_t_stride, num_kv_heads))) return rc;
+  cudaError_t e = attn::launch_prefill_tc(a, tq, tk, tv, (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_prefill_fp8 launch");
 }
 
 }  // extern "C"

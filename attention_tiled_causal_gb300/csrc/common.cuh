@@ -23,6 +23,7 @@ enum DeviceError : unsigned {
   DEV_BAD_PAGE = 0x201,         // page-table entry outside [0, num_pages)
   DEV_BAD_SLOT = 0x202,         // cache slot outside [-1, num_pages * page_size)
   DEV_FP16_RANGE = 0x203,       // a value the INT8 decode feeds the fp16 MMAs exceeds 65504
+  DEV_FP8_ALIGN = 0x204,        // FP8 prefill: a key sequence does not start at a multiple of 16 tokens
 };
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
@@ -189,6 +190,18 @@ __device__ __forceinline__ void tc_mma_bf16_warp(uint32_t d_tmem, uint64_t a_des
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// The same for 8-bit operands: kind::f8f6f4, K = 32 per instruction (the
+// instruction descriptor names the two element formats; both must be K-major).
+__device__ __forceinline__ void tc_mma_fp8_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
 // tcgen05.commit from the elected lane of a converged warp (the lane that
 // issued the MMAs, so it tracks all of them).
 __device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
@@ -351,6 +364,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void rope_rotate(float x1, float x2, float cs, float sn, float& y1, float& y2) {
   y1 = __fmaf_rn(x1, cs, -__fmul_rn(x2, sn));
   y2 = __fmaf_rn(x2, cs, __fmul_rn(x1, sn));
+}
+
+// Two fp32 values -> two e4m3 bytes, lo in the low byte (round to nearest
+// even, saturating at +-448).
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

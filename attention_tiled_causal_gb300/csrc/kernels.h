@@ -74,6 +74,10 @@ struct PrefillLaunch {
   int causal;
   unsigned* err;
   const float* q_rope_cs = nullptr;  // tcgen05 kernel only: [total_q][d/2][2] cos, sin; rotate Q on the fly
+  // tcgen05 kernel only: q, k are e4m3 codes [T][H][128], v the transposed codes
+  // [hkv][128][t_stride]; values are code * scale
+  int fp8 = 0;
+  const float *q_scale = nullptr, *k_scale = nullptr, *v_scale = nullptr;
 };
 // CUDA-core kernel: any supported dtype / head_dim / page size.
 cudaError_t launch_prefill_simt(const PrefillLaunch& a, cudaStream_t s);

@@ -35,6 +35,7 @@
 // Every mbarrier wait is bounded; on expiry the kernel records an error code,
 // unwinds, frees its TMEM and returns (no trap).
 #include <math.h>
+#include <float.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -52,14 +53,24 @@ namespace tc {
 
 constexpr int BM = 128, BN = 128, D = 128;
 constexpr int NSLOT = 3;
-constexpr int TILE = BM * D * 2;  // 32 KB: one Q, K, V or P tile
-constexpr int HALF = TILE / 2;    // 16 KB: 128 rows x 64 elements (one swizzled box)
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + 2 * TILE;
-constexpr int OFF_P = OFF_KV + NSLOT * TILE;
-constexpr int OFF_BAR = OFF_P + 2 * TILE;
 constexpr int NBAR = 18;
-constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 32 + 1024;
+constexpr int HALF = 16384;  // one 128-byte-swizzled TMA box: 128 rows x 128 bytes
+
+// Tile geometry of the two element types.  bf16: a 128 x 128 tile is two
+// boxes of 64 elements (32 KB); an MMA k-step is 16 elements.  e4m3: one box of
+// 128 elements (16 KB); a k-step is 32 elements.  Both step through a
+// 128-byte swizzle row 32 bytes at a time.
+template <bool FP8>
+struct Cfg {
+  static constexpr int TILE = FP8 ? 16384 : 32768;
+  static constexpr int NBOX = FP8 ? 1 : 2;
+  static constexpr int KSTEPS = FP8 ? 4 : 8;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + 2 * TILE;
+  static constexpr int OFF_P = OFF_KV + NSLOT * TILE;
+  static constexpr int OFF_BAR = OFF_P + 2 * TILE;
+  static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 32 + 1024;
+};
 // 12 warps = 3 warpgroups.  The register file is split across the SM's four
 // sub-partitions, so 3 warps per sub-partition launch with at most 168
 // registers each; every role fits in that without spilling.
@@ -69,6 +80,9 @@ constexpr int REGS_LAUNCH = 168;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);    // P K-major, V MN-major
+// e4m3 x e4m3 -> fp32 (kind::f8f6f4: A and B format 0), both operands K-major:
+// P V reads V^T rows (values stored transposed), since 8-bit MMA operands are K-major.
+constexpr uint32_t IDESC_FP8 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 constexpr float kRescaleLog2 = 8.f;
 
 struct Smem {
@@ -95,6 +109,10 @@ struct Params {
   float scale;
   int wave;  // CTAs resident at once (one per SM): the CTA `wave` launches later likely follows this one
   const float4* q_cs;  // NULL, or [total_q][32] float4: (cos, sin) of the 64 RoPE angles of each query row
+  // e4m3 inputs: the value of a code is code * scale
+  const float* q_scale;  // [total_q][hq]: one scale per query row
+  const float* k_scale;  // [hkv]
+  const float* v_scale;  // [hkv]
 };
 
 // Number of keys with position <= qp among k_pos[0..n), positions
@@ -137,32 +155,45 @@ __device__ int count_le_warp(const int32_t* k_pos, int n, int qp, int lane) {
 __device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int ring_pos_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 
-// S_t = Q_t K_j^T: eight k-steps of 16 over head_dim, both operands K-major.
+// S_t = Q_t K_j^T over head_dim, both operands K-major: bf16 eight k-steps of
+// 16 (two boxes), e4m3 four k-steps of 32 (one box).
+template <bool FP8>
 __device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint64_t a0, uint64_t b0) {
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
+  for (int kk = 0; kk < Cfg<FP8>::KSTEPS; ++kk) {
     const uint64_t o = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
-    tc_mma_bf16_warp(d_tmem, a0 + o, b0 + o, IDESC_QK, kk > 0 ? 1u : 0u);
+    if constexpr (FP8)
+      tc_mma_fp8_warp(d_tmem, a0 + o, b0 + o, IDESC_FP8, kk > 0 ? 1u : 0u);
+    else
+      tc_mma_bf16_warp(d_tmem, a0 + o, b0 + o, IDESC_QK, kk > 0 ? 1u : 0u);
   }
 }
 
-// O_t (+)= P_t V_j: eight k-steps of 16 tokens; P K-major, V MN-major (16
-// tokens = two 8-row swizzle atoms = 2048 bytes).
+// O_t (+)= P_t V_j.  bf16: eight k-steps of 16 tokens; P K-major, V MN-major
+// (16 tokens = two 8-row swizzle atoms = 2048 bytes).  e4m3: four k-steps of
+// 32 tokens; P and V^T both K-major.
+template <bool FP8>
 __device__ __forceinline__ void mma_values(uint32_t d_tmem, uint64_t a0, uint64_t b0, bool accumulate) {
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk) {
+  for (int kk = 0; kk < Cfg<FP8>::KSTEPS; ++kk) {
     const uint64_t o = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
-    tc_mma_bf16_warp(d_tmem, a0 + o, b0 + (uint64_t)(kk * (2048 >> 4)), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+    if constexpr (FP8)
+      tc_mma_fp8_warp(d_tmem, a0 + o, b0 + o, IDESC_FP8, (accumulate || kk > 0) ? 1u : 0u);
+    else
+      tc_mma_bf16_warp(d_tmem, a0 + o, b0 + (uint64_t)(kk * (2048 >> 4)), IDESC_PV,
+                       (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
-template <bool PAGED>
+template <bool PAGED, bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  using C = Cfg<FP8>;
+  constexpr int TILE = C::TILE, OFF_Q = C::OFF_Q, OFF_KV = C::OFF_KV, OFF_P = C::OFF_P, OFF_BAR = C::OFF_BAR;
 
   // Work item: query head h, pair of 128-row query tiles (longest first), sequence b.
   const int h = p.h_lo + blockIdx.x;
@@ -179,6 +210,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     k_beg = p.cu_k[b];
     Sk = p.cu_k[b + 1] - k_beg;
+  }
+  // e4m3 V^T tiles are addressed by key index in the innermost (byte)
+  // dimension, which a TMA copy needs at a multiple of 16: the whole CTA leaves,
+  // before any barrier or TMEM is set up, if the sequence does not start there.
+  if (FP8 && (k_beg & 15)) {
+    if (threadIdx.x == 0) record_error(p.err, DEV_FP8_ALIGN);
+    return;
   }
 
   Smem sm;
@@ -235,8 +273,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t* dst = smem + OFF_KV + slot * TILE;
     ATTN_TC_TRACE(20 + (is_v ? 1 : 0), j);
     mbar_arrive_expect_tx(&sm.kv_full[slot], TILE);
-    if (!PAGED) {
-      for (int hf = 0; hf < 2; ++hf) tma_load_3d(dst + hf * HALF, tm, &sm.kv_full[slot], hf * 64, g, k_beg + j * BN);
+    if (FP8 && is_v) {  // V^T codes [hkv][128][keys]: one box of 128 keys x 128 dims
+      tma_load_3d(dst, tm, &sm.kv_full[slot], k_beg + j * BN, 0, g);
+    } else if (!PAGED) {
+      for (int hf = 0; hf < C::NBOX; ++hf)
+        tma_load_3d(dst + hf * HALF, tm, &sm.kv_full[slot], hf * 64, g, k_beg + j * BN);
     } else {
       for (int pp = 0; pp < 2; ++pp) {  // two 64-token pages per tile
         const int lp = j * 2 + pp;
@@ -278,7 +319,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int t = 0; t < 2; ++t) {
       if (q0 + t * BM >= Sq) continue;
       mbar_arrive_expect_tx(&sm.q_full[t], TILE);
-      for (int hf = 0; hf < 2; ++hf)
+      for (int hf = 0; hf < C::NBOX; ++hf)
         tma_load_3d(smem + OFF_Q + t * TILE + hf * HALF, &tm_q, &sm.q_full[t], hf * 64, h, q_beg + q0 + t * BM);
     }
     if (k0_early) load_kv(0, false, 0);
@@ -295,7 +336,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int q0n = (gridDim.y - 1 - yn) * 2 * BM;
       for (int t = 0; t < 2; ++t)
         if (q0n + t * BM < sqn)
-          for (int hf = 0; hf < 2; ++hf) tma_prefetch_l2_3d(&tm_q, hf * 64, p.h_lo + xn, qbn + q0n + t * BM);
+          for (int hf = 0; hf < C::NBOX; ++hf) tma_prefetch_l2_3d(&tm_q, hf * 64, p.h_lo + xn, qbn + q0n + t * BM);
     }
   }
   tc_fence_before();
@@ -378,7 +419,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               tc_fence_after();
             }
             ATTN_TC_TRACE(22 + t, j);
-            mma_scores(tmem + t * BN, dQ + t * kTile16, dK + slotK * kTile16);
+            mma_scores<FP8>(tmem + t * BN, dQ + t * kTile16, dK + slotK * kTile16);
             tc_commit_warp(&sm.s_full[t]);
             ATTN_TC_TRACE(2 + 3 * t, j);
           }
@@ -387,7 +428,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       } else {
         const uint64_t dP = sdesc_sw128(smem_u32(smem + OFF_P), 16, 1024);
-        const uint64_t dV = sdesc_sw128(smem_u32(smem + OFF_KV), HALF, 1024);
+        const uint64_t dV = sdesc_sw128(smem_u32(smem + OFF_KV), FP8 ? 16 : HALF, 1024);
         bool ok = true;
         for (int j = 0; j < nkv && ok; ++j) {
           const int iV = ring_pos_v(j, nkv), slotV = iV % NSLOT;
@@ -400,7 +441,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_after();
             ATTN_TC_TRACE(7 - 4 * t, j);
             ATTN_TC_TRACE(24 + t, j);
-            mma_values(tmem + 2 * BN + t * D, dP + t * kTile16, dV + slotV * kTile16, j > 0);
+            mma_values<FP8>(tmem + 2 * BN + t * D, dP + t * kTile16, dV + slotV * kTile16, j > 0);
             tc_commit_warp(&sm.o_done[t]);
             ATTN_TC_TRACE(8 - 4 * t, j);
           }
@@ -419,7 +460,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int qp = rv ? p.q_pos[q_beg + rq] : 0;
     const int nkv_t = sm.nkv[t];
     const int nfull_t = sm.nfull[t];
-    const float sl2 = p.scale * 1.4426950408889634f;
+    // score = c_row * (MMA output): the softmax scale, times the query row's and
+    // the key head's e4m3 scales when the inputs are codes.  A zero scale (an
+    // all-zero group, whose codes are all zero) makes every score 0; c_row is
+    // kept at least FLT_MIN so that masked scores (-inf) still give weight 0.
+    const float c_row = FP8 ? fmaxf(p.scale * (rv ? __ldg(p.q_scale + (int64_t)(q_beg + rq) * p.hq + h) : 0.f) *
+                                        __ldg(p.k_scale + g),
+                                    FLT_MIN)
+                            : p.scale;
+    const float sl2 = c_row * 1.4426950408889634f;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * BN;
     const uint32_t tO = tmem + lane_base + 2 * BN + t * D;
@@ -427,7 +476,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
 
-    if (p.q_cs && nkv_t > 0) {
+    if (!FP8 && p.q_cs && nkv_t > 0) {
       // RoPE of the query, fused: the warp rotates its 32 rows of Q_t in shared
       // memory with the same cos/sin and the same rounding as rope_apply, so the
       // scores are those of rope_apply followed by this kernel, bit for bit.
@@ -564,23 +613,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint64_t acc[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] = f2_pack(0.f, 0.f);
+      if constexpr (!FP8) {
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        float e[8];
+        for (int c8 = 0; c8 < 16; ++c8) {
+          float e[8];
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[c8 * 8 + i], s[c8 * 8 + i + 1]), sl2x2, nmbx2), x0, x1);
-          e[i] = fast_exp2(x0);
-          e[i + 1] = fast_exp2(x1);
-          acc[i >> 1] = f2_add(acc[i >> 1], f2_pack(e[i], e[i + 1]));
+          for (int i = 0; i < 8; i += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[c8 * 8 + i], s[c8 * 8 + i + 1]), sl2x2, nmbx2), x0, x1);
+            e[i] = fast_exp2(x0);
+            e[i + 1] = fast_exp2(x1);
+            acc[i >> 1] = f2_add(acc[i >> 1], f2_pack(e[i], e[i + 1]));
+          }
+          uint4 v;
+          v.x = pack_bf16x2(e[0], e[1]);
+          v.y = pack_bf16x2(e[2], e[3]);
+          v.z = pack_bf16x2(e[4], e[5]);
+          v.w = pack_bf16x2(e[6], e[7]);
+          *reinterpret_cast<uint4*>(prow + (c8 >> 3) * HALF + (((c8 & 7) ^ (row & 7)) << 4)) = v;
         }
-        uint4 v;
-        v.x = pack_bf16x2(e[0], e[1]);
-        v.y = pack_bf16x2(e[2], e[3]);
-        v.z = pack_bf16x2(e[4], e[5]);
-        v.w = pack_bf16x2(e[6], e[7]);
-        *reinterpret_cast<uint4*>(prow + (c8 >> 3) * HALF + (((c8 & 7) ^ (row & 7)) << 4)) = v;
+      } else {
+        // e4m3 P: 16 keys per 16-byte chunk of the single box (P <= 256 < 448)
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16) {
+          float e[16];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[c16 * 16 + i], s[c16 * 16 + i + 1]), sl2x2, nmbx2), x0, x1);
+            e[i] = fast_exp2(x0);
+            e[i + 1] = fast_exp2(x1);
+            acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(e[i], e[i + 1]));
+          }
+          uint4 v;
+          v.x = (uint32_t)pack_e4m3x2(e[0], e[1]) | ((uint32_t)pack_e4m3x2(e[2], e[3]) << 16);
+          v.y = (uint32_t)pack_e4m3x2(e[4], e[5]) | ((uint32_t)pack_e4m3x2(e[6], e[7]) << 16);
+          v.z = (uint32_t)pack_e4m3x2(e[8], e[9]) | ((uint32_t)pack_e4m3x2(e[10], e[11]) << 16);
+          v.w = (uint32_t)pack_e4m3x2(e[12], e[13]) | ((uint32_t)pack_e4m3x2(e[14], e[15]) << 16);
+          *reinterpret_cast<uint4*>(prow + ((c16 ^ (row & 7)) << 4)) = v;
+        }
       }
       {
         float a0, a1;
@@ -620,7 +691,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
     }
     const bool have_o = ok && nkv_t > 0;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? (FP8 ? __ldg(p.v_scale + g) : 1.f) / l : 0.f;
     const int64_t orow = ((int64_t)(q_beg + rq) * p.hq + h) * D;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -654,7 +725,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-    if (rv && p.lse) p.lse[(int64_t)(q_beg + rq) * p.hq + h] = l > 0.f ? m_ref * p.scale + logf(l) : -INFINITY;
+    if (rv && p.lse) p.lse[(int64_t)(q_beg + rq) * p.hq + h] = l > 0.f ? m_ref * c_row + logf(l) : -INFINITY;
     if (row == 0) ATTN_TC_TRACE(30 + t, 0);
   }
 
@@ -669,34 +740,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 }  // namespace tc
 
+namespace {
+
+template <bool PAGED, bool FP8>
+cudaError_t launch_variant(const tc::Params& p, dim3 grid, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t s) {
+  // per device: raise the dynamic shared-memory limit once, and check the
+  // compiled register count (384 threads fit on an SM only at <= 168 registers),
+  // so a toolchain change shows up as an error, not a failed launch
+  static int ready[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!ready[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tc::prefill_tc_kernel<PAGED, FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Cfg<FP8>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, tc::prefill_tc_kernel<PAGED, FP8>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs > tc::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
+    ready[dev] = 1;
+  }
+  tc::prefill_tc_kernel<PAGED, FP8><<<grid, tc::NTHREADS, tc::Cfg<FP8>::SMEM_BYTES, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, const CUtensorMap& tk,
                               const CUtensorMap& tv, cudaStream_t s) {
-  static bool attr_set[2][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   const bool paged = a.page_table != nullptr;
-  if (dev < 64 && !attr_set[paged][dev]) {
-    cudaError_t e = paged ? cudaFuncSetAttribute(tc::prefill_tc_kernel<true>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES)
-                          : cudaFuncSetAttribute(tc::prefill_tc_kernel<false>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set[paged][dev] = true;
-  }
+  if (a.fp8 && paged) return cudaErrorInvalidValue;
   if (a.max_seqlen_q == 0 || a.batch == 0 || a.h_hi == a.h_lo) return cudaSuccess;
-  {
-    // 384 threads fit on an SM only at <= 168 registers per thread; check the
-    // compiled count so a toolchain change shows up as an error, not a failed launch.
-    static int regs[2][64] = {};
-    if (dev < 64 && regs[paged][dev] == 0) {
-      cudaFuncAttributes fa;
-      cudaError_t e = paged ? cudaFuncGetAttributes(&fa, tc::prefill_tc_kernel<true>)
-                            : cudaFuncGetAttributes(&fa, tc::prefill_tc_kernel<false>);
-      if (e != cudaSuccess) return e;
-      regs[paged][dev] = fa.numRegs;
-    }
-    if (dev >= 64 || regs[paged][dev] > tc::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
-  }
   tc::Params p;
   p.cu_q = a.cu_q;
   p.q_pos = a.q_pos;
@@ -716,6 +794,9 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, con
   p.out_f32 = a.out_f32;
   p.scale = a.scale;
   p.q_cs = reinterpret_cast<const float4*>(a.q_rope_cs);
+  p.q_scale = a.q_scale;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
   {
     static int sms[64] = {};
     if (dev < 64 && sms[dev] == 0) {
@@ -727,11 +808,9 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, const CUtensorMap& tq, con
   }
   const int pairs = (a.max_seqlen_q + 2 * tc::BM - 1) / (2 * tc::BM);
   dim3 grid(a.h_hi - a.h_lo, pairs, a.batch);
-  if (paged)
-    tc::prefill_tc_kernel<true><<<grid, tc::NTHREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, p);
-  else
-    tc::prefill_tc_kernel<false><<<grid, tc::NTHREADS, tc::SMEM_BYTES, s>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  if (a.fp8) return launch_variant<false, true>(p, grid, tq, tk, tv, s);
+  if (paged) return launch_variant<true, false>(p, grid, tq, tk, tv, s);
+  return launch_variant<false, false>(p, grid, tq, tk, tv, s);
 }
 
 }  // namespace attn

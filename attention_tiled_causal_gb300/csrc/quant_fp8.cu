@@ -15,12 +15,7 @@
 namespace attn {
 namespace q8 {
 
-// Two fp32 values -> two e4m3 bytes (round to nearest even, saturating at +-448).
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) { return pack_e4m3x2(lo, hi); }
 
 __device__ __forceinline__ void unpack_bf16x4(uint2 w, float (&x)[4]) {
   x[0] = __uint_as_float(w.x << 16);
@@ -99,7 +94,9 @@ __global__ void __launch_bounds__(256) quant_heads_kernel(const __nv_bfloat16* _
 }
 
 // Transposed codes [heads][128][t_stride]: a block takes 32 tokens x one head,
-// reads the 32 rows coalesced, and writes 128 rows of 32 contiguous bytes.
+// reads the 32 rows coalesced, and writes 128 rows of 32 contiguous bytes.  The
+// grid spans t_stride, so columns [tokens, t_stride) are written as zero codes
+// (the prefill's last K/V tile reads them, with weight 0).
 __global__ void __launch_bounds__(256) quant_heads_t_kernel(const __nv_bfloat16* __restrict__ x, int64_t tokens,
                                                             int heads, const unsigned* __restrict__ amax_bits,
                                                             uint8_t* __restrict__ codes_t, int64_t t_stride) {
@@ -128,16 +125,11 @@ __global__ void __launch_bounds__(256) quant_heads_t_kernel(const __nv_bfloat16*
   for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
     const int dd = i >> 3, q = i & 7;
     const int64_t t = t0 + q * 4;
-    if (t >= tokens) continue;
+    if (t >= t_stride) continue;  // t_stride is a multiple of 16: the word fits whole
     uint32_t w = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) w |= (uint32_t)tile[dd][q * 4 + e] << (8 * e);
-    uint8_t* dst = codes_t + ((int64_t)h * 128 + dd) * t_stride + t;
-    if (t + 4 <= tokens) {
-      *reinterpret_cast<uint32_t*>(dst) = w;
-    } else {
-      for (int e = 0; e < 4 && t + e < tokens; ++e) dst[e] = (uint8_t)(w >> (8 * e));
-    }
+    *reinterpret_cast<uint32_t*>(codes_t + ((int64_t)h * 128 + dd) * t_stride + t) = w;
   }
 }
 
@@ -165,7 +157,7 @@ cudaError_t launch_quant_fp8_heads(const void* x, int64_t tokens, int heads, voi
   dim3 agrid((unsigned)min((tokens * 16 + 255) / 256, (int64_t)512), (unsigned)heads);
   q8::head_amax_kernel<<<agrid, 256, 0, s>>>((const __nv_bfloat16*)x, tokens, heads, amax_scratch);
   if (transposed) {
-    dim3 grid((unsigned)((tokens + 31) / 32), (unsigned)heads);
+    dim3 grid((unsigned)((t_stride + 31) / 32), (unsigned)heads);
     q8::quant_heads_t_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)x, tokens, heads, amax_scratch,
                                                   (uint8_t*)codes, t_stride);
   } else {

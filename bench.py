@@ -1,7 +1,7 @@
 """Benchmark of the attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload all|prefill|decode|long|chunked] [--no-cpu-baseline] [--decode-requests N]
+                    [--workload all|prefill|decode|long|chunked|fp8] [--no-cpu-baseline] [--decode-requests N]
 
 Headline (the JSON `value`): causal GQA prefill, batch 1 x 8192 tokens, 64 query /
 8 KV heads, head_dim 128, bf16 -- one step = RoPE of Q and K at absolute
@@ -11,6 +11,8 @@ contexts U[16384, 131072], 16 splits + LSE merge) is reported in `decode`,
 as KV-cache GB/s.  `prefill_64k` times 2 x 65536-token causal prefill over all
 heads and over heads 16..31 alone; `chunked` times chunked prefill of 4 x 8192
 new tokens over a 57344-token paged prefix (prefix call + chunk call + merge).
+`prefill_fp8` times the 8K prefill in the FP8 mode (e4m3 Q/K/V codes with
+per-row / per-head scales; the quantisation is inside the step).
 Inputs are synthetic and seeded (N(0,1)/sqrt(2) bf16).
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on
@@ -323,6 +325,64 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
     return res
 
 
+def fp8_prefill_arm(wl, args, timer, peaks, peak_src, inputs=None):
+    """The 8K prefill in the FP8 mode: RoPE of Q and K in bf16, e4m3 codes for Q (one
+    scale per token and head), K and V (one scale per KV head; V transposed), then
+    attention on the codes.  The tensor-core peak for e4m3 is the measured bf16
+    peak times the nominal e4m3 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)."""
+    import attention_tiled_causal_gb300 as atc
+    if inputs is None:
+        inp = wl.make("cuda")
+        inputs = (inp["q"], inp["k"], inp["v"], inp["pos"], inp["cu"])
+    q, k, v, pos, cu = inputs
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    codes = {}
+
+    def quant():
+        codes["q"] = atc.quant_fp8_rows(q)
+        codes["k"] = atc.quant_fp8_heads(k)
+        codes["v"] = atc.quant_fp8_heads(v, transposed=True)
+
+    def attend():
+        (cq, sq), (ck, sk), (cv, sv) = codes["q"], codes["k"], codes["v"]
+        atc.attn_prefill_fp8(cq, sq, ck, sk, cv, sv, out, lse, cu, pos, wl.seq, cu, pos)
+
+    def step(ev=()):
+        atc.rope_apply(q, pos)
+        atc.rope_apply(k, pos)
+        quant()
+        if ev:
+            ev[0].record()
+        attend()
+        if ev:
+            ev[1].record()
+
+    ms, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
+    ms_q, _ = timer.run(lambda ev=(): quant(), args.steps, args.warmup)
+    atc.attn_device_status()
+    flops = wl.flops()
+    peak = 2.0 * peaks["bf16_tflops"]
+    achieved = flops / (ms_kernel * 1e-3) / 1e12
+    quant_bytes = (q.numel() + 2 * k.numel()) * 2 + (q.numel() + 2 * k.numel()) + q.numel() // 128 * 4 \
+        + 2 * k.numel() * 2  # bf16 in, codes out, row scales; K and V read twice (max, then codes)
+    return {
+        "workload": wl.name + " with e4m3 Q/K/V codes (RoPE + quantisation + attention, O and LSE)",
+        "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+        "steps": args.steps, "warmup": args.warmup, "dtype": "e4m3 operands, fp32 accumulation and softmax",
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic("prefill_tc_fp8_causal_8k.md", "prefill_tc.cu"),
+                     "traffic_scope": "prefill_tc_kernel<false, true> (ncu)",
+                     "kernel": "attn::tc::prefill_tc_kernel<false, true>", "kernel_ms": round(ms_kernel, 4),
+                     "peak_source": f"{peak_src} bf16 dense (burst) x 2, the nominal e4m3 / bf16 ratio",
+                     "vs_bf16_kernel_peak": round(achieved / peaks["bf16_tflops"], 4)},
+        "quantisation": hbm_line("quant_fp8_rows (Q) + quant_fp8_heads (K; V transposed)", quant_bytes, ms_q, peaks,
+                                 peak_src),
+        "gpu_launches_per_step": 2 + 1 + 2 * 3 + 1,
+    }
+
+
 def decode_arm(wl, args, timer, peaks, peak_src):
     import attention_tiled_causal_gb300 as atc
     inp = wl.make("cuda")
@@ -598,7 +658,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="all", choices=["all", "prefill", "decode", "long", "chunked"])
+    ap.add_argument("--workload", default="all", choices=["all", "prefill", "decode", "long", "chunked", "fp8"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-requests", type=int, default=None,
                     help="decode workload with fewer requests (first N of the seeded 32); for small profiler captures")
@@ -650,6 +710,9 @@ def main():
         dec["cached_tokens_per_s"] = round(int(dwl.ctx_lens().astype(np.int64).sum()) / (dec["ms_per_step"] * 1e-3), 0)
         torch.cuda.empty_cache()
     extra = {}
+    if args.workload in ("all", "fp8"):
+        extra["prefill_fp8"] = fp8_prefill_arm(wl, args, timer, peaks, peak_src, res["inputs"] if res else None)
+        torch.cuda.empty_cache()
     if args.workload in ("all", "long"):
         extra["prefill_64k"] = long_prefill_arm(synth.PREFILL_64K, args, timer, peaks, peak_src)
         torch.cuda.empty_cache()

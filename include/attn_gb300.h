@@ -157,7 +157,8 @@ ATTN_API int attn_kv_append_paged_int8(const void *k_new, const void *v_new, con
  *                   scales [heads]; codes [tokens][heads][128] (transposed = 0)
  *                   or [heads][128][t_stride] (transposed = 1, t_stride >= tokens
  *                   and a multiple of 16: the values, whose P V contraction reads
- *                   V^T rows).  amax_scratch: caller-owned [heads] unsigned.
+ *                   V^T rows; columns [tokens, t_stride) are written as zero
+ *                   codes).  amax_scratch: caller-owned [heads] unsigned.
  * x and codes 16-byte aligned; head_dim must be 128.
  */
 ATTN_API int quant_fp8_rows(const void *x, int64_t tokens, int heads, int head_dim, void *codes, float *scales,
@@ -232,6 +233,32 @@ ATTN_API int attn_prefill_rope_q(const void *q, const void *k, const void *v, vo
                                  const int32_t *k_lens, int max_pages, int page_size, int64_t num_pages,
                                  int num_q_heads, int num_kv_heads, int head_dim, int h_lo, int h_hi, float scale,
                                  int causal, const float *q_rope_cs, void *stream);
+
+/*
+ * attn_prefill_fp8 -- attn_prefill (contiguous source) on e4m3 codes: the FP8
+ * mode of "Flash Attention and distributed parallelism", section 18.5, with
+ * block quantisation.  The attention computed is that of the values the codes
+ * stand for: q = code * q_scale[row], k = code * k_scale[kv head], v = code *
+ * v_scale[kv head] (quant_fp8_rows / quant_fp8_heads produce them).  Both
+ * contractions run on e4m3 operands with fp32 accumulation; the softmax is
+ * fp32 and the weights P are rounded to e4m3 for P V (P <= 256), so O carries
+ * that rounding (relative 2^-4 per weight); LSE uses the unrounded weights.
+ *
+ *  q        [total_q][num_q_heads][128] e4m3;  q_scale [total_q][num_q_heads] fp32.
+ *  k        [total_k][num_kv_heads][128] e4m3; k_scale [num_kv_heads] fp32.
+ *  v_t      [num_kv_heads][128][v_t_stride] e4m3 (values transposed, keys
+ *           contiguous; v_t_stride >= total_k, a multiple of 16); v_scale
+ *           [num_kv_heads] fp32.
+ *  Every key sequence must start at a multiple of 16 tokens (cu_k[b] % 16 == 0):
+ *  a CTA whose sequence does not records a device error and writes nothing.
+ *  Everything else as attn_prefill (head_dim 128; no paged source).
+ */
+ATTN_API int attn_prefill_fp8(const void *q, const float *q_scale, const void *k, const float *k_scale,
+                              const void *v_t, const float *v_scale, int64_t v_t_stride, void *out,
+                              attn_dtype_t out_dtype, float *lse, int batch, const int32_t *cu_q,
+                              const int32_t *q_pos, int64_t total_q, int max_seqlen_q, const int32_t *cu_k,
+                              const int32_t *k_pos, int64_t total_k, int num_q_heads, int num_kv_heads,
+                              int head_dim, int h_lo, int h_hi, float scale, int causal, void *stream);
 
 /*
  * attn_decode_paged -- split-KV decode over a head-major paged KV cache.

@@ -855,3 +855,125 @@ def test_quant_fp8_rows_and_heads_match_oracle():
     np.testing.assert_array_equal(s_t.cpu().numpy(), ws_h)
     assert c_t.shape == (H, 128, 336)
     np.testing.assert_array_equal(c_t.float().cpu().numpy()[:, :, :T], np.transpose(want_h, (1, 2, 0)))
+    assert (c_t.view(torch.uint8)[:, :, T:] == 0).all()   # the padding columns are zero codes
+
+
+# ------------------------------------------------------------------ FP8 (e4m3) prefill
+
+def _fp8_case(lens, hq, hkv, starts, seed, zero_k=False):
+    """Already-rotated bf16 Q/K/V; every sequence but the last is a multiple of 16
+    tokens long, so every key sequence starts on a 16-token boundary."""
+    T = sum(lens)
+    q = synth.randn((T, hq, 128), seed, 0.7071)
+    k = torch.zeros((T, hkv, 128), dtype=torch.bfloat16) if zero_k else synth.randn((T, hkv, 128), seed + 1, 0.7071)
+    v = synth.randn((T, hkv, 128), seed + 2, 0.7071)
+    return q, k, v, synth.positions(lens, starts), synth.cu_seqlens(lens)
+
+
+def _run_fp8(q, k, v, pos, cu, lens, causal=True, h_lo=0, h_hi=None, out_dtype=torch.bfloat16):
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    cq, sq = atc.quant_fp8_rows(qd)
+    ck, sk = atc.quant_fp8_heads(kd)
+    cv, sv = atc.quant_fp8_heads(vd, transposed=True)
+    posd, cud = torch.from_numpy(pos).to(DEV), torch.from_numpy(cu).to(DEV)
+    out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=DEV)
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    atc.attn_prefill_fp8(cq, sq, ck, sk, cv, sv, out, lse, cud, posd, max(lens), cud, posd, h_lo=h_lo, h_hi=h_hi,
+                         causal=causal)
+    atc.attn_device_status()
+    return out, lse
+
+
+def _fp8_oracle(q, k, v, pos, cu, lens, causal=True, h_lo=0, h_hi=None):
+    """Attention in fp64 over the values the e4m3 codes stand for (code x group scale)."""
+    cq, sq = oracle.quant_e4m3(synth.as_f64(q), [0, 1])
+    ck, sk = oracle.quant_e4m3(synth.as_f64(k), [1])
+    cv, sv = oracle.quant_e4m3(synth.as_f64(v), [1])
+    qh = cq * sq.astype(np.float64)[:, :, None]
+    kh = ck * sk.astype(np.float64)[None, :, None]
+    vh = cv * sv.astype(np.float64)[None, :, None]
+    o, l = oracle.attention(qh, seq_ids(lens), pos, kh, vh, cu, pos, 128 ** -0.5, causal=causal, h_lo=h_lo,
+                            h_hi=h_hi)
+    return o, l, vh
+
+
+# The FP8 path rounds each softmax weight p (0 <= p <= 256 with the lazy
+# rescale) to e4m3 before P V, while l sums the unrounded weights.  A normal
+# e4m3 value carries relative error <= 2^-4, so |dO| <= 2^-4 max|v| per row plus
+# at most 2^-10 per subnormal weight (p < 2^-6), which l >= 1 divides.  The
+# rounding errors are zero-mean and independent: with RMS relative error about
+# 2^-4 / sqrt(3) and softmax rows over n ~ U[1, N] keys of std 0.71, the mean
+# |dO| is about 0.8 * 0.036 * 0.71 * 2 / sqrt(N), 2e-3 at N = 300; the mean
+# bound below is twice that, and the max bound adds the subnormal term for the
+# few keys a row can see with non-negligible weight.  The scores are exact
+# products of e4m3 codes summed in fp32, so the LSE bound stays 1e-3.
+FP8_MEAN = 4e-3
+
+
+def _fp8_max_tol(vh):
+    return 2.0 ** -4 * np.abs(vh).max() + 32 * 2.0 ** -10 * np.abs(vh).max()
+
+
+FP8_CASES = [
+    ([300], 16, 2, [0]),                      # several tiles and a ragged tail
+    ([256, 144, 512, 1], 16, 2, [0, 5, 100000, 7]),  # varlen, offsets, a 1-token sequence
+    ([160, 333], 8, 1, [0, 0]),               # MQA, ragged last sequence
+    ([704], 64, 8, [0]),                      # the 64/8 head layout
+]
+
+
+@pytest.mark.parametrize("lens,hq,hkv,starts", FP8_CASES)
+def test_prefill_fp8_matches_oracle_on_dequantised_inputs(lens, hq, hkv, starts):
+    q, k, v, pos, cu = _fp8_case(lens, hq, hkv, starts, 900 + hq + len(lens))
+    out, lse = _run_fp8(q, k, v, pos, cu, lens)
+    want_o, want_l, vh = _fp8_oracle(q, k, v, pos, cu, lens)
+    check(out, lse, want_o, want_l, tol_max=_fp8_max_tol(vh), tol_mean=FP8_MEAN, what=f"fp8 {lens}")
+
+
+def test_prefill_fp8_uniform_weights_are_exact():
+    """Zero keys make every visible score 0, so each weight is exactly 1 in e4m3 and
+    O is the plain mean of the visible dequantised values: the P V side (V^T
+    layout, value scale, masking, the e4m3 P tile) is checked to fp32 rounding."""
+    lens = [256, 77]
+    q, k, v, pos, cu = _fp8_case(lens, 16, 2, [0, 3], 910, zero_k=True)
+    out, lse = _run_fp8(q, k, v, pos, cu, lens, out_dtype=torch.float32)
+    want_o, want_l, vh = _fp8_oracle(q, k, v, pos, cu, lens)
+    check(out, lse, want_o, want_l, tol_max=1e-5, tol_mean=1e-6, tol_lse=1e-5, what="fp8 uniform")
+
+
+def test_prefill_fp8_non_causal_head_slice_fp32_out():
+    lens = [192, 200]
+    q, k, v, pos, cu = _fp8_case(lens, 16, 2, [0, 0], 911)
+    out, lse = _run_fp8(q, k, v, pos, cu, lens, causal=False, h_lo=8, h_hi=16, out_dtype=torch.float32)
+    want_o, want_l, vh = _fp8_oracle(q, k, v, pos, cu, lens, causal=False, h_lo=8, h_hi=16)
+    check(out[:, 8:], lse[:, 8:], want_o[:, 8:], want_l[:, 8:], tol_max=_fp8_max_tol(vh), tol_mean=FP8_MEAN,
+          what="fp8 non-causal")
+    assert torch.isnan(out[:, :8]).all()
+
+
+def test_prefill_fp8_is_deterministic():
+    lens = [1024, 320]
+    q, k, v, pos, cu = _fp8_case(lens, 64, 8, [0, 9], 912)
+    first = _run_fp8(q, k, v, pos, cu, lens)
+    for _ in range(2):
+        o, l = _run_fp8(q, k, v, pos, cu, lens)
+        assert torch.equal(o, first[0]) and torch.equal(l, first[1])
+
+
+def test_prefill_fp8_misaligned_key_sequence_is_reported():
+    """A key sequence starting off a 16-token boundary is refused by its CTAs
+    (recorded device error, nothing written); the aligned sequence is computed."""
+    lens = [8, 200]
+    q, k, v, pos, cu = _fp8_case(lens, 8, 1, [0, 0], 913)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    cq, sq = atc.quant_fp8_rows(qd)
+    ck, sk = atc.quant_fp8_heads(kd)
+    cv, sv = atc.quant_fp8_heads(vd, transposed=True)
+    posd, cud = torch.from_numpy(pos).to(DEV), torch.from_numpy(cu).to(DEV)
+    out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=DEV)
+    atc.attn_prefill_fp8(cq, sq, ck, sk, cv, sv, out, None, cud, posd, 200, cud, posd)
+    with pytest.raises(atc.AttnError) as e:
+        atc.attn_device_status(clear=True)
+    assert "0x204" in str(e.value)
+    assert torch.isnan(out[8:].float()).all()
+    assert not torch.isnan(out[:8].float()).any()
