@@ -16,6 +16,7 @@ Entry points (same names as the C ABI):
     attn_prefill(q, k, v, out, lse, cu_q, q_pos, ...)   tiled causal GQA attention
     attn_prefill_fp8(q, q_scale, k, k_scale, v_t, v_scale, ...)  the same on e4m3 codes (FP8 mode)
     quant_fp8_rows(x) / quant_fp8_heads(x, transposed)   e4m3 codes and scales for it
+    rope_quant_fp8_rows / rope_quant_fp8_heads(x, positions)  RoPE fused into that quantisation
     attn_decode_paged(q, k_cache, v_cache, ...)         split-KV decode over a paged cache
     attn_decode_paged_int8(q, k_codes, v_codes, k_scale, v_scale, ...)   the same over an INT8 cache
     attn_lse_merge(part_out, part_lse, out, lse, ...)   log-sum-exp merge of partials
@@ -23,8 +24,10 @@ Entry points (same names as the C ABI):
 from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_decode_paged_int8,
                        attn_device_status,
                        attn_kv_append_paged, attn_kv_append_paged_int8, attn_lse_merge, attn_prefill, attn_prefill_fp8,
-                       decode_workspace, lib_path, library, prefill, quant_fp8_heads, quant_fp8_rows, rope_apply, rope_table)
+                       decode_workspace, lib_path, library, prefill, quant_fp8_heads, quant_fp8_rows, rope_apply, rope_quant_fp8_heads,
+                       rope_quant_fp8_rows, rope_table)
 
 __all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_decode_paged_int8", "attn_device_status",
            "attn_kv_append_paged", "attn_kv_append_paged_int8", "attn_lse_merge", "attn_prefill", "attn_prefill_fp8", "decode_workspace", "lib_path", "library",
-           "prefill", "quant_fp8_heads", "quant_fp8_rows", "rope_apply", "rope_table"]
+           "prefill", "quant_fp8_heads", "quant_fp8_rows", "rope_apply", "rope_quant_fp8_heads",
+           "rope_quant_fp8_rows", "rope_table"]

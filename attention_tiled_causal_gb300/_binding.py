@@ -51,6 +51,10 @@ def library():
                                      I32, I32, I32, F32, I32, P]
     lib.attn_prefill_fp8.restype = I32
     lib.quant_fp8_rows.argtypes = [P, I64, I32, I32, P, P, P]
+    lib.rope_quant_fp8_rows.argtypes = [P, I64, I32, I32, P, F64, P, P, P]
+    lib.rope_quant_fp8_rows.restype = I32
+    lib.rope_quant_fp8_heads.argtypes = [P, I64, I32, I32, P, F64, P, P, P, P]
+    lib.rope_quant_fp8_heads.restype = I32
     lib.quant_fp8_rows.restype = I32
     lib.quant_fp8_heads.argtypes = [P, I64, I32, I32, P, P, P, I32, I64, P]
     lib.quant_fp8_heads.restype = I32
@@ -233,6 +237,33 @@ def quant_fp8_heads(x, transposed: bool = False, stream=None):
     scratch = torch.empty((H,), dtype=torch.int32, device=x.device)
     _check(library().quant_fp8_heads(_ptr(x), T, H, d, _ptr(codes), _ptr(scales), _ptr(scratch),
                                      1 if transposed else 0, t_stride, _stream(stream)))
+    return codes.view(torch.float8_e4m3fn), scales
+
+
+def rope_quant_fp8_rows(x, positions, base: float = 10000.0, stream=None):
+    """RoPE at `positions` fused into quant_fp8_rows (x is not modified): returns
+    (codes float8_e4m3fn [tokens, heads, 128], scales [tokens, heads])."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 3:
+        raise ValueError("x must be a contiguous bf16 [tokens, heads, head_dim] tensor")
+    T, H, d = x.shape
+    codes = torch.empty((T, H, d), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _check(library().rope_quant_fp8_rows(_ptr(x), T, H, d, _ptr(_i32(positions, "positions")), float(base),
+                                         _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes.view(torch.float8_e4m3fn), scales
+
+
+def rope_quant_fp8_heads(x, positions, base: float = 10000.0, stream=None):
+    """RoPE at `positions` fused into quant_fp8_heads, row layout (x is not modified):
+    returns (codes float8_e4m3fn [tokens, heads, 128], scales [heads])."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 3:
+        raise ValueError("x must be a contiguous bf16 [tokens, heads, head_dim] tensor")
+    T, H, d = x.shape
+    codes = torch.empty((T, H, d), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((H,), dtype=torch.float32, device=x.device)
+    scratch = torch.empty((H,), dtype=torch.int32, device=x.device)
+    _check(library().rope_quant_fp8_heads(_ptr(x), T, H, d, _ptr(_i32(positions, "positions")), float(base),
+                                          _ptr(codes), _ptr(scales), _ptr(scratch), _stream(stream)))
     return codes.view(torch.float8_e4m3fn), scales
 
 

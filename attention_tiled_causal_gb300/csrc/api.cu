@@ -256,6 +256,38 @@ int quant_fp8_rows(const void* x, int64_t tokens, int heads, int head_dim, void*
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "quant_fp8_rows launch");
 }
 
+static int rope_quant_check(const char* name, const void* x, int64_t tokens, int heads, int head_dim,
+                            const int32_t* positions, double base, const void* codes, const float* scales) {
+  if (tokens < 0 || heads < 0) return fail(ATTN_ERR_ARG, "%s: negative size", name);
+  if (head_dim != 128) return fail(ATTN_ERR_SHAPE, "%s: head_dim %d (need 128)", name, head_dim);
+  if (!(base > 0.0)) return fail(ATTN_ERR_ARG, "%s: base must be positive", name);
+  if (tokens == 0 || heads == 0) return ATTN_OK;
+  if (!x || !positions || !codes || !scales) return fail(ATTN_ERR_ARG, "%s: null pointer", name);
+  if (!aligned16(x) || !aligned16(codes)) return fail(ATTN_ERR_ALIGN, "%s: x / codes not 16-byte aligned", name);
+  return ATTN_OK;
+}
+
+int rope_quant_fp8_rows(const void* x, int64_t tokens, int heads, int head_dim, const int32_t* positions,
+                        double base, void* codes, float* scales, void* stream) {
+  int rc = rope_quant_check("rope_quant_fp8_rows", x, tokens, heads, head_dim, positions, base, codes, scales);
+  if (rc || tokens == 0 || heads == 0) return rc;
+  cudaError_t e = attn::launch_rope_quant_fp8(x, tokens, heads, positions, base, codes, scales, nullptr,
+                                              (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "rope_quant_fp8_rows launch");
+}
+
+int rope_quant_fp8_heads(const void* x, int64_t tokens, int heads, int head_dim, const int32_t* positions,
+                         double base, void* codes, float* scales, unsigned* amax_scratch, void* stream) {
+  int rc = rope_quant_check("rope_quant_fp8_heads", x, tokens, heads, head_dim, positions, base, codes, scales);
+  if (rc || tokens == 0 || heads == 0) return rc;
+  if (heads > attn::kMaxQuantHeads)
+    return fail(ATTN_ERR_SHAPE, "rope_quant_fp8_heads: %d heads (at most %d)", heads, attn::kMaxQuantHeads);
+  if (!amax_scratch) return fail(ATTN_ERR_ARG, "rope_quant_fp8_heads: null amax_scratch");
+  cudaError_t e = attn::launch_rope_quant_fp8(x, tokens, heads, positions, base, codes, scales, amax_scratch,
+                                              (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "rope_quant_fp8_heads launch");
+}
+
 int quant_fp8_heads(const void* x, int64_t tokens, int heads, int head_dim, void* codes, float* scales,
                     unsigned* amax_scratch, int transposed, int64_t t_stride, void* stream) {
   if (tokens < 0 || heads < 0) return fail(ATTN_ERR_ARG, "quant_fp8_heads: negative size");

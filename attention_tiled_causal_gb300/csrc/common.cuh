@@ -353,6 +353,21 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 // ------------------------------------------------------------------ misc
+// x / s rounded to nearest even in fp32, given r = 1/s rounded to nearest
+// (__frcp_rn): q = x r, then one correction q + (x - q s) r, the remainder
+// formed exactly by an FMA (Markstein's theorem, as in Muller et al.,
+// "Handbook of Floating-Point Arithmetic": with r the correctly rounded
+// reciprocal and q within an ulp, the corrected quotient is the correctly
+// rounded one).  Three instructions instead of a full division.  The remainder
+// is exact while it does not underflow, so callers take this path only for
+// s >= 2^-90 with |x / s| <= 448: an x small enough to underflow it gives a
+// quotient below 2^-13, whose e4m3 code is 0 either way.
+__device__ __forceinline__ float div_rn_recip(float x, float s, float r) {
+  const float q = __fmul_rn(x, r);
+  return __fmaf_rn(__fmaf_rn(-q, s, x), r, q);
+}
+constexpr float kFastDivMinScale = 0x1p-90f;
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -372,6 +387,15 @@ __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// e4m3 codes of x[0..3] / s (see div_rn_recip), packed little-endian.
+template <bool FAST>
+__device__ __forceinline__ uint32_t e4m3x4_div(float x0, float x1, float x2, float x3, float s, float r) {
+  if (FAST)
+    return (uint32_t)pack_e4m3x2(div_rn_recip(x0, s, r), div_rn_recip(x1, s, r)) |
+           ((uint32_t)pack_e4m3x2(div_rn_recip(x2, s, r), div_rn_recip(x3, s, r)) << 16);
+  return (uint32_t)pack_e4m3x2(x0 / s, x1 / s) | ((uint32_t)pack_e4m3x2(x2 / s, x3 / s) << 16);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -42,6 +42,11 @@ cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s);
 cudaError_t launch_quant_fp8_rows(const void* x, int64_t rows, void* codes, float* scales, cudaStream_t s);
 cudaError_t launch_quant_fp8_heads(const void* x, int64_t tokens, int heads, void* codes, float* scales,
                                    unsigned* amax_scratch, bool transposed, int64_t t_stride, cudaStream_t s);
+// RoPE + e4m3 quantisation of a bf16 [tokens][heads][128] tensor: one scale per
+// row when amax_scratch is null, else one per head (amax_scratch: [heads]).
+constexpr int kMaxQuantHeads = 256;
+cudaError_t launch_rope_quant_fp8(const void* x, int64_t tokens, int heads, const int32_t* positions, double base,
+                                  void* codes, float* scales, unsigned* amax_scratch, cudaStream_t s);
 
 struct MergeLaunch {
   const float* part_out;

@@ -1,8 +1,9 @@
 // FP8 (e4m3) quantisation of Q, K and V for the FP8 prefill (Flash Attention
 // page, section 18.5: an FP8 mode with block quantisation).  A group of values
 // shares one fp32 scale = max|x| / 448 (the largest e4m3 value), and each value
-// is stored as e4m3(x / scale), rounded to nearest even with x / scale in fp32;
-// an all-zero group gets scale 0 and codes 0.
+// is stored as e4m3(x / scale), rounded to nearest even with x / scale in fp32
+// (correctly rounded; div_rn_recip computes it in three instructions); an
+// all-zero group gets scale 0 and codes 0.
 //
 //   rows:  a group is one (token, head) row of head_dim values (the queries);
 //   heads: a group is one head over all tokens (keys, values); the codes keep
@@ -15,7 +16,20 @@
 namespace attn {
 namespace q8 {
 
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) { return pack_e4m3x2(lo, hi); }
+// Codes of 8 values x / s: the three-instruction division for normal scales,
+// the full one below kFastDivMinScale; 0 for a zero scale.
+__device__ __forceinline__ uint2 e4m3x8(const float (&v)[4], const float (&u)[4], float s) {
+  uint2 out = make_uint2(0u, 0u);
+  if (s >= kFastDivMinScale) {
+    const float r = __frcp_rn(s);
+    out.x = e4m3x4_div<true>(v[0], v[1], v[2], v[3], s, r);
+    out.y = e4m3x4_div<true>(u[0], u[1], u[2], u[3], s, r);
+  } else if (s != 0.0f) {
+    out.x = e4m3x4_div<false>(v[0], v[1], v[2], v[3], s, 0.f);
+    out.y = e4m3x4_div<false>(u[0], u[1], u[2], u[3], s, 0.f);
+  }
+  return out;
+}
 
 __device__ __forceinline__ void unpack_bf16x4(uint2 w, float (&x)[4]) {
   x[0] = __uint_as_float(w.x << 16);
@@ -37,7 +51,10 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float s = amax / 448.0f;
   uint32_t packed = 0;
-  if (s != 0.0f) packed = (uint32_t)e4m3x2(v[0] / s, v[1] / s) | ((uint32_t)e4m3x2(v[2] / s, v[3] / s) << 16);
+  if (s >= kFastDivMinScale)
+    packed = e4m3x4_div<true>(v[0], v[1], v[2], v[3], s, __frcp_rn(s));
+  else if (s != 0.0f)
+    packed = e4m3x4_div<false>(v[0], v[1], v[2], v[3], s, 0.f);
   reinterpret_cast<uint32_t*>(codes + r * 128)[lane] = packed;
   if (lane == 0) scales[r] = s;
 }
@@ -84,12 +101,7 @@ __global__ void __launch_bounds__(256) quant_heads_kernel(const __nv_bfloat16* _
     float v[4], u[4];
     unpack_bf16x4(make_uint2(w.x, w.y), v);
     unpack_bf16x4(make_uint2(w.z, w.w), u);
-    uint2 out = make_uint2(0u, 0u);
-    if (s != 0.0f) {
-      out.x = (uint32_t)e4m3x2(v[0] / s, v[1] / s) | ((uint32_t)e4m3x2(v[2] / s, v[3] / s) << 16);
-      out.y = (uint32_t)e4m3x2(u[0] / s, u[1] / s) | ((uint32_t)e4m3x2(u[2] / s, u[3] / s) << 16);
-    }
-    reinterpret_cast<uint2*>(codes)[c] = out;
+    reinterpret_cast<uint2*>(codes)[c] = e4m3x8(v, u, s);
   }
 }
 
@@ -114,8 +126,7 @@ __global__ void __launch_bounds__(256) quant_heads_t_kernel(const __nv_bfloat16*
       float v[4], u[4];
       unpack_bf16x4(make_uint2(w.x, w.y), v);
       unpack_bf16x4(make_uint2(w.z, w.w), u);
-      out.x = (uint32_t)e4m3x2(v[0] / s, v[1] / s) | ((uint32_t)e4m3x2(v[2] / s, v[3] / s) << 16);
-      out.y = (uint32_t)e4m3x2(u[0] / s, u[1] / s) | ((uint32_t)e4m3x2(u[2] / s, u[3] / s) << 16);
+      out = e4m3x8(v, u, s);
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) tile[c * 8 + e][tt] = (uint8_t)((e < 4 ? out.x : out.y) >> (8 * (e & 3)));

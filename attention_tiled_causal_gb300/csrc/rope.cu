@@ -36,11 +36,12 @@ constexpr int kTok = 4;  // tokens per block
 // shared memory.  The angle is reduced modulo 2 pi in fp64, then sincosf runs
 // on the reduced fp32 angle.  Every kernel that rotates keys calls this, so
 // their results agree bit for bit.
-__device__ __forceinline__ void angle_tables(float (*cs_s)[128], float (*sn_s)[128], int64_t t0, int64_t tokens,
+template <int NT = kTok, int W = 128>
+__device__ __forceinline__ void angle_tables(float (*cs_s)[W], float (*sn_s)[W], int64_t t0, int64_t tokens,
                                              int half, const int32_t* __restrict__ pos, const InvFreq& f) {
   constexpr double kTwoPi = 6.283185307179586476925286766559;
   constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
-  for (int i = threadIdx.x; i < kTok * half; i += blockDim.x) {
+  for (int i = threadIdx.x; i < NT * half; i += blockDim.x) {
     const int tt = i / half, ii = i % half;
     const int64_t t = t0 + tt;
     if (t < tokens) {
@@ -208,6 +209,23 @@ __device__ __forceinline__ void quant_store_int8(const float (&x)[4], int lane, 
   if (lane == 0) *scale_dst = sc;
 }
 
+// The four values lane l of a warp holds, dims 4l..4l+3 of a 128-wide head
+// row, rotated exactly as rope_kernel rotates them (the RoPE partner of dim i
+// sits 16 lanes away) and rounded to bf16, the value rope_apply stores.
+__device__ __forceinline__ void rope_row4(float (&x)[4], int lane, const float* cs, const float* sn) {
+  const int i0 = 4 * (lane & 15);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float xp = __shfl_xor_sync(0xffffffffu, x[e], 16);
+    float y1, y2;
+    if (lane < 16)
+      rope_rotate(x[e], xp, cs[i0 + e], sn[i0 + e], y1, y2);
+    else
+      rope_rotate(xp, x[e], cs[i0 + e], sn[i0 + e], y1, y2);
+    x[e] = __bfloat162float(__float2bfloat16_rn(lane < 16 ? y1 : y2));
+  }
+}
+
 // kv_append_kernel for an INT8 cache: one warp per (token, KV head), lane l
 // holding dims 4l..4l+3.  A key is rotated exactly as rope_kernel rotates it
 // (its RoPE partner sits 16 lanes away) and rounded to bf16 -- the value a
@@ -251,17 +269,7 @@ __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendLaunch a, con
       x[2] = __uint_as_float(w2.y << 16), x[3] = __uint_as_float(w2.y & 0xffff0000u);
     }
     if (rotate) {
-      const int i0 = 4 * (lane & 15);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float xp = __shfl_xor_sync(0xffffffffu, x[e], 16);
-        float y1, y2;
-        if (lane < 16)
-          rope_rotate(x[e], xp, cs_s[tt][i0 + e], sn_s[tt][i0 + e], y1, y2);
-        else
-          rope_rotate(xp, x[e], cs_s[tt][i0 + e], sn_s[tt][i0 + e], y1, y2);
-        x[e] = __bfloat162float(__float2bfloat16_rn(lane < 16 ? y1 : y2));
-      }
+      rope_row4(x, lane, cs_s[tt], sn_s[tt]);
       if (ko) {
         uint2 o2;
         o2.x = pack_bf16x2(x[0], x[1]);
@@ -288,6 +296,177 @@ cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s) {
   const int64_t blocks = (a.tokens + kTok - 1) / kTok;
   kv_append_int8_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, f);
   return cudaGetLastError();
+}
+
+// RoPE fused into the e4m3 quantisation of the FP8 prefill's inputs.  Each
+// (token, head) row of 128 values is rotated and rounded to bf16 exactly as
+// rope_apply stores it, then quantised exactly as quant_fp8_rows /
+// quant_fp8_heads quantise a bf16 row: scale = max|x| / 448, code =
+// e4m3(x / scale) in fp32, ties to even, saturating; an all-zero group has
+// scale 0 and codes 0.  The input is not modified.
+//
+// The kernels take rope_kernel's layout: a block holds NT tokens
+// (their angles computed once, into shared memory) and a thread one 16-byte
+// chunk c of the first half of a (token, head) row together with the partner
+// chunk of the second half, so each RoPE pair is in one thread's registers.
+// Eight consecutive lanes hold one row; its maximum takes three shuffles.
+// NT * heads is a multiple of 4, so every warp covers whole rows and runs the
+// loop the same number of times: rows past the last token load nothing and
+// store nothing, but still take part in the shuffles.
+struct RowChunk {
+  float a[8], b[8];  // dims 8c..8c+7 and 64+8c..64+8c+7, rotated and rounded to bf16
+};
+
+template <int NT>
+__device__ __forceinline__ bool rope_chunk(const __nv_bfloat16* __restrict__ x, int64_t t0, int64_t tokens,
+                                           int heads, int it, const float (*cs_s)[64], const float (*sn_s)[64],
+                                           RowChunk& r, int64_t& row) {
+  const int c = it & 7, rr = it >> 3, tt = rr / heads;
+  const int64_t t = t0 + tt;
+  row = t * heads + rr % heads;
+  const bool ok = t < tokens;
+  uint4 u1 = make_uint4(0u, 0u, 0u, 0u), u2 = u1;
+  if (ok) {
+    u1 = __ldg(reinterpret_cast<const uint4*>(x + row * 128 + 8 * c));
+    u2 = __ldg(reinterpret_cast<const uint4*>(x + row * 128 + 64 + 8 * c));
+  }
+  const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w}, w2[4] = {u2.x, u2.y, u2.z, u2.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float x1 = __uint_as_float((e & 1) ? (w1[e >> 1] & 0xffff0000u) : (w1[e >> 1] << 16));
+    const float x2 = __uint_as_float((e & 1) ? (w2[e >> 1] & 0xffff0000u) : (w2[e >> 1] << 16));
+    float y1, y2;
+    rope_rotate(x1, x2, cs_s[tt][8 * c + e], sn_s[tt][8 * c + e], y1, y2);
+    r.a[e] = __bfloat162float(__float2bfloat16_rn(y1));
+    r.b[e] = __bfloat162float(__float2bfloat16_rn(y2));
+  }
+  return ok;
+}
+
+__device__ __forceinline__ float chunk_amax(const RowChunk& r) {
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmax3(m, fabsf(r.a[e]), fabsf(r.b[e]));
+#pragma unroll
+  for (int o = 4; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+template <bool FAST>
+__device__ __forceinline__ void chunk_codes(const RowChunk& r, float sc, float rc, uint2& a, uint2& b) {
+  a.x = e4m3x4_div<FAST>(r.a[0], r.a[1], r.a[2], r.a[3], sc, rc);
+  a.y = e4m3x4_div<FAST>(r.a[4], r.a[5], r.a[6], r.a[7], sc, rc);
+  b.x = e4m3x4_div<FAST>(r.b[0], r.b[1], r.b[2], r.b[3], sc, rc);
+  b.y = e4m3x4_div<FAST>(r.b[4], r.b[5], r.b[6], r.b[7], sc, rc);
+}
+
+__device__ __forceinline__ void chunk_store(const RowChunk& r, float sc, uint8_t* row_codes, int c) {
+  uint2 a = make_uint2(0u, 0u), b = a;
+  if (sc >= kFastDivMinScale)
+    chunk_codes<true>(r, sc, __frcp_rn(sc), a, b);
+  else if (sc != 0.0f)
+    chunk_codes<false>(r, sc, 0.f, a, b);
+  *reinterpret_cast<uint2*>(row_codes + 8 * c) = a;
+  *reinterpret_cast<uint2*>(row_codes + 64 + 8 * c) = b;
+}
+
+// One scale per row (the queries).
+template <int NT>
+__global__ void __launch_bounds__(256) rope_quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t tokens,
+                                                              int heads, const int32_t* __restrict__ pos,
+                                                              const InvFreq f, uint8_t* __restrict__ codes,
+                                                              float* __restrict__ scales) {
+  __shared__ __align__(16) float cs_s[NT][64], sn_s[NT][64];
+  const int64_t t0 = (int64_t)blockIdx.x * NT;
+  angle_tables<NT, 64>(cs_s, sn_s, t0, tokens, 64, pos, f);
+  const int items = NT * heads * 8;
+#pragma unroll 2
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    RowChunk r;
+    int64_t row;
+    const bool ok = rope_chunk<NT>(x, t0, tokens, heads, it, cs_s, sn_s, r, row);
+    const float sc = chunk_amax(r) / 448.0f;
+    if (ok) {
+      chunk_store(r, sc, codes + row * 128, it & 7);
+      if ((it & 7) == 0) scales[row] = sc;
+    }
+  }
+}
+
+// One scale per head over all tokens (the keys), pass 1: max |rotated x| per
+// head, gathered in shared memory and folded into amax_bits[head] (the bits of
+// a non-negative float order like the integers) with one atomic per block.
+template <int NT>
+__global__ void __launch_bounds__(256) rope_amax_heads_kernel(const __nv_bfloat16* __restrict__ x, int64_t tokens,
+                                                              int heads, const int32_t* __restrict__ pos,
+                                                              const InvFreq f, unsigned* __restrict__ amax_bits) {
+  __shared__ __align__(16) float cs_s[NT][64], sn_s[NT][64];
+  __shared__ unsigned hmax[kMaxQuantHeads];
+  for (int h = threadIdx.x; h < heads; h += blockDim.x) hmax[h] = 0u;
+  const int64_t t0 = (int64_t)blockIdx.x * NT;
+  angle_tables<NT, 64>(cs_s, sn_s, t0, tokens, 64, pos, f);  // its barrier also publishes hmax
+  const int items = NT * heads * 8;
+#pragma unroll 2
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    RowChunk r;
+    int64_t row;
+    const bool ok = rope_chunk<NT>(x, t0, tokens, heads, it, cs_s, sn_s, r, row);
+    const float m = chunk_amax(r);  // 0 for rows past the end
+    if (ok && (it & 7) == 0) atomicMax(&hmax[(it >> 3) % heads], __float_as_uint(m));
+  }
+  __syncthreads();
+  for (int h = threadIdx.x; h < heads; h += blockDim.x)
+    if (hmax[h]) atomicMax(amax_bits + h, hmax[h]);
+}
+
+// Pass 2: codes with the head's scale, row layout; block 0 also writes the scales.
+template <int NT>
+__global__ void __launch_bounds__(256) rope_quant_heads_kernel(const __nv_bfloat16* __restrict__ x, int64_t tokens,
+                                                               int heads, const int32_t* __restrict__ pos,
+                                                               const InvFreq f, const unsigned* __restrict__ amax_bits,
+                                                               uint8_t* __restrict__ codes, float* __restrict__ scales) {
+  __shared__ __align__(16) float cs_s[NT][64], sn_s[NT][64];
+  const int64_t t0 = (int64_t)blockIdx.x * NT;
+  angle_tables<NT, 64>(cs_s, sn_s, t0, tokens, 64, pos, f);
+  if (blockIdx.x == 0)
+    for (int h = threadIdx.x; h < heads; h += blockDim.x) scales[h] = __uint_as_float(amax_bits[h]) / 448.0f;
+  const int items = NT * heads * 8;
+#pragma unroll 2
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    RowChunk r;
+    int64_t row;
+    if (rope_chunk<NT>(x, t0, tokens, heads, it, cs_s, sn_s, r, row))
+      chunk_store(r, __uint_as_float(__ldg(amax_bits + (it >> 3) % heads)) / 448.0f, codes + row * 128, it & 7);
+  }
+}
+
+template <int NT>
+static cudaError_t rope_quant_launch(const __nv_bfloat16* x, int64_t tokens, int heads, const int32_t* positions,
+                                     const InvFreq& f, void* codes, float* scales, unsigned* amax_scratch,
+                                     cudaStream_t s) {
+  const unsigned blocks = (unsigned)((tokens + NT - 1) / NT);
+  if (!amax_scratch) {
+    rope_quant_rows_kernel<NT><<<blocks, 256, 0, s>>>(x, tokens, heads, positions, f, (uint8_t*)codes, scales);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned) * heads, s);
+  if (e != cudaSuccess) return e;
+  rope_amax_heads_kernel<NT><<<blocks, 256, 0, s>>>(x, tokens, heads, positions, f, amax_scratch);
+  rope_quant_heads_kernel<NT><<<blocks, 256, 0, s>>>(x, tokens, heads, positions, f, amax_scratch,
+                                                     (uint8_t*)codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_quant_fp8(const void* x, int64_t tokens, int heads, const int32_t* positions, double base,
+                                  void* codes, float* scales, unsigned* amax_scratch, cudaStream_t s) {
+  InvFreq f;
+  for (int i = 0; i < 64; ++i) f.v[i] = pow(base, -2.0 * (double)i / 128.0);
+  if (tokens == 0 || heads == 0) return cudaSuccess;
+  const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
+  // about 256 rows per block either way: few heads take more tokens per block
+  if (heads >= 64) return rope_quant_launch<4>(xb, tokens, heads, positions, f, codes, scales, amax_scratch, s);
+  if (heads >= 8) return rope_quant_launch<32>(xb, tokens, heads, positions, f, codes, scales, amax_scratch, s);
+  return rope_quant_launch<64>(xb, tokens, heads, positions, f, codes, scales, amax_scratch, s);
 }
 
 // cos and sin of every (token, pair) angle, interleaved [tokens][d/2][2] fp32:

@@ -167,6 +167,26 @@ ATTN_API int quant_fp8_heads(const void *x, int64_t tokens, int heads, int head_
                              unsigned *amax_scratch, int transposed, int64_t t_stride, void *stream);
 
 /*
+ * rope_quant_fp8_rows / rope_quant_fp8_heads -- RoPE (as rope_apply) fused into
+ * the e4m3 quantisation above, for unrotated queries and keys: each row is
+ * rotated at its absolute position and rounded to bf16 exactly as rope_apply
+ * stores it, then quantised exactly as quant_fp8_rows / quant_fp8_heads
+ * quantise that bf16 row.  The result equals rope_apply (on a copy) followed by
+ * quant_fp8_rows / quant_fp8_heads (row layout) bit for bit; x is not modified.
+ *
+ *  x          [tokens][heads][128] bf16, 16-byte aligned, unrotated.
+ *  positions  [tokens] int32 absolute positions; base > 0 (e.g. 10000).
+ *  codes      [tokens][heads][128] e4m3, 16-byte aligned.
+ *  scales     rows: [tokens][heads] fp32; heads: [heads] fp32.
+ *  amax_scratch (heads only): caller-owned [heads] unsigned; heads <= 256.
+ * Reads x once (rows) or twice (heads: the per-head maximum, then the codes).
+ */
+ATTN_API int rope_quant_fp8_rows(const void *x, int64_t tokens, int heads, int head_dim, const int32_t *positions,
+                                 double base, void *codes, float *scales, void *stream);
+ATTN_API int rope_quant_fp8_heads(const void *x, int64_t tokens, int heads, int head_dim, const int32_t *positions,
+                                  double base, void *codes, float *scales, unsigned *amax_scratch, void *stream);
+
+/*
  * attn_prefill -- exact causal GQA attention, FlashAttention-style tiled.
  *
  * Computes, for every query row of every sequence and every query head h in

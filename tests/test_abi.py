@@ -178,3 +178,39 @@ def test_kv_append_int8_rejects_bad_arguments(lib):
     assert call(ks=None) == ERR_ARG
     assert call(vs=8) == ERR_ALIGN
     assert call(T=0) == 0
+
+
+def test_quant_fp8_and_fp8_prefill_reject_bad_arguments(lib):
+    assert lib.quant_fp8_rows(16, 4, 2, 64, 16, 16, None) == ERR_SHAPE
+    assert lib.quant_fp8_rows(8, 4, 2, 128, 16, 16, None) == ERR_ALIGN
+    assert lib.quant_fp8_heads(16, 4, 2, 128, 16, 16, 16, 1, 8, None) == ERR_ARG     # t_stride < tokens
+    assert lib.quant_fp8_heads(16, 4, 2, 128, 16, 16, 16, 1, 20, None) == ERR_ARG    # not a multiple of 16
+    assert lib.quant_fp8_rows(16, 0, 2, 128, None, None, None) == 0
+    a = dict(q=16, qs=16, k=16, ks=16, vt=16, vs=16, vts=16, out=16, odt=0, lse=None, batch=1, cu_q=16, q_pos=16,
+             total_q=4, max_q=4, cu_k=16, k_pos=16, total_k=4, hq=8, hkv=2, d=128, h_lo=0, h_hi=8, scale=0.1,
+             causal=1, stream=None)
+
+    def call(**kw):
+        b = dict(a)
+        b.update(kw)
+        return lib.attn_prefill_fp8(*b.values())
+
+    assert call(d=64) == ERR_SHAPE
+    assert call(h_lo=1) == ERR_SHAPE
+    assert call(vts=8) == ERR_ARG          # v_t_stride < total_k
+    assert call(vts=24) == ERR_ARG         # not a multiple of 16
+    assert call(qs=None) == ERR_ARG
+    assert call(vt=8) == ERR_ALIGN
+    assert call(scale=0.0) == ERR_ARG
+    assert call(odt=7) == ERR_UNSUPPORTED
+    assert call(batch=0) == 0
+
+
+def test_rope_quant_fp8_rejects_bad_arguments(lib):
+    assert lib.rope_quant_fp8_rows(16, 4, 2, 64, 16, 1e4, 16, 16, None) == ERR_SHAPE
+    assert lib.rope_quant_fp8_rows(16, 4, 2, 128, 16, 0.0, 16, 16, None) == ERR_ARG   # base
+    assert lib.rope_quant_fp8_rows(16, 4, 2, 128, None, 1e4, 16, 16, None) == ERR_ARG  # positions
+    assert lib.rope_quant_fp8_rows(16, 4, 2, 128, 16, 1e4, 8, 16, None) == ERR_ALIGN
+    assert lib.rope_quant_fp8_rows(16, 0, 2, 128, None, 1e4, None, None, None) == 0
+    assert lib.rope_quant_fp8_heads(16, 4, 300, 128, 16, 1e4, 16, 16, 16, None) == ERR_SHAPE   # > 256 heads
+    assert lib.rope_quant_fp8_heads(16, 4, 8, 128, 16, 1e4, 16, 16, None, None) == ERR_ARG    # no scratch

@@ -858,6 +858,61 @@ def test_quant_fp8_rows_and_heads_match_oracle():
     assert (c_t.view(torch.uint8)[:, :, T:] == 0).all()   # the padding columns are zero codes
 
 
+
+
+def test_quant_fp8_codes_over_group_maxima_across_the_fp32_range():
+    """e4m3 codes bit-exact with the oracle's fp32 division x / scale over group
+    maxima spread across 2^-130..2^127 (the three-instruction division serves
+    scales from 2^-90 up, the full division below), with every other value a
+    random bf16 number no larger than the row's maximum, some of them subnormal."""
+    rows = 4096
+    g = torch.Generator().manual_seed(740)
+    expo = torch.randint(-130, 127, (rows, 1), generator=g).float()
+    amax = (torch.rand((rows, 1), generator=g) + 1.0) * torch.pow(2.0, expo)
+    frac = torch.rand((rows, 128), generator=g) * 2 - 1
+    frac[:, ::7] *= torch.pow(2.0, -torch.randint(0, 40, (rows, 19), generator=g).float())
+    x = (frac * amax).to(torch.bfloat16)
+    x[:, 0] = amax[:, 0].to(torch.bfloat16)
+    x = x.view(rows // 8, 8, 128)
+    codes, scales = atc.quant_fp8_rows(x.to(DEV))
+    atc.attn_device_status()
+    want, wsc = oracle.quant_e4m3(synth.as_f64(x), [0, 1])
+    np.testing.assert_array_equal(scales.cpu().numpy(), wsc)
+    np.testing.assert_array_equal(codes.float().cpu().numpy(), want)
+
+def test_rope_quant_fp8_equals_rope_then_quant_and_matches_oracle():
+    """The fused RoPE + e4m3 quantisation equals rope_apply followed by
+    quant_fp8_rows / quant_fp8_heads bit for bit, leaves its input alone, and is
+    within one e4m3 step of the oracle's quantisation of its own rotation (the
+    rotations differ by at most one bf16 ulp in under 1% of elements)."""
+    T, H = 301, 8
+    x = synth.randn((T, H, 128), 720, 0.7071)
+    pos = synth.positions([T], [99000])
+    xd, posd = x.to(DEV), torch.from_numpy(pos).to(DEV)
+    x0 = xd.clone()
+    c_r, s_r = atc.rope_quant_fp8_rows(xd, posd)
+    c_h, s_h = atc.rope_quant_fp8_heads(xd, posd)
+    atc.attn_device_status()
+    assert torch.equal(xd, x0)
+    xr = xd.clone()
+    atc.rope_apply(xr, posd)
+    w_r, ws_r = atc.quant_fp8_rows(xr)
+    w_h, ws_h = atc.quant_fp8_heads(xr)
+    assert torch.equal(c_r.view(torch.uint8), w_r.view(torch.uint8)) and torch.equal(s_r, ws_r)
+    assert torch.equal(c_h.view(torch.uint8), w_h.view(torch.uint8)) and torch.equal(s_h, ws_h)
+    rot = rotated_bf16(x, pos)
+    for (codes, sc), axes in (((c_r, s_r), [0, 1]), ((c_h, s_h), [1])):
+        want, wsc = oracle.quant_e4m3(rot, axes)
+        got_sc = sc.cpu().numpy().astype(np.float64)
+        np.testing.assert_allclose(got_sc, wsc, rtol=2.0 ** -7)
+        shape = (T, H, 1) if axes == [0, 1] else (1, H, 1)
+        got_v = codes.float().cpu().numpy() * got_sc.reshape(shape)
+        want_v = want * wsc.astype(np.float64).reshape(shape)
+        step = 2.0 ** -3 * np.maximum(np.abs(got_v), np.abs(want_v)) + 2.0 ** -9 * wsc.reshape(shape)
+        assert (np.abs(got_v - want_v) <= step).all()
+        assert (codes.float().cpu().numpy() != want).mean() < 0.03
+
+
 # ------------------------------------------------------------------ FP8 (e4m3) prefill
 
 def _fp8_case(lens, hq, hkv, starts, seed, zero_k=False):
