@@ -111,11 +111,13 @@ __global__ void __launch_bounds__(256) quant_heads_kernel(const __nv_bfloat16* _
 // (the prefill's last K/V tile reads them, with weight 0).
 __global__ void __launch_bounds__(256) quant_heads_t_kernel(const __nv_bfloat16* __restrict__ x, int64_t tokens,
                                                             int heads, const unsigned* __restrict__ amax_bits,
-                                                            uint8_t* __restrict__ codes_t, int64_t t_stride) {
+                                                            uint8_t* __restrict__ codes_t, int64_t t_stride,
+                                                            float* __restrict__ scales) {
   __shared__ uint8_t tile[128][33];  // [dim][token], padded
   const int64_t t0 = (int64_t)blockIdx.x * 32;
   const int h = blockIdx.y;
   const float s = __uint_as_float(__ldg(amax_bits + h)) / 448.0f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) scales[h] = s;
   // read: 32 tokens x 128 dims, 16 threads per token row (8 values each)
   for (int i = threadIdx.x; i < 32 * 16; i += blockDim.x) {
     const int tt = i >> 4, c = i & 15;
@@ -170,12 +172,12 @@ cudaError_t launch_quant_fp8_heads(const void* x, int64_t tokens, int heads, voi
   if (transposed) {
     dim3 grid((unsigned)((t_stride + 31) / 32), (unsigned)heads);
     q8::quant_heads_t_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)x, tokens, heads, amax_scratch,
-                                                  (uint8_t*)codes, t_stride);
+                                                  (uint8_t*)codes, t_stride, scales);
   } else {
     q8::quant_heads_kernel<<<blocks, 256, 0, s>>>((const __nv_bfloat16*)x, tokens, heads, amax_scratch,
                                                   (uint8_t*)codes);
+    q8::head_scales_kernel<<<(heads + 127) / 128, 128, 0, s>>>(amax_scratch, heads, scales);
   }
-  q8::head_scales_kernel<<<(heads + 127) / 128, 128, 0, s>>>(amax_scratch, heads, scales);
   return cudaGetLastError();
 }
 

@@ -5,14 +5,34 @@
 // head of those tokens.  A thread rotates one 16-byte vector of the first half
 // of a head together with the matching vector of the second half; consecutive
 // threads take consecutive vectors, so a warp covers whole 128-byte segments.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace attn {
 
+// The rotation frequencies as fractions of a turn per position step:
+// theta_i = base^(-2i/d) / (2 pi), held as theta_i * 2^64 in a 64-bit integer
+// (i < d/2 <= 128).  The angle of position p is then p * theta_i turns, and its
+// fractional part -- all a rotation needs -- is the low 64 bits of the integer
+// product p * turns[i], exactly.
 struct InvFreq {
-  double v[128];  // base^(-2i/d), i < d/2 <= 128
+  uint64_t turns[128];
 };
+
+// theta_i in units of 2^-64 turns, from the fp64 frequency (53 significant
+// bits; the product with a 32-bit position keeps the phase to about 2^-22
+// relative, as an fp64 angle would).  base <= 0 gives 0: no rotation.
+static InvFreq make_inv_freq(double base, int head_dim) {
+  constexpr double kTwoPi = 6.283185307179586476925286766559;
+  InvFreq f;
+  for (int i = 0; i < 128; ++i) f.turns[i] = 0;
+  if (base > 0.0)
+    for (int i = 0; i < head_dim / 2 && i < 128; ++i)
+      f.turns[i] = (uint64_t)ldexp(pow(base, -2.0 * (double)i / (double)head_dim) / kTwoPi, 64);
+  return f;
+}
 
 template <typename T>
 struct Vec;
@@ -32,22 +52,22 @@ __device__ __forceinline__ void from_f(float x, float& y) { y = x; }
 
 constexpr int kTok = 4;  // tokens per block
 
-// cos and sin of pos * base^(-2i/d) for the block's kTok tokens, i < d/2, into
-// shared memory.  The angle is reduced modulo 2 pi in fp64, then sincosf runs
-// on the reduced fp32 angle.  Every kernel that rotates keys calls this, so
-// their results agree bit for bit.
+// cos and sin of pos * base^(-2i/d) for the block's NT tokens, i < d/2, into
+// shared memory.  The angle is reduced modulo one turn exactly, in integers
+// (InvFreq); its top 32 bits, as a signed fraction of a turn in [-1/2, 1/2),
+// go to sincospif.  No fp64 arithmetic, which runs at a small fraction of the
+// fp32 rate on this GPU.  Every kernel that rotates calls this, so their
+// results agree bit for bit.
 template <int NT = kTok, int W = 128>
 __device__ __forceinline__ void angle_tables(float (*cs_s)[W], float (*sn_s)[W], int64_t t0, int64_t tokens,
                                              int half, const int32_t* __restrict__ pos, const InvFreq& f) {
-  constexpr double kTwoPi = 6.283185307179586476925286766559;
-  constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
   for (int i = threadIdx.x; i < NT * half; i += blockDim.x) {
     const int tt = i / half, ii = i % half;
     const int64_t t = t0 + tt;
     if (t < tokens) {
-      const double a = (double)__ldg(pos + t) * f.v[ii];
-      const double r = fma(-rint(a * kInvTwoPi), kTwoPi, a);
-      sincosf((float)r, &sn_s[tt][ii], &cs_s[tt][ii]);
+      const uint64_t phase = (uint64_t)(int64_t)__ldg(pos + t) * f.turns[ii];  // mod 2^64: the fraction of a turn
+      const int32_t hi = (int32_t)(phase >> 32);                               // turns * 2^32 in [-2^31, 2^31)
+      sincospif((float)hi * 0x1p-31f, &sn_s[tt][ii], &cs_s[tt][ii]);           // angle = 2 pi * turns
     }
   }
   __syncthreads();
@@ -180,9 +200,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const In
 }
 
 cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s) {
-  InvFreq f;
-  const int half = a.head_dim / 2;
-  for (int i = 0; i < half; ++i) f.v[i] = a.base > 0.0 ? pow(a.base, -2.0 * (double)i / (double)a.head_dim) : 0.0;
+  const InvFreq f = make_inv_freq(a.base, a.head_dim);
   if (a.tokens == 0) return cudaSuccess;
   const int64_t blocks = (a.tokens + kTok - 1) / kTok;
   kv_append_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, f);
@@ -290,8 +308,7 @@ __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendLaunch a, con
 }
 
 cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s) {
-  InvFreq f;
-  for (int i = 0; i < 64; ++i) f.v[i] = a.base > 0.0 ? pow(a.base, -2.0 * (double)i / 128.0) : 0.0;
+  const InvFreq f = make_inv_freq(a.base, 128);
   if (a.tokens == 0) return cudaSuccess;
   const int64_t blocks = (a.tokens + kTok - 1) / kTok;
   kv_append_int8_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, f);
@@ -331,12 +348,17 @@ __device__ __forceinline__ bool rope_chunk(const __nv_bfloat16* __restrict__ x, 
     u2 = __ldg(reinterpret_cast<const uint4*>(x + row * 128 + 64 + 8 * c));
   }
   const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w}, w2[4] = {u2.x, u2.y, u2.z, u2.w};
+  // the chunk's 8 cos and 8 sin values as four 16-byte shared loads
+  const float4 ca = reinterpret_cast<const float4*>(cs_s[tt])[2 * c], cb = reinterpret_cast<const float4*>(cs_s[tt])[2 * c + 1];
+  const float4 sa = reinterpret_cast<const float4*>(sn_s[tt])[2 * c], sb = reinterpret_cast<const float4*>(sn_s[tt])[2 * c + 1];
+  const float cs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+  const float sn[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const float x1 = __uint_as_float((e & 1) ? (w1[e >> 1] & 0xffff0000u) : (w1[e >> 1] << 16));
     const float x2 = __uint_as_float((e & 1) ? (w2[e >> 1] & 0xffff0000u) : (w2[e >> 1] << 16));
     float y1, y2;
-    rope_rotate(x1, x2, cs_s[tt][8 * c + e], sn_s[tt][8 * c + e], y1, y2);
+    rope_rotate(x1, x2, cs[e], sn[e], y1, y2);
     r.a[e] = __bfloat162float(__float2bfloat16_rn(y1));
     r.b[e] = __bfloat162float(__float2bfloat16_rn(y2));
   }
@@ -396,6 +418,8 @@ __global__ void __launch_bounds__(256) rope_quant_rows_kernel(const __nv_bfloat1
 // One scale per head over all tokens (the keys), pass 1: max |rotated x| per
 // head, gathered in shared memory and folded into amax_bits[head] (the bits of
 // a non-negative float order like the integers) with one atomic per block.
+// The grid is persistent (a few blocks per SM, each taking groups of NT tokens
+// in turn), so the global atomics number blocks x heads, not tokens.
 template <int NT>
 __global__ void __launch_bounds__(256) rope_amax_heads_kernel(const __nv_bfloat16* __restrict__ x, int64_t tokens,
                                                               int heads, const int32_t* __restrict__ pos,
@@ -403,16 +427,20 @@ __global__ void __launch_bounds__(256) rope_amax_heads_kernel(const __nv_bfloat1
   __shared__ __align__(16) float cs_s[NT][64], sn_s[NT][64];
   __shared__ unsigned hmax[kMaxQuantHeads];
   for (int h = threadIdx.x; h < heads; h += blockDim.x) hmax[h] = 0u;
-  const int64_t t0 = (int64_t)blockIdx.x * NT;
-  angle_tables<NT, 64>(cs_s, sn_s, t0, tokens, 64, pos, f);  // its barrier also publishes hmax
   const int items = NT * heads * 8;
+  const int64_t groups = (tokens + NT - 1) / NT;
+  for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {
+    const int64_t t0 = g * NT;
+    __syncthreads();  // the previous group's angles are no longer read
+    angle_tables<NT, 64>(cs_s, sn_s, t0, tokens, 64, pos, f);  // its barrier also publishes hmax
 #pragma unroll 2
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
-    RowChunk r;
-    int64_t row;
-    const bool ok = rope_chunk<NT>(x, t0, tokens, heads, it, cs_s, sn_s, r, row);
-    const float m = chunk_amax(r);  // 0 for rows past the end
-    if (ok && (it & 7) == 0) atomicMax(&hmax[(it >> 3) % heads], __float_as_uint(m));
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+      RowChunk r;
+      int64_t row;
+      const bool ok = rope_chunk<NT>(x, t0, tokens, heads, it, cs_s, sn_s, r, row);
+      const float m = chunk_amax(r);  // 0 for rows past the end
+      if (ok && (it & 7) == 0) atomicMax(&hmax[(it >> 3) % heads], __float_as_uint(m));
+    }
   }
   __syncthreads();
   for (int h = threadIdx.x; h < heads; h += blockDim.x)
@@ -451,7 +479,11 @@ static cudaError_t rope_quant_launch(const __nv_bfloat16* x, int64_t tokens, int
   }
   cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned) * heads, s);
   if (e != cudaSuccess) return e;
-  rope_amax_heads_kernel<NT><<<blocks, 256, 0, s>>>(x, tokens, heads, positions, f, amax_scratch);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const unsigned pblocks = (unsigned)std::min<int64_t>(blocks, 2 * std::max(sms, 1));
+  rope_amax_heads_kernel<NT><<<pblocks, 256, 0, s>>>(x, tokens, heads, positions, f, amax_scratch);
   rope_quant_heads_kernel<NT><<<blocks, 256, 0, s>>>(x, tokens, heads, positions, f, amax_scratch,
                                                      (uint8_t*)codes, scales);
   return cudaGetLastError();
@@ -459,14 +491,13 @@ static cudaError_t rope_quant_launch(const __nv_bfloat16* x, int64_t tokens, int
 
 cudaError_t launch_rope_quant_fp8(const void* x, int64_t tokens, int heads, const int32_t* positions, double base,
                                   void* codes, float* scales, unsigned* amax_scratch, cudaStream_t s) {
-  InvFreq f;
-  for (int i = 0; i < 64; ++i) f.v[i] = pow(base, -2.0 * (double)i / 128.0);
+  const InvFreq f = make_inv_freq(base, 128);
   if (tokens == 0 || heads == 0) return cudaSuccess;
   const __nv_bfloat16* xb = (const __nv_bfloat16*)x;
-  // about 256 rows per block either way: few heads take more tokens per block
-  if (heads >= 64) return rope_quant_launch<4>(xb, tokens, heads, positions, f, codes, scales, amax_scratch, s);
-  if (heads >= 8) return rope_quant_launch<32>(xb, tokens, heads, positions, f, codes, scales, amax_scratch, s);
-  return rope_quant_launch<64>(xb, tokens, heads, positions, f, codes, scales, amax_scratch, s);
+  // blocks of 32-256 rows: few heads take more tokens per block
+  if (heads >= 32) return rope_quant_launch<4>(xb, tokens, heads, positions, f, codes, scales, amax_scratch, s);
+  if (heads >= 4) return rope_quant_launch<8>(xb, tokens, heads, positions, f, codes, scales, amax_scratch, s);
+  return rope_quant_launch<32>(xb, tokens, heads, positions, f, codes, scales, amax_scratch, s);
 }
 
 // cos and sin of every (token, pair) angle, interleaved [tokens][d/2][2] fp32:
@@ -486,9 +517,7 @@ __global__ void __launch_bounds__(256) rope_table_kernel(float2* __restrict__ cs
 
 cudaError_t launch_rope_table(float* cs_out, int64_t tokens, int head_dim, const int32_t* positions, double base,
                               cudaStream_t s) {
-  InvFreq f;
-  const int half = head_dim / 2;
-  for (int i = 0; i < half; ++i) f.v[i] = pow(base, -2.0 * (double)i / (double)head_dim);
+  const InvFreq f = make_inv_freq(base, head_dim);
   if (tokens == 0) return cudaSuccess;
   const int64_t blocks = (tokens + kTok - 1) / kTok;
   rope_table_kernel<<<(unsigned)blocks, 256, 0, s>>>((float2*)cs_out, tokens, head_dim, positions, f);
@@ -496,9 +525,7 @@ cudaError_t launch_rope_table(float* cs_out, int64_t tokens, int head_dim, const
 }
 
 cudaError_t launch_rope(const RopeLaunch& a, cudaStream_t s) {
-  InvFreq f;
-  const int half = a.head_dim / 2;
-  for (int i = 0; i < half; ++i) f.v[i] = pow(a.base, -2.0 * (double)i / (double)a.head_dim);
+  const InvFreq f = make_inv_freq(a.base, a.head_dim);
   if (a.tokens == 0) return cudaSuccess;
   const int64_t blocks = (a.tokens + kTok - 1) / kTok;
   if (a.dtype == 0)

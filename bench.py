@@ -208,6 +208,30 @@ class Timer:
         return tot / steps, (sub / steps if inner else None)
 
 
+def graph_step_ms(timer, fn, steps, warmup):
+    """ms per step of `fn` captured once into a CUDA graph and replayed (the
+    launches of a step go to the GPU as one unit, with no host work between
+    them), timed like an eager step; None if the capture fails."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+    except Exception as e:  # noqa: BLE001 -- reported, and the eager number stands
+        print(f"graph capture failed: {e}", file=sys.stderr)
+        torch.cuda.synchronize()
+        return None
+    ms, _ = timer.run(lambda ev=(): g.replay(), steps, warmup)
+    del g
+    return ms
+
+
 def pipelined_e2e(atc, host_in, host_out, dev, pos, cu, seq, steps, warmup):
     """End-to-end time per step through the public API as a serving loop runs it:
     every step uploads its Q/K/V from pinned host memory, runs RoPE + attention and
@@ -309,7 +333,9 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
         if ev:
             ev[1].record()
 
-    ms, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
+    ms_eager, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
+    ms_graph = graph_step_ms(timer, step, args.steps, args.warmup)
+    ms = ms_graph if ms_graph is not None else ms_eager
     atc.attn_device_status()
     flops = wl.flops()
     # end to end through the public API: pinned host inputs in, O and LSE back out
@@ -339,6 +365,10 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
     traffic = profiled_traffic("prefill_tc_causal_8k.md", "prefill_tc.cu")
     res = {
         "ms_per_step": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
+        "launch": {"step": "CUDA graph of the step's 3 launches, replayed" if ms_graph is not None
+                   else "eager (graph capture failed)",
+                   "eager_ms_per_step": round(ms_eager, 4),
+                   "graph_ms_per_step": None if ms_graph is None else round(ms_graph, 4)},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_scope": "prefill_tc_kernel (ncu)",
                      "kernel": "attn::tc::prefill_tc_kernel", "kernel_ms": round(ms_kernel, 4),
@@ -390,8 +420,12 @@ def fp8_prefill_arm(wl, args, timer, peaks, peak_src, inputs=None):
         if ev:
             ev[1].record()
 
-    ms, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
-    ms_q, _ = timer.run(lambda ev=(): quant(), args.steps, args.warmup)
+    ms_eager, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
+    ms_graph = graph_step_ms(timer, step, args.steps, args.warmup)
+    ms = ms_graph if ms_graph is not None else ms_eager
+    ms_q = graph_step_ms(timer, quant, args.steps, args.warmup)
+    if ms_q is None:
+        ms_q, _ = timer.run(lambda ev=(): quant(), args.steps, args.warmup)
     atc.attn_device_status()
     flops = wl.flops()
     peak = 2.0 * peaks["bf16_tflops"]
@@ -402,6 +436,10 @@ def fp8_prefill_arm(wl, args, timer, peaks, peak_src, inputs=None):
         "workload": wl.name + " with e4m3 Q/K/V codes (RoPE fused into the quantisation + attention, O and LSE)",
         "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
         "steps": args.steps, "warmup": args.warmup, "dtype": "e4m3 operands, fp32 accumulation and softmax",
+        "launch": {"step": "CUDA graph of the step's 7 launches, replayed" if ms_graph is not None
+                   else "eager (graph capture failed)",
+                   "eager_ms_per_step": round(ms_eager, 4),
+                   "graph_ms_per_step": None if ms_graph is None else round(ms_graph, 4)},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic("prefill_tc_fp8_causal_8k.md", "prefill_tc.cu"),
@@ -773,7 +811,7 @@ def main():
                                 "head_dim": wl.d, "flops_per_step": res["flops"], "l2_flush": True,
                                 "parallelism": f"replicas x{ws}"},
                      "roofline": res["roofline"], "e2e": res["e2e"], "clocks": clocks,
-                     "gpu_launches": res["launches_per_step"] * args.steps})
+                     "launch": res["launch"], "gpu_launches": res["launches_per_step"] * args.steps})
     else:
         line.update({"value": dec["value"], "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
                      "warmup": args.warmup, "ms_per_step": dec["ms_per_step"], "higher_is_better": True,
