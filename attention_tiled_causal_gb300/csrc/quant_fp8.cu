@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(256) quant_heads_kernel(const __nv_bfloat16* _
                                                           uint8_t* __restrict__ codes) {
   const int64_t chunks = tokens * heads * 16;
   for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < chunks; c += (int64_t)gridDim.x * blockDim.x) {
-    const int h = (int)((c >> 4) % heads);
+    const int64_t rw = c >> 4;  // (token, head) row; 32-bit division while it fits
+    const int h = rw < 0x7fffffff ? (int)((uint32_t)rw % (uint32_t)heads) : (int)(rw % heads);
     const float s = __uint_as_float(__ldg(amax_bits + h)) / 448.0f;
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(x) + c);
     float v[4], u[4];

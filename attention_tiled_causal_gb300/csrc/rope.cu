@@ -207,52 +207,96 @@ cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// One cache row of 128 values (4 per lane of a warp) quantised to symmetric
-// int8: scale = max|x| / 127, code = x / scale rounded to the nearest integer
-// (ties to even) and clamped to [-127, 127], all in fp32; an all-zero row gets
-// scale 0 and codes 0.  The 128 codes go to dst (4 bytes per lane).
-__device__ __forceinline__ void quant_store_int8(const float (&x)[4], int lane, int8_t* dst, float* scale_dst) {
-  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float sc = amax / 127.0f;
-  uint32_t packed = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    float q = sc == 0.0f ? 0.0f : rintf(x[e] / sc);
-    q = fminf(fmaxf(q, -127.0f), 127.0f);
-    packed |= (uint32_t)(uint8_t)(int8_t)(int)q << (8 * e);
+// A thread's share of one (token, head) row of 128 values in the chunk-pair
+// layout: chunk c (dims 8c..8c+7) of the first half and its RoPE partner chunk
+// (dims 64+8c..64+8c+7) of the second half, as fp32.  Eight consecutive lanes
+// hold a row.
+struct RowChunk {
+  float a[8], b[8];
+};
+
+__device__ __forceinline__ void load_chunk(const __nv_bfloat16* __restrict__ rowp, int c, bool ok, RowChunk& r) {
+  uint4 u1 = make_uint4(0u, 0u, 0u, 0u), u2 = u1;
+  if (ok) {
+    u1 = __ldg(reinterpret_cast<const uint4*>(rowp + 8 * c));
+    u2 = __ldg(reinterpret_cast<const uint4*>(rowp + 64 + 8 * c));
   }
-  *reinterpret_cast<uint32_t*>(dst + 4 * lane) = packed;
-  if (lane == 0) *scale_dst = sc;
+  const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w}, w2[4] = {u2.x, u2.y, u2.z, u2.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    r.a[e] = __uint_as_float((e & 1) ? (w1[e >> 1] & 0xffff0000u) : (w1[e >> 1] << 16));
+    r.b[e] = __uint_as_float((e & 1) ? (w2[e >> 1] & 0xffff0000u) : (w2[e >> 1] << 16));
+  }
 }
 
-// The four values lane l of a warp holds, dims 4l..4l+3 of a 128-wide head
-// row, rotated exactly as rope_kernel rotates them (the RoPE partner of dim i
-// sits 16 lanes away) and rounded to bf16, the value rope_apply stores.
-__device__ __forceinline__ void rope_row4(float (&x)[4], int lane, const float* cs, const float* sn) {
-  const int i0 = 4 * (lane & 15);
+// Rotates the chunk pair exactly as rope_kernel rotates it and rounds to bf16,
+// the value rope_apply stores.  cs, sn: the token's 64 cos / sin values.
+__device__ __forceinline__ void rotate_chunk(RowChunk& r, const float* cs_row, const float* sn_row, int c) {
+  // the chunk's 8 cos and 8 sin values as four 16-byte shared loads
+  const float4 ca = reinterpret_cast<const float4*>(cs_row)[2 * c], cb = reinterpret_cast<const float4*>(cs_row)[2 * c + 1];
+  const float4 sa = reinterpret_cast<const float4*>(sn_row)[2 * c], sb = reinterpret_cast<const float4*>(sn_row)[2 * c + 1];
+  const float cs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+  const float sn[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float xp = __shfl_xor_sync(0xffffffffu, x[e], 16);
+  for (int e = 0; e < 8; ++e) {
     float y1, y2;
-    if (lane < 16)
-      rope_rotate(x[e], xp, cs[i0 + e], sn[i0 + e], y1, y2);
-    else
-      rope_rotate(xp, x[e], cs[i0 + e], sn[i0 + e], y1, y2);
-    x[e] = __bfloat162float(__float2bfloat16_rn(lane < 16 ? y1 : y2));
+    rope_rotate(r.a[e], r.b[e], cs[e], sn[e], y1, y2);
+    r.a[e] = __bfloat162float(__float2bfloat16_rn(y1));
+    r.b[e] = __bfloat162float(__float2bfloat16_rn(y2));
   }
 }
 
-// kv_append_kernel for an INT8 cache: one warp per (token, KV head), lane l
-// holding dims 4l..4l+3.  A key is rotated exactly as rope_kernel rotates it
-// (its RoPE partner sits 16 lanes away) and rounded to bf16 -- the value a
-// bf16 cache would hold -- before both rows are quantised.
+// max |x| over the row (the eight lanes holding it).
+__device__ __forceinline__ float chunk_amax(const RowChunk& r) {
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmax3(m, fabsf(r.a[e]), fabsf(r.b[e]));
+#pragma unroll
+  for (int o = 4; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+// Symmetric int8 codes of the chunk pair: code = x / sc rounded to the nearest
+// integer (ties to even) and clamped to [-127, 127], the quotient correctly
+// rounded in fp32 (div_rn_recip for normal scales); 0 for a zero scale.
+template <bool FAST>
+__device__ __forceinline__ uint32_t int8x4(const float* x, float sc, float rc) {
+  uint32_t p = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float q = rintf(FAST ? div_rn_recip(x[e], sc, rc) : x[e] / sc);
+    q = fminf(fmaxf(q, -127.0f), 127.0f);
+    p |= (uint32_t)(uint8_t)(int8_t)(int)q << (8 * e);
+  }
+  return p;
+}
+
+__device__ __forceinline__ void chunk_store_int8(const RowChunk& r, float sc, int8_t* row_codes, int c) {
+  uint2 a = make_uint2(0u, 0u), b = a;
+  if (sc >= kFastDivMinScale) {
+    const float rc = __frcp_rn(sc);
+    a = make_uint2(int8x4<true>(r.a, sc, rc), int8x4<true>(r.a + 4, sc, rc));
+    b = make_uint2(int8x4<true>(r.b, sc, rc), int8x4<true>(r.b + 4, sc, rc));
+  } else if (sc != 0.0f) {
+    a = make_uint2(int8x4<false>(r.a, sc, 0.f), int8x4<false>(r.a + 4, sc, 0.f));
+    b = make_uint2(int8x4<false>(r.b, sc, 0.f), int8x4<false>(r.b + 4, sc, 0.f));
+  }
+  *reinterpret_cast<uint2*>(row_codes + 8 * c) = a;
+  *reinterpret_cast<uint2*>(row_codes + 64 + 8 * c) = b;
+}
+
+// kv_append_kernel for an INT8 cache, in the chunk-pair layout: a block takes
+// kAppendTok tokens, first every key row (rotated and rounded to bf16 -- the
+// value a bf16 cache would hold), then every value row, each quantised with one
+// fp32 scale per cache row: scale = max|x| / 127.  NT * heads * 8 is a multiple
+// of 32, so a warp handles only keys or only values, and whole rows.
+constexpr int kAppendTok = 8;
+
 __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendLaunch a, const InvFreq f) {
-  __shared__ float cs_s[kTok][128], sn_s[kTok][128];
-  __shared__ int64_t slot_s[kTok];
-  const int64_t t0 = (int64_t)blockIdx.x * kTok;
-  if (threadIdx.x < kTok) {
+  __shared__ __align__(16) float cs_s[kAppendTok][64], sn_s[kAppendTok][64];
+  __shared__ int64_t slot_s[kAppendTok];
+  const int64_t t0 = (int64_t)blockIdx.x * kAppendTok;
+  if (threadIdx.x < kAppendTok) {
     const int64_t t = t0 + threadIdx.x;
     int64_t sl = -1;
     if (t < a.tokens) {
@@ -265,52 +309,44 @@ __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendLaunch a, con
     slot_s[threadIdx.x] = sl;
   }
   const bool rotate = a.base > 0.0;
-  if (rotate) angle_tables(cs_s, sn_s, t0, a.tokens, 64, a.positions, f);
+  if (rotate) angle_tables<kAppendTok, 64>(cs_s, sn_s, t0, a.tokens, 64, a.positions, f);
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
   const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
-  int8_t* kc = (int8_t*)a.k_cache;
-  int8_t* vc = (int8_t*)a.v_cache;
   __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
-  for (int w = warp; w < kTok * a.heads; w += blockDim.x / 32) {
-    const int tt = w / a.heads, h = w % a.heads;
+  const int items = kAppendTok * a.heads * 8;
+  for (int it = threadIdx.x; it < 2 * items; it += blockDim.x) {
+    const bool is_v = it >= items;
+    const int jt = is_v ? it - items : it;
+    const int c = jt & 7, rr = jt >> 3, tt = rr / a.heads, h = rr % a.heads;
     const int64_t sl = slot_s[tt];
-    if (sl < 0) continue;
-    const int64_t t = t0 + tt;
-    const int64_t src = (t * a.heads + h) * 128 + 4 * lane;
-    const int64_t row = (int64_t)h * a.cache_rows + sl;
-    float x[4];
-    {
-      const uint2 w2 = __ldg(reinterpret_cast<const uint2*>(kn + src));
-      x[0] = __uint_as_float(w2.x << 16), x[1] = __uint_as_float(w2.x & 0xffff0000u);
-      x[2] = __uint_as_float(w2.y << 16), x[3] = __uint_as_float(w2.y & 0xffff0000u);
+    const bool ok = sl >= 0;  // tokens past the end carry slot -1
+    const int64_t src = ((t0 + tt) * a.heads + h) * 128;
+    RowChunk r;
+    load_chunk((is_v ? vn : kn) + src, c, ok, r);
+    if (!is_v && rotate) rotate_chunk(r, cs_s[tt], sn_s[tt], c);
+    if (!is_v && ko && ok) {
+      uint4 o1, o2;
+      o1.x = pack_bf16x2(r.a[0], r.a[1]), o1.y = pack_bf16x2(r.a[2], r.a[3]);
+      o1.z = pack_bf16x2(r.a[4], r.a[5]), o1.w = pack_bf16x2(r.a[6], r.a[7]);
+      o2.x = pack_bf16x2(r.b[0], r.b[1]), o2.y = pack_bf16x2(r.b[2], r.b[3]);
+      o2.z = pack_bf16x2(r.b[4], r.b[5]), o2.w = pack_bf16x2(r.b[6], r.b[7]);
+      *reinterpret_cast<uint4*>(ko + src + 8 * c) = o1;
+      *reinterpret_cast<uint4*>(ko + src + 64 + 8 * c) = o2;
     }
-    if (rotate) {
-      rope_row4(x, lane, cs_s[tt], sn_s[tt]);
-      if (ko) {
-        uint2 o2;
-        o2.x = pack_bf16x2(x[0], x[1]);
-        o2.y = pack_bf16x2(x[2], x[3]);
-        *reinterpret_cast<uint2*>(ko + src) = o2;
-      }
-    } else if (ko) {
-      *reinterpret_cast<uint2*>(ko + src) = __ldg(reinterpret_cast<const uint2*>(kn + src));
+    const float sc = chunk_amax(r) / 127.0f;
+    if (ok) {
+      const int64_t row = (int64_t)h * a.cache_rows + sl;
+      chunk_store_int8(r, sc, (int8_t*)(is_v ? a.v_cache : a.k_cache) + row * 128, c);
+      if (c == 0) (is_v ? a.v_scale : a.k_scale)[row] = sc;
     }
-    quant_store_int8(x, lane, kc + row * 128, a.k_scale + row);
-    {
-      const uint2 w2 = __ldg(reinterpret_cast<const uint2*>(vn + src));
-      x[0] = __uint_as_float(w2.x << 16), x[1] = __uint_as_float(w2.x & 0xffff0000u);
-      x[2] = __uint_as_float(w2.y << 16), x[3] = __uint_as_float(w2.y & 0xffff0000u);
-    }
-    quant_store_int8(x, lane, vc + row * 128, a.v_scale + row);
   }
 }
 
 cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s) {
   const InvFreq f = make_inv_freq(a.base, 128);
   if (a.tokens == 0) return cudaSuccess;
-  const int64_t blocks = (a.tokens + kTok - 1) / kTok;
+  const int64_t blocks = (a.tokens + kAppendTok - 1) / kAppendTok;
   kv_append_int8_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, f);
   return cudaGetLastError();
 }
@@ -330,10 +366,6 @@ cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s) {
 // NT * heads is a multiple of 4, so every warp covers whole rows and runs the
 // loop the same number of times: rows past the last token load nothing and
 // store nothing, but still take part in the shuffles.
-struct RowChunk {
-  float a[8], b[8];  // dims 8c..8c+7 and 64+8c..64+8c+7, rotated and rounded to bf16
-};
-
 template <int NT>
 __device__ __forceinline__ bool rope_chunk(const __nv_bfloat16* __restrict__ x, int64_t t0, int64_t tokens,
                                            int heads, int it, const float (*cs_s)[64], const float (*sn_s)[64],
@@ -342,36 +374,9 @@ __device__ __forceinline__ bool rope_chunk(const __nv_bfloat16* __restrict__ x, 
   const int64_t t = t0 + tt;
   row = t * heads + rr % heads;
   const bool ok = t < tokens;
-  uint4 u1 = make_uint4(0u, 0u, 0u, 0u), u2 = u1;
-  if (ok) {
-    u1 = __ldg(reinterpret_cast<const uint4*>(x + row * 128 + 8 * c));
-    u2 = __ldg(reinterpret_cast<const uint4*>(x + row * 128 + 64 + 8 * c));
-  }
-  const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w}, w2[4] = {u2.x, u2.y, u2.z, u2.w};
-  // the chunk's 8 cos and 8 sin values as four 16-byte shared loads
-  const float4 ca = reinterpret_cast<const float4*>(cs_s[tt])[2 * c], cb = reinterpret_cast<const float4*>(cs_s[tt])[2 * c + 1];
-  const float4 sa = reinterpret_cast<const float4*>(sn_s[tt])[2 * c], sb = reinterpret_cast<const float4*>(sn_s[tt])[2 * c + 1];
-  const float cs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-  const float sn[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float x1 = __uint_as_float((e & 1) ? (w1[e >> 1] & 0xffff0000u) : (w1[e >> 1] << 16));
-    const float x2 = __uint_as_float((e & 1) ? (w2[e >> 1] & 0xffff0000u) : (w2[e >> 1] << 16));
-    float y1, y2;
-    rope_rotate(x1, x2, cs[e], sn[e], y1, y2);
-    r.a[e] = __bfloat162float(__float2bfloat16_rn(y1));
-    r.b[e] = __bfloat162float(__float2bfloat16_rn(y2));
-  }
+  load_chunk(x + row * 128, c, ok, r);
+  rotate_chunk(r, cs_s[tt], sn_s[tt], c);
   return ok;
-}
-
-__device__ __forceinline__ float chunk_amax(const RowChunk& r) {
-  float m = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) m = fmax3(m, fabsf(r.a[e]), fabsf(r.b[e]));
-#pragma unroll
-  for (int o = 4; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  return m;
 }
 
 template <bool FAST>

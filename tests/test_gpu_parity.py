@@ -101,19 +101,28 @@ def test_rope_strided_token_rows():
 # ------------------------------------------------------------------ LSE merge
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_lse_merge_matches_oracle(out_dtype):
-    P, R, H, d = 5, 37, 6, 128
-    rng = np.random.default_rng(7)
+@pytest.mark.parametrize("P", [1, 2, 3, 5, 16, 40])
+def test_lse_merge_matches_oracle(out_dtype, P):
+    """Part counts that take each merge kernel (2 or fewer, 4 or fewer, 32 or
+    fewer, more), a ragged number of (row, head) items, an empty part whose
+    output rows hold NaN (a part with LSE -inf contributes nothing, whatever its
+    rows hold) and a row with no part at all."""
+    R, H, d = 37, 6, 128
+    rng = np.random.default_rng(7 + P)
     po = rng.normal(0, 1, (P, R, H, d)).astype(np.float32)
     pl = rng.normal(0, 3, (P, R, H)).astype(np.float32)
-    pl[1, :, 0] = -np.inf          # an empty part
+    pl[P // 2, :, 0] = -np.inf      # an empty part
     pl[:, 3, 2] = -np.inf          # a row with no part at all
     want_o, want_l = oracle.lse_merge(po.astype(np.float64), pl.astype(np.float64))
+    po_gpu = po.copy()
+    po_gpu[P // 2, :, 0] = np.nan   # never read into the sum
+    po_gpu[:, 3, 2] = np.nan
     out = torch.empty((R, H, d), dtype=out_dtype, device=DEV)
     lse = torch.empty((R, H), dtype=torch.float32, device=DEV)
-    atc.attn_lse_merge(torch.from_numpy(po).to(DEV), torch.from_numpy(pl).to(DEV), out, lse)
-    tol = 1e-5 if out_dtype == torch.float32 else 8e-3
-    check(out, lse, want_o, want_l, tol_max=tol, tol_mean=tol, tol_lse=1e-5, what="merge")
+    atc.attn_lse_merge(torch.from_numpy(po_gpu).to(DEV), torch.from_numpy(pl).to(DEV), out, lse)
+    # bf16 output: rounding to nearest costs at most half an ulp, 2^-8 of |O| (relative to its binade)
+    tol = 1e-5 if out_dtype == torch.float32 else 2.0 ** -8 * np.abs(want_o).max() + 1e-5
+    check(out, lse, want_o, want_l, tol_max=tol, tol_mean=tol, tol_lse=1e-5, what=f"merge P={P}")
     assert torch.all(out[3, 2] == 0)
 
 
