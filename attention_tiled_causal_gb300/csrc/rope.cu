@@ -1,6 +1,6 @@
 // RoPE at absolute positions, in place (Ulysses page, sections 3.2 and 5.3).
 //
-// Each block takes kTok consecutive tokens: it first computes their cos/sin
+// Each block takes NT consecutive tokens: it first computes their cos/sin
 // tables (d/2 angles per token, once) into shared memory, then streams every
 // head of those tokens.  A thread rotates one 16-byte vector of the first half
 // of a head together with the matching vector of the second half; consecutive
@@ -73,17 +73,17 @@ __device__ __forceinline__ void angle_tables(float (*cs_s)[W], float (*sn_s)[W],
   __syncthreads();
 }
 
-template <typename T>
+template <typename T, int NT>
 __global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t tokens, int heads, int d,
                                                    int64_t stride_tok, const int32_t* __restrict__ pos,
                                                    const InvFreq f) {
   constexpr int V = Vec<T>::N;
-  __shared__ float cs_s[kTok][128], sn_s[kTok][128];
+  __shared__ float cs_s[NT][128], sn_s[NT][128];
   const int half = d / 2;
   const int chunks = half / V;
-  const int64_t t0 = (int64_t)blockIdx.x * kTok;
-  angle_tables(cs_s, sn_s, t0, tokens, half, pos, f);
-  const int items = kTok * heads * chunks;
+  const int64_t t0 = (int64_t)blockIdx.x * NT;
+  angle_tables<NT, 128>(cs_s, sn_s, t0, tokens, half, pos, f);
+  const int items = NT * heads * chunks;
 #pragma unroll 4
   for (int w = threadIdx.x; w < items; w += blockDim.x) {
     const int c = w % chunks;
@@ -115,19 +115,20 @@ __global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t to
 }
 
 // New tokens' K and V into the head-major paged cache (SGLang page, sections
-// 2.1-2.2), K rotated as rope_kernel rotates it.  Each block takes kTok tokens:
+// 2.1-2.2), K rotated as rope_kernel rotates it.  Each block takes NT tokens:
 // angle tables first, then one 16-byte vector of the first half of a key head
 // with its partner vector of the second half per thread (rotated, written to
 // the cache row and optionally to k_rot_out), then the value rows copied as
 // 16-byte vectors.  Slots are checked per token: -1 skips, out of range is
 // recorded and skipped.
+template <int NT>
 __global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const InvFreq f) {
   constexpr int V = 8;  // bf16 per 16-byte vector
-  __shared__ float cs_s[kTok][128], sn_s[kTok][128];
-  __shared__ int64_t slot_s[kTok];
+  __shared__ float cs_s[NT][128], sn_s[NT][128];
+  __shared__ int64_t slot_s[NT];
   const int d = a.head_dim, half = d / 2;
-  const int64_t t0 = (int64_t)blockIdx.x * kTok;
-  if (threadIdx.x < kTok) {
+  const int64_t t0 = (int64_t)blockIdx.x * NT;
+  if (threadIdx.x < NT) {
     const int64_t t = t0 + threadIdx.x;
     int64_t sl = -1;
     if (t < a.tokens) {
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const In
     slot_s[threadIdx.x] = sl;
   }
   const bool rotate = a.base > 0.0;
-  if (rotate) angle_tables(cs_s, sn_s, t0, a.tokens, half, a.positions, f);
+  if (rotate) angle_tables<NT, 128>(cs_s, sn_s, t0, a.tokens, half, a.positions, f);
   __syncthreads();
   const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
   const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const In
   __nv_bfloat16* vc = (__nv_bfloat16*)a.v_cache;
   __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
   const int chunks = half / V;
-  const int kitems = kTok * a.heads * chunks;
+  const int kitems = NT * a.heads * chunks;
   for (int w = threadIdx.x; w < kitems; w += blockDim.x) {
     const int c = w % chunks;
     const int h = (w / chunks) % a.heads;
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const In
     }
   }
   const int vchunks = d / V;
-  const int vitems = kTok * a.heads * vchunks;
+  const int vitems = NT * a.heads * vchunks;
   for (int w = threadIdx.x; w < vitems; w += blockDim.x) {
     const int c = w % vchunks;
     const int h = (w / vchunks) % a.heads;
@@ -202,8 +203,15 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const In
 cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s) {
   const InvFreq f = make_inv_freq(a.base, a.head_dim);
   if (a.tokens == 0) return cudaSuccess;
-  const int64_t blocks = (a.tokens + kTok - 1) / kTok;
-  kv_append_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, f);
+  // enough rows per block that the angle tables and the block's start-up are
+  // amortised: 16 tokens for up to 16 heads, else 4
+  if (a.heads <= 16) {
+    const int64_t blocks = (a.tokens + 15) / 16;
+    kv_append_kernel<16><<<(unsigned)blocks, 256, 0, s>>>(a, f);
+  } else {
+    const int64_t blocks = (a.tokens + kTok - 1) / kTok;
+    kv_append_kernel<kTok><<<(unsigned)blocks, 256, 0, s>>>(a, f);
+  }
   return cudaGetLastError();
 }
 
@@ -532,13 +540,24 @@ cudaError_t launch_rope_table(float* cs_out, int64_t tokens, int head_dim, const
 cudaError_t launch_rope(const RopeLaunch& a, cudaStream_t s) {
   const InvFreq f = make_inv_freq(a.base, a.head_dim);
   if (a.tokens == 0) return cudaSuccess;
+  // few heads: 16 tokens per block, so the angle tables are amortised over enough rows
+  if (a.heads <= 16) {
+    const int64_t blocks = (a.tokens + 15) / 16;
+    if (a.dtype == 0)
+      rope_kernel<__nv_bfloat16, 16><<<(unsigned)blocks, 256, 0, s>>>(
+          (__nv_bfloat16*)a.x, a.tokens, a.heads, a.head_dim, a.stride_token, a.positions, f);
+    else
+      rope_kernel<float, 16><<<(unsigned)blocks, 256, 0, s>>>((float*)a.x, a.tokens, a.heads, a.head_dim,
+                                                              a.stride_token, a.positions, f);
+    return cudaGetLastError();
+  }
   const int64_t blocks = (a.tokens + kTok - 1) / kTok;
   if (a.dtype == 0)
-    rope_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
+    rope_kernel<__nv_bfloat16, kTok><<<(unsigned)blocks, 256, 0, s>>>(
         (__nv_bfloat16*)a.x, a.tokens, a.heads, a.head_dim, a.stride_token, a.positions, f);
   else
-    rope_kernel<float><<<(unsigned)blocks, 256, 0, s>>>((float*)a.x, a.tokens, a.heads, a.head_dim,
-                                                        a.stride_token, a.positions, f);
+    rope_kernel<float, kTok><<<(unsigned)blocks, 256, 0, s>>>((float*)a.x, a.tokens, a.heads, a.head_dim,
+                                                              a.stride_token, a.positions, f);
   return cudaGetLastError();
 }
 
