@@ -1,7 +1,8 @@
 """Parity at the full workload sizes, in the launch configuration bench.py times.
 
 The CUDA path runs the whole problem; the fp64 oracle checks every row where it
-finishes in seconds (8K prefill) and seeded samples elsewhere: 512 rows per
+finishes in seconds (8K prefill), 1024 seeded rows of the 8K FP8 prefill, and
+seeded samples elsewhere: 512 rows per
 sequence for the 2 x 64K prefill, 96 rows per request for chunked prefill over
 the 57K-token paged prefix, and 6 whole requests of the 32-request decode.
 Inputs are drawn on the GPU by the seeded generators and copied back for the
@@ -58,6 +59,40 @@ def test_prefill_8k_all_rows():
                               cu.cpu().numpy(), p, w.scale)
     check(out, lse, wo, wl, "8K prefill, all rows")
 
+
+
+def test_prefill_fp8_8k_sampled_rows():
+    """The FP8 prefill on the 8K workload's inputs taken as already rotated (the
+    quantisers are bit-exact with the oracle's, so the codes on both sides are
+    equal) over 1024 seeded query rows, all 64 heads, against the fp64 oracle over
+    the dequantised values; bounds as for the small FP8 cases."""
+    w = synth.PREFILL_8K
+    inp = w.make(DEV)
+    q_raw, k_raw, v_raw = inp["q"].cpu(), inp["k"].cpu(), inp["v"].cpu()
+    pos, cu = inp["pos"], inp["cu"]
+    cq, sq = atc.quant_fp8_rows(inp["q"])
+    ck, sk = atc.quant_fp8_heads(inp["k"])
+    cv, sv = atc.quant_fp8_heads(inp["v"], transposed=True)
+    out = torch.empty(inp["q"].shape, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32, device=DEV)
+    atc.attn_prefill_fp8(cq, sq, ck, sk, cv, sv, out, lse, cu, pos, w.seq, cu, pos)
+    atc.attn_device_status()
+    rows = synth.sample_rows(w.seq, 1024, 90)
+    p = pos.cpu().numpy()
+    oq, osq = oracle.quant_e4m3(synth.as_f64(q_raw[rows]), [0, 1])
+    ok, osk = oracle.quant_e4m3(synth.as_f64(k_raw), [1])
+    ov, osv = oracle.quant_e4m3(synth.as_f64(v_raw), [1])
+    vh = ov * osv.astype(np.float64)[None, :, None]
+    wo, wl = oracle.attention(oq * osq.astype(np.float64)[:, :, None], np.zeros(len(rows), np.int32), p[rows],
+                              ok * osk.astype(np.float64)[None, :, None], vh, cu.cpu().numpy(), p, w.scale)
+    o = out[torch.from_numpy(rows).to(DEV)].float().cpu().numpy()
+    l = lse[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    d = np.abs(o - wo)
+    assert np.isfinite(o).all()
+    tol_max = (2.0 ** -4 + 32 * 2.0 ** -10) * np.abs(vh).max()
+    assert d.max() <= tol_max, f"fp8 8K: max |dO| = {d.max():.3g} > {tol_max:.3g}"
+    assert d.mean() <= 4e-3, f"fp8 8K: mean |dO| = {d.mean():.3g}"
+    assert np.abs(l - wl).max() <= TOL_LSE, f"fp8 8K: max |dLSE| = {np.abs(l - wl).max():.3g}"
 
 def test_prefill_64k_x2_head_slice_and_all_heads():
     w = synth.PREFILL_64K
