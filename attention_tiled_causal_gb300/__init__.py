@@ -8,6 +8,7 @@ PyTorch provides device memory and streams.
 
 Entry points (same names as the C ABI):
     rope_apply(x, positions, base)                      RoPE at absolute positions, in place
+    rope_apply_qk(q, k, positions, base)                the same on queries and keys in one launch
     rope_table(positions, head_dim, base)               cos/sin table for on-the-fly rotation
     attn_prefill(..., q_rope_cs=table)                  attention with the query's RoPE fused in
     attn_kv_append_paged(k_new, v_new, positions, slots, k_cache, v_cache)
@@ -24,10 +25,10 @@ Entry points (same names as the C ABI):
 from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_decode_paged_int8,
                        attn_device_status,
                        attn_kv_append_paged, attn_kv_append_paged_int8, attn_lse_merge, attn_prefill, attn_prefill_fp8,
-                       decode_workspace, lib_path, library, prefill, quant_fp8_heads, quant_fp8_rows, rope_apply, rope_quant_fp8_heads,
+                       decode_workspace, lib_path, library, prefill, quant_fp8_heads, quant_fp8_rows, rope_apply, rope_apply_qk, rope_quant_fp8_heads,
                        rope_quant_fp8_rows, rope_table)
 
 __all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_decode_paged_int8", "attn_device_status",
            "attn_kv_append_paged", "attn_kv_append_paged_int8", "attn_lse_merge", "attn_prefill", "attn_prefill_fp8", "decode_workspace", "lib_path", "library",
-           "prefill", "quant_fp8_heads", "quant_fp8_rows", "rope_apply", "rope_quant_fp8_heads",
+           "prefill", "quant_fp8_heads", "quant_fp8_rows", "rope_apply", "rope_apply_qk", "rope_quant_fp8_heads",
            "rope_quant_fp8_rows", "rope_table"]

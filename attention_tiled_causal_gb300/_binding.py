@@ -43,6 +43,8 @@ def library():
     lib.rope_apply.argtypes = [P, I32, I64, I32, I32, I64, P, F64, P]
     lib.rope_apply.restype = I32
     lib.rope_table.argtypes = [P, I64, I32, F64, P, P]
+    lib.rope_apply_qk.argtypes = [P, I32, I64, P, I32, I64, I32, I64, I32, P, F64, P]
+    lib.rope_apply_qk.restype = I32
     lib.rope_table.restype = I32
     lib.attn_prefill_rope_q.argtypes = [P, P, P, P, I32, P, I32, I32, P, P, I64, I32, P, P, I64, P, P, I32, I32,
                                         I64, I32, I32, I32, I32, I32, F32, I32, P, P]
@@ -127,6 +129,23 @@ def rope_apply(x: torch.Tensor, positions: torch.Tensor, base: float = 10000.0, 
     _check(library().rope_apply(_ptr(x), _dt(x), x.shape[0], x.shape[1], x.shape[2], x.stride(0),
                                 _ptr(positions), float(base), _stream(stream)))
     return x
+
+
+def rope_apply_qk(q: torch.Tensor, k: torch.Tensor, positions: torch.Tensor, base: float = 10000.0,
+                  stream=None) -> None:
+    """rope_apply on q [tokens, Hq, d] and k [tokens, Hkv, d] (same dtype and d) in one
+    launch, in place, at the same absolute positions."""
+    for t, n in ((q, "q"), (k, "k")):
+        if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} must be [tokens, heads, head_dim] with heads and head_dim packed")
+    if q.dtype != k.dtype or q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2]:
+        raise ValueError("q and k must share dtype, token count and head_dim")
+    T, Hq, d = q.shape
+    positions = _i32(positions, "positions")
+    if positions.numel() != T:
+        raise ValueError("positions must hold one entry per token")
+    _check(library().rope_apply_qk(_ptr(q), Hq, q.stride(0), _ptr(k), k.shape[1], k.stride(0), _dt(q), T, d,
+                                   _ptr(positions), float(base), _stream(stream)))
 
 
 def attn_kv_append_paged(k_new, v_new, positions, slots, k_cache, v_cache, *, k_rot_out=None,

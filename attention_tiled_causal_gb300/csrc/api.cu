@@ -196,6 +196,34 @@ int rope_apply(void* x, attn_dtype_t dtype, int64_t tokens, int heads, int head_
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "rope_apply launch");
 }
 
+int rope_apply_qk(void* q, int q_heads, int64_t q_stride_token, void* k, int k_heads, int64_t k_stride_token,
+                  attn_dtype_t dtype, int64_t tokens, int head_dim, const int32_t* positions, double base,
+                  void* stream) {
+  if (tokens < 0 || q_heads < 0 || k_heads < 0 || head_dim <= 0)
+    return fail(ATTN_ERR_ARG, "rope_apply_qk: negative size");
+  if (tokens == 0 || q_heads + k_heads == 0) return ATTN_OK;
+  if ((q_heads && !q) || (k_heads && !k) || !positions) return fail(ATTN_ERR_ARG, "rope_apply_qk: null pointer");
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP32) return fail(ATTN_ERR_UNSUPPORTED, "rope_apply_qk: dtype");
+  const int V = dtype == ATTN_BF16 ? 8 : 4;
+  if (head_dim % 2 || (head_dim / 2) % V || head_dim > 256)
+    return fail(ATTN_ERR_SHAPE, "rope_apply_qk: head_dim %d (need head_dim/2 a multiple of %d, <= 256)", head_dim, V);
+  if ((q_heads && q_stride_token < (int64_t)q_heads * head_dim) ||
+      (k_heads && k_stride_token < (int64_t)k_heads * head_dim))
+    return fail(ATTN_ERR_ARG, "rope_apply_qk: stride_token too small");
+  if ((q_heads && (!aligned16(q) || q_stride_token % V)) || (k_heads && (!aligned16(k) || k_stride_token % V)))
+    return fail(ATTN_ERR_ALIGN, "rope_apply_qk: q / k / strides not 16-byte aligned");
+  if (!(base > 0.0)) return fail(ATTN_ERR_ARG, "rope_apply_qk: base must be positive");
+  attn::RopeLaunch a{q_heads ? q : k, dtype == ATTN_BF16 ? 0 : 1, tokens, q_heads ? q_heads : k_heads, head_dim,
+                     q_heads ? q_stride_token : k_stride_token, positions, base};
+  if (q_heads && k_heads) {
+    a.x2 = k;
+    a.heads2 = k_heads;
+    a.stride2 = k_stride_token;
+  }
+  cudaError_t e = attn::launch_rope(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "rope_apply_qk launch");
+}
+
 int attn_kv_append_paged(const void* k_new, const void* v_new, const int32_t* positions, const int32_t* slots,
                          int64_t tokens, int num_kv_heads, int head_dim, void* k_cache, void* v_cache,
                          int64_t num_pages, int page_size, void* k_rot_out, double base, void* stream) {

@@ -16,6 +16,9 @@ struct RopeLaunch {
   int64_t stride_token;
   const int32_t* positions;
   double base;
+  void* x2 = nullptr;  // optional second tensor rotated at the same positions (keys with the queries)
+  int heads2 = 0;
+  int64_t stride2 = 0;
 };
 cudaError_t launch_rope(const RopeLaunch& a, cudaStream_t s);
 cudaError_t launch_rope_table(float* cs_out, int64_t tokens, int head_dim, const int32_t* positions, double base,

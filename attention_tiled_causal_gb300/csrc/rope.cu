@@ -73,25 +73,30 @@ __device__ __forceinline__ void angle_tables(float (*cs_s)[W], float (*sn_s)[W],
   __syncthreads();
 }
 
+// Rotates the heads of x and, when heads2 > 0, those of x2 at the same token
+// positions (queries and keys in one launch): a token's rows are its heads of
+// x, then its heads of x2, all sharing the block's angle tables.
 template <typename T, int NT>
 __global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t tokens, int heads, int d,
-                                                   int64_t stride_tok, const int32_t* __restrict__ pos,
+                                                   int64_t stride_tok, T* __restrict__ x2, int heads2,
+                                                   int64_t stride2, const int32_t* __restrict__ pos,
                                                    const InvFreq f) {
   constexpr int V = Vec<T>::N;
   __shared__ float cs_s[NT][128], sn_s[NT][128];
   const int half = d / 2;
   const int chunks = half / V;
+  const int hall = heads + heads2;
   const int64_t t0 = (int64_t)blockIdx.x * NT;
   angle_tables<NT, 128>(cs_s, sn_s, t0, tokens, half, pos, f);
-  const int items = NT * heads * chunks;
+  const int items = NT * hall * chunks;
 #pragma unroll 4
   for (int w = threadIdx.x; w < items; w += blockDim.x) {
     const int c = w % chunks;
-    const int h = (w / chunks) % heads;
-    const int tt = w / (chunks * heads);
+    const int h = (w / chunks) % hall;
+    const int tt = w / (chunks * hall);
     const int64_t t = t0 + tt;
     if (t >= tokens) continue;
-    T* p1 = x + t * stride_tok + (int64_t)h * d + c * V;
+    T* p1 = (h < heads ? x + t * stride_tok + (int64_t)h * d : x2 + t * stride2 + (int64_t)(h - heads) * d) + c * V;
     T* p2 = p1 + half;
     uint4 u1 = *reinterpret_cast<const uint4*>(p1);
     uint4 u2 = *reinterpret_cast<const uint4*>(p2);
@@ -539,25 +544,30 @@ cudaError_t launch_rope_table(float* cs_out, int64_t tokens, int head_dim, const
 
 cudaError_t launch_rope(const RopeLaunch& a, cudaStream_t s) {
   const InvFreq f = make_inv_freq(a.base, a.head_dim);
-  if (a.tokens == 0) return cudaSuccess;
+  if (a.tokens == 0 || a.heads + a.heads2 == 0) return cudaSuccess;
   // few heads: 16 tokens per block, so the angle tables are amortised over enough rows
-  if (a.heads <= 16) {
-    const int64_t blocks = (a.tokens + 15) / 16;
-    if (a.dtype == 0)
-      rope_kernel<__nv_bfloat16, 16><<<(unsigned)blocks, 256, 0, s>>>(
-          (__nv_bfloat16*)a.x, a.tokens, a.heads, a.head_dim, a.stride_token, a.positions, f);
+  const bool few = a.heads + a.heads2 <= 16;
+  const int nt = few ? 16 : kTok;
+  const unsigned blocks = (unsigned)((a.tokens + nt - 1) / nt);
+  if (a.dtype == 0) {
+    auto* x = (__nv_bfloat16*)a.x;
+    auto* x2 = (__nv_bfloat16*)a.x2;
+    if (few)
+      rope_kernel<__nv_bfloat16, 16><<<blocks, 256, 0, s>>>(x, a.tokens, a.heads, a.head_dim, a.stride_token, x2,
+                                                            a.heads2, a.stride2, a.positions, f);
     else
-      rope_kernel<float, 16><<<(unsigned)blocks, 256, 0, s>>>((float*)a.x, a.tokens, a.heads, a.head_dim,
-                                                              a.stride_token, a.positions, f);
-    return cudaGetLastError();
+      rope_kernel<__nv_bfloat16, kTok><<<blocks, 256, 0, s>>>(x, a.tokens, a.heads, a.head_dim, a.stride_token, x2,
+                                                              a.heads2, a.stride2, a.positions, f);
+  } else {
+    auto* x = (float*)a.x;
+    auto* x2 = (float*)a.x2;
+    if (few)
+      rope_kernel<float, 16><<<blocks, 256, 0, s>>>(x, a.tokens, a.heads, a.head_dim, a.stride_token, x2, a.heads2,
+                                                    a.stride2, a.positions, f);
+    else
+      rope_kernel<float, kTok><<<blocks, 256, 0, s>>>(x, a.tokens, a.heads, a.head_dim, a.stride_token, x2, a.heads2,
+                                                      a.stride2, a.positions, f);
   }
-  const int64_t blocks = (a.tokens + kTok - 1) / kTok;
-  if (a.dtype == 0)
-    rope_kernel<__nv_bfloat16, kTok><<<(unsigned)blocks, 256, 0, s>>>(
-        (__nv_bfloat16*)a.x, a.tokens, a.heads, a.head_dim, a.stride_token, a.positions, f);
-  else
-    rope_kernel<float, kTok><<<(unsigned)blocks, 256, 0, s>>>((float*)a.x, a.tokens, a.heads, a.head_dim,
-                                                              a.stride_token, a.positions, f);
   return cudaGetLastError();
 }
 

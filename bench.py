@@ -272,8 +272,7 @@ def pipelined_e2e(atc, host_in, host_out, dev, pos, cu, seq, steps, warmup):
                 s_cmp.wait_event(in_done[b])
                 if i >= 2 or not first:
                     s_cmp.wait_event(out_done[b])  # this buffer's previous outputs are read back
-                atc.rope_apply(q, pos)
-                atc.rope_apply(k, pos)
+                atc.rope_apply_qk(q, k, pos)
                 atc.attn_prefill(q, k, v, out, lse, cu, pos, seq, cu_k=cu, k_pos=pos)
                 cmp_done[b].record(s_cmp)
             with torch.cuda.stream(s_out):
@@ -331,11 +330,10 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
     q, k, v, pos, cu = inp["q"], inp["k"], inp["v"], inp["pos"], inp["cu"]
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
-    launches = 3  # rope(Q), rope(K), prefill
+    launches = 2  # RoPE of Q and K (one launch), prefill
 
     def step(ev=()):
-        atc.rope_apply(q, pos)
-        atc.rope_apply(k, pos)
+        atc.rope_apply_qk(q, k, pos)
         if ev:
             ev[0].record()
         atc.attn_prefill(q, k, v, out, lse, cu, pos, wl.seq, cu_k=cu, k_pos=pos)
@@ -365,7 +363,7 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
                            args.warmup)
     ms_link = link_floor_ms((hq_, hk_, hv_), (q, k, v), (ho, hl), (out, lse))
     # RoPE alone (S1), an HBM stream: read + write of Q and of K
-    ms_rope = short_ms(timer, lambda ev=(): (atc.rope_apply(q, pos), atc.rope_apply(k, pos)), args.steps, args.warmup)
+    ms_rope = short_ms(timer, lambda ev=(): atc.rope_apply_qk(q, k, pos), args.steps, args.warmup)
     rope_bytes = 2 * (q.numel() + k.numel()) * q.element_size()
     h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
@@ -374,7 +372,7 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
     traffic = profiled_traffic("prefill_tc_causal_8k.md", "prefill_tc.cu")
     res = {
         "ms_per_step": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
-        "launch": {"step": "CUDA graph of the step's 3 launches, replayed" if ms_graph is not None
+        "launch": {"step": "CUDA graph of the step's 2 launches, replayed" if ms_graph is not None
                    else "eager (graph capture failed)",
                    "eager_ms_per_step": round(ms_eager, 4),
                    "graph_ms_per_step": None if ms_graph is None else round(ms_graph, 4)},
@@ -392,7 +390,7 @@ def prefill_arm(wl, args, timer, peaks, peak_src):
                            "ms_per_step": round(ms_e2e_serial, 4),
                            "schedule": "upload, compute and download of each step in turn on one stream"}},
         "launches_per_step": launches,
-        "rope": hbm_line("rope_apply (Q and K of the 8K prefill)", rope_bytes, ms_rope, peaks, peak_src),
+        "rope": hbm_line("rope_apply_qk (Q and K of the 8K prefill, one launch)", rope_bytes, ms_rope, peaks, peak_src),
         "inputs": (q, k, v, pos, cu),
     }
     return res

@@ -79,6 +79,19 @@ ATTN_API int rope_apply(void *x, attn_dtype_t dtype, int64_t tokens, int heads, 
                int64_t stride_token, const int32_t *positions, double base, void *stream);
 
 /*
+ * rope_apply_qk -- rope_apply on a token's queries and keys in one launch: q
+ * [tokens][q_heads][head_dim] (row t at q + t*q_stride_token) and k
+ * [tokens][k_heads][head_dim] (row t at k + t*k_stride_token), both rotated in
+ * place at the same absolute positions, bit for bit as two rope_apply calls
+ * would rotate them (one angle table per token serves both).  Either head count
+ * may be 0 (its pointer is then ignored).  Same dtype, head_dim, alignment and
+ * error rules as rope_apply, for each tensor.
+ */
+ATTN_API int rope_apply_qk(void *q, int q_heads, int64_t q_stride_token, void *k, int k_heads,
+                           int64_t k_stride_token, attn_dtype_t dtype, int64_t tokens, int head_dim,
+                           const int32_t *positions, double base, void *stream);
+
+/*
  * rope_table -- the cos and sin of every RoPE angle, for kernels that rotate on
  * the fly: cs_out[t][i] = (cos a, sin a), a = positions[t] * base^(-2i/head_dim),
  * i < head_dim/2, as fp32 pairs [tokens][head_dim/2][2] (16-byte aligned).  The

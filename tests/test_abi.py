@@ -214,3 +214,14 @@ def test_rope_quant_fp8_rejects_bad_arguments(lib):
     assert lib.rope_quant_fp8_rows(16, 0, 2, 128, None, 1e4, None, None, None) == 0
     assert lib.rope_quant_fp8_heads(16, 4, 300, 128, 16, 1e4, 16, 16, 16, None) == ERR_SHAPE   # > 256 heads
     assert lib.rope_quant_fp8_heads(16, 4, 8, 128, 16, 1e4, 16, 16, None, None) == ERR_ARG    # no scratch
+
+
+def test_rope_apply_qk_rejects_bad_arguments(lib):
+    f = lib.rope_apply_qk
+    assert f(16, 8, 1024, 16, 2, 256, 0, 4, 100, 16, 1e4, None) == ERR_SHAPE     # 50 not a multiple of 8
+    assert f(16, 8, 100, 16, 2, 256, 0, 4, 128, 16, 1e4, None) == ERR_ARG       # q stride < heads * d
+    assert f(16, 8, 1024, 8, 2, 256, 0, 4, 128, 16, 1e4, None) == ERR_ALIGN     # misaligned k
+    assert f(16, 8, 1024, 16, 2, 256, 0, 4, 128, None, 1e4, None) == ERR_ARG    # no positions
+    assert f(16, 8, 1024, 16, 2, 256, 0, 4, 128, 16, 0.0, None) == ERR_ARG      # base
+    assert f(16, 8, 1024, 16, 2, 256, 5, 4, 128, 16, 1e4, None) == ERR_UNSUPPORTED
+    assert f(None, 0, 0, None, 0, 0, 0, 4, 128, 16, 1e4, None) == 0              # nothing to rotate

@@ -86,6 +86,23 @@ def test_rope_fp32_matches_oracle():
     assert np.abs(xd.cpu().double().numpy() - want).max() < 2e-6
 
 
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_rope_apply_qk_equals_two_rope_apply_calls(dtype):
+    """Queries and keys rotated in one launch equal two rope_apply calls bit for
+    bit, for the 64/8 layout (4 tokens per block) and a few-head one (16 per
+    block), with a ragged token count."""
+    for T, hq, hk, seed in ((301, 64, 8, 760), (77, 8, 2, 761)):
+        q = synth.randn((T, hq, 128), seed, 0.7071, dtype=dtype).to(DEV)
+        k = synth.randn((T, hk, 128), seed + 1, 0.7071, dtype=dtype).to(DEV)
+        pos = torch.from_numpy(synth.positions([T], [123456])).to(DEV)
+        q2, k2 = q.clone(), k.clone()
+        atc.rope_apply_qk(q, k, pos)
+        atc.rope_apply(q2, pos)
+        atc.rope_apply(k2, pos)
+        atc.attn_device_status()
+        assert torch.equal(q, q2) and torch.equal(k, k2)
+
 def test_rope_strided_token_rows():
     """Rotating a [T, H, d] view of a wider buffer touches only that view."""
     T, H, d = 64, 4, 128
