@@ -52,6 +52,36 @@ __device__ __forceinline__ void from_f(float x, float& y) { y = x; }
 
 constexpr int kTok = 4;  // tokens per block
 
+// The items w = w0, w0 + step, w0 + 2 step, ... of a block, where item w is
+// chunk w % inner of row w / inner, and row r is head r % heads of token
+// r / heads: the coordinates advance by constants, so the loop body does no
+// integer division (three per item were most of these kernels' instructions).
+struct GridWalk {
+  int c, h, tt;
+  int dc, dh, dt, inner, heads;
+  __device__ __forceinline__ GridWalk(int w0, int step, int inner_, int heads_) : inner(inner_), heads(heads_) {
+    c = w0 % inner;
+    const int r = w0 / inner;
+    h = r % heads;
+    tt = r / heads;
+    dc = step % inner;
+    const int dr = step / inner;
+    dh = dr % heads;
+    dt = dr / heads;
+  }
+  __device__ __forceinline__ void next() {
+    c += dc;
+    const int carry = c >= inner;
+    if (carry) c -= inner;
+    h += dh + carry;  // < 2 heads
+    tt += dt;
+    if (h >= heads) {
+      h -= heads;
+      ++tt;
+    }
+  }
+};
+
 // cos and sin of pos * base^(-2i/d) for the block's NT tokens, i < d/2, into
 // shared memory.  The angle is reduced modulo one turn exactly, in integers
 // (InvFreq); its top 32 bits, as a signed fraction of a turn in [-1/2, 1/2),
@@ -89,11 +119,10 @@ __global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t to
   const int64_t t0 = (int64_t)blockIdx.x * NT;
   angle_tables<NT, 128>(cs_s, sn_s, t0, tokens, half, pos, f);
   const int items = NT * hall * chunks;
+  GridWalk gw(threadIdx.x, blockDim.x, chunks, hall);
 #pragma unroll 4
-  for (int w = threadIdx.x; w < items; w += blockDim.x) {
-    const int c = w % chunks;
-    const int h = (w / chunks) % hall;
-    const int tt = w / (chunks * hall);
+  for (int w = threadIdx.x; w < items; w += blockDim.x, gw.next()) {
+    const int c = gw.c, h = gw.h, tt = gw.tt;
     const int64_t t = t0 + tt;
     if (t >= tokens) continue;
     T* p1 = (h < heads ? x + t * stride_tok + (int64_t)h * d : x2 + t * stride2 + (int64_t)(h - heads) * d) + c * V;
@@ -155,53 +184,79 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const In
   __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
   const int chunks = half / V;
   const int kitems = NT * a.heads * chunks;
-  for (int w = threadIdx.x; w < kitems; w += blockDim.x) {
-    const int c = w % chunks;
-    const int h = (w / chunks) % a.heads;
-    const int tt = w / (chunks * a.heads);
-    const int64_t sl = slot_s[tt];
-    if (sl < 0) continue;
-    const int64_t t = t0 + tt;
-    const int64_t src = (t * a.heads + h) * d + c * V;
-    uint4 u1 = __ldg(reinterpret_cast<const uint4*>(kn + src));
-    uint4 u2 = __ldg(reinterpret_cast<const uint4*>(kn + src + half));
-    if (rotate) {
-      const __nv_bfloat16* a1 = reinterpret_cast<const __nv_bfloat16*>(&u1);
-      const __nv_bfloat16* a2 = reinterpret_cast<const __nv_bfloat16*>(&u2);
-      uint4 w1, w2;
-      __nv_bfloat16* b1 = reinterpret_cast<__nv_bfloat16*>(&w1);
-      __nv_bfloat16* b2 = reinterpret_cast<__nv_bfloat16*>(&w2);
+  // Items go in batches whose loads are all issued before the first store: the
+  // compiler may not move loads above stores to memory it cannot tell apart.
+  constexpr int kKB = 2, kVB = 4;
+  GridWalk gk(threadIdx.x, blockDim.x, chunks, a.heads);
+  for (int w0 = threadIdx.x; w0 < kitems; w0 += kKB * blockDim.x) {
+    uint4 u1[kKB], u2[kKB];
+    int64_t src[kKB], dst[kKB];
+    int tts[kKB], cc[kKB];
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float cs = cs_s[tt][c * V + e], sn = sn_s[tt][c * V + e];
-        const float x1 = to_f(a1[e]), x2 = to_f(a2[e]);
-        float y1, y2;
-        rope_rotate(x1, x2, cs, sn, y1, y2);
-        from_f(y1, b1[e]);
-        from_f(y2, b2[e]);
+    for (int k = 0; k < kKB; ++k) {
+      dst[k] = -1;
+      tts[k] = gk.tt;
+      cc[k] = gk.c;
+      if (w0 + k * (int)blockDim.x < kitems) {
+        const int64_t sl = slot_s[gk.tt];
+        if (sl >= 0) {
+          src[k] = ((t0 + gk.tt) * a.heads + gk.h) * d + gk.c * V;
+          dst[k] = ((int64_t)gk.h * a.cache_rows + sl) * d + gk.c * V;
+          u1[k] = __ldg(reinterpret_cast<const uint4*>(kn + src[k]));
+          u2[k] = __ldg(reinterpret_cast<const uint4*>(kn + src[k] + half));
+        }
       }
-      u1 = w1;
-      u2 = w2;
+      gk.next();
     }
-    const int64_t dst = ((int64_t)h * a.cache_rows + sl) * d + c * V;
-    *reinterpret_cast<uint4*>(kc + dst) = u1;
-    *reinterpret_cast<uint4*>(kc + dst + half) = u2;
-    if (ko) {
-      *reinterpret_cast<uint4*>(ko + src) = u1;
-      *reinterpret_cast<uint4*>(ko + src + half) = u2;
+#pragma unroll
+    for (int k = 0; k < kKB; ++k) {
+      if (dst[k] < 0) continue;
+      if (rotate) {
+        const __nv_bfloat16* a1 = reinterpret_cast<const __nv_bfloat16*>(&u1[k]);
+        const __nv_bfloat16* a2 = reinterpret_cast<const __nv_bfloat16*>(&u2[k]);
+        uint4 w1, w2;
+        __nv_bfloat16* b1 = reinterpret_cast<__nv_bfloat16*>(&w1);
+        __nv_bfloat16* b2 = reinterpret_cast<__nv_bfloat16*>(&w2);
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          const float cs = cs_s[tts[k]][cc[k] * V + e], sn = sn_s[tts[k]][cc[k] * V + e];
+          float y1, y2;
+          rope_rotate(to_f(a1[e]), to_f(a2[e]), cs, sn, y1, y2);
+          from_f(y1, b1[e]);
+          from_f(y2, b2[e]);
+        }
+        u1[k] = w1;
+        u2[k] = w2;
+      }
+      *reinterpret_cast<uint4*>(kc + dst[k]) = u1[k];
+      *reinterpret_cast<uint4*>(kc + dst[k] + half) = u2[k];
+      if (ko) {
+        *reinterpret_cast<uint4*>(ko + src[k]) = u1[k];
+        *reinterpret_cast<uint4*>(ko + src[k] + half) = u2[k];
+      }
     }
   }
   const int vchunks = d / V;
   const int vitems = NT * a.heads * vchunks;
-  for (int w = threadIdx.x; w < vitems; w += blockDim.x) {
-    const int c = w % vchunks;
-    const int h = (w / vchunks) % a.heads;
-    const int tt = w / (vchunks * a.heads);
-    const int64_t sl = slot_s[tt];
-    if (sl < 0) continue;
-    const int64_t t = t0 + tt;
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(vn + (t * a.heads + h) * d + c * V));
-    *reinterpret_cast<uint4*>(vc + ((int64_t)h * a.cache_rows + sl) * d + c * V) = u;
+  GridWalk gv(threadIdx.x, blockDim.x, vchunks, a.heads);
+  for (int w0 = threadIdx.x; w0 < vitems; w0 += kVB * blockDim.x) {
+    uint4 u[kVB];
+    int64_t dst[kVB];
+#pragma unroll
+    for (int k = 0; k < kVB; ++k) {
+      dst[k] = -1;
+      if (w0 + k * (int)blockDim.x < vitems) {
+        const int64_t sl = slot_s[gv.tt];
+        if (sl >= 0) {
+          u[k] = __ldg(reinterpret_cast<const uint4*>(vn + ((t0 + gv.tt) * a.heads + gv.h) * d + gv.c * V));
+          dst[k] = ((int64_t)gv.h * a.cache_rows + sl) * d + gv.c * V;
+        }
+      }
+      gv.next();
+    }
+#pragma unroll
+    for (int k = 0; k < kVB; ++k)
+      if (dst[k] >= 0) *reinterpret_cast<uint4*>(vc + dst[k]) = u[k];
   }
 }
 
@@ -271,15 +326,19 @@ __device__ __forceinline__ float chunk_amax(const RowChunk& r) {
 
 // Symmetric int8 codes of the chunk pair: code = x / sc rounded to the nearest
 // integer (ties to even) and clamped to [-127, 127], the quotient correctly
-// rounded in fp32 (div_rn_recip for normal scales); 0 for a zero scale.
+// rounded in fp32 (div_rn_recip for normal scales); 0 for a zero scale.  The
+// quotient is clamped first (the same codes: anything beyond +-127 rounds to
+// +-127 or past it) and rounded by adding 1.5 * 2^23, where an fp32 add rounds
+// to an integer, ties to even, whose two's complement sits in the low bits --
+// on the FMA and integer pipes rather than the conversion unit.
 template <bool FAST>
 __device__ __forceinline__ uint32_t int8x4(const float* x, float sc, float rc) {
   uint32_t p = 0;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    float q = rintf(FAST ? div_rn_recip(x[e], sc, rc) : x[e] / sc);
-    q = fminf(fmaxf(q, -127.0f), 127.0f);
-    p |= (uint32_t)(uint8_t)(int8_t)(int)q << (8 * e);
+    const float q = fminf(fmaxf(FAST ? div_rn_recip(x[e], sc, rc) : x[e] / sc, -127.0f), 127.0f);
+    const uint32_t code = (uint32_t)__float_as_int(__fadd_rn(q, 12582912.0f)) - 0x4B400000u;
+    p |= (code & 0xffu) << (8 * e);
   }
   return p;
 }
@@ -302,7 +361,7 @@ __device__ __forceinline__ void chunk_store_int8(const RowChunk& r, float sc, in
 // kAppendTok tokens, first every key row (rotated and rounded to bf16 -- the
 // value a bf16 cache would hold), then every value row, each quantised with one
 // fp32 scale per cache row: scale = max|x| / 127.  NT * heads * 8 is a multiple
-// of 32, so a warp handles only keys or only values, and whole rows.
+// of 32, so every warp covers whole rows and runs each loop as often as the others.
 constexpr int kAppendTok = 8;
 
 __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendLaunch a, const InvFreq f) {
@@ -328,30 +387,32 @@ __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendLaunch a, con
   const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
   __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
   const int items = kAppendTok * a.heads * 8;
-  for (int it = threadIdx.x; it < 2 * items; it += blockDim.x) {
-    const bool is_v = it >= items;
-    const int jt = is_v ? it - items : it;
-    const int c = jt & 7, rr = jt >> 3, tt = rr / a.heads, h = rr % a.heads;
-    const int64_t sl = slot_s[tt];
-    const bool ok = sl >= 0;  // tokens past the end carry slot -1
-    const int64_t src = ((t0 + tt) * a.heads + h) * 128;
-    RowChunk r;
-    load_chunk((is_v ? vn : kn) + src, c, ok, r);
-    if (!is_v && rotate) rotate_chunk(r, cs_s[tt], sn_s[tt], c);
-    if (!is_v && ko && ok) {
-      uint4 o1, o2;
-      o1.x = pack_bf16x2(r.a[0], r.a[1]), o1.y = pack_bf16x2(r.a[2], r.a[3]);
-      o1.z = pack_bf16x2(r.a[4], r.a[5]), o1.w = pack_bf16x2(r.a[6], r.a[7]);
-      o2.x = pack_bf16x2(r.b[0], r.b[1]), o2.y = pack_bf16x2(r.b[2], r.b[3]);
-      o2.z = pack_bf16x2(r.b[4], r.b[5]), o2.w = pack_bf16x2(r.b[6], r.b[7]);
-      *reinterpret_cast<uint4*>(ko + src + 8 * c) = o1;
-      *reinterpret_cast<uint4*>(ko + src + 64 + 8 * c) = o2;
-    }
-    const float sc = chunk_amax(r) / 127.0f;
-    if (ok) {
-      const int64_t row = (int64_t)h * a.cache_rows + sl;
-      chunk_store_int8(r, sc, (int8_t*)(is_v ? a.v_cache : a.k_cache) + row * 128, c);
-      if (c == 0) (is_v ? a.v_scale : a.k_scale)[row] = sc;
+  for (int pass = 0; pass < 2; ++pass) {  // keys, then values
+    const bool is_v = pass == 1;
+    GridWalk gw(threadIdx.x, blockDim.x, 8, a.heads);
+    for (int it = threadIdx.x; it < items; it += blockDim.x, gw.next()) {
+      const int c = gw.c, tt = gw.tt, h = gw.h;
+      const int64_t sl = slot_s[tt];
+      const bool ok = sl >= 0;  // tokens past the end carry slot -1
+      const int64_t src = ((t0 + tt) * a.heads + h) * 128;
+      RowChunk r;
+      load_chunk((is_v ? vn : kn) + src, c, ok, r);
+      if (!is_v && rotate) rotate_chunk(r, cs_s[tt], sn_s[tt], c);
+      if (!is_v && ko && ok) {
+        uint4 o1, o2;
+        o1.x = pack_bf16x2(r.a[0], r.a[1]), o1.y = pack_bf16x2(r.a[2], r.a[3]);
+        o1.z = pack_bf16x2(r.a[4], r.a[5]), o1.w = pack_bf16x2(r.a[6], r.a[7]);
+        o2.x = pack_bf16x2(r.b[0], r.b[1]), o2.y = pack_bf16x2(r.b[2], r.b[3]);
+        o2.z = pack_bf16x2(r.b[4], r.b[5]), o2.w = pack_bf16x2(r.b[6], r.b[7]);
+        *reinterpret_cast<uint4*>(ko + src + 8 * c) = o1;
+        *reinterpret_cast<uint4*>(ko + src + 64 + 8 * c) = o2;
+      }
+      const float sc = chunk_amax(r) / 127.0f;
+      if (ok) {
+        const int64_t row = (int64_t)h * a.cache_rows + sl;
+        chunk_store_int8(r, sc, (int8_t*)(is_v ? a.v_cache : a.k_cache) + row * 128, c);
+        if (c == 0) (is_v ? a.v_scale : a.k_scale)[row] = sc;
+      }
     }
   }
 }
@@ -379,13 +440,12 @@ cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s) {
 // NT * heads is a multiple of 4, so every warp covers whole rows and runs the
 // loop the same number of times: rows past the last token load nothing and
 // store nothing, but still take part in the shuffles.
-template <int NT>
 __device__ __forceinline__ bool rope_chunk(const __nv_bfloat16* __restrict__ x, int64_t t0, int64_t tokens,
-                                           int heads, int it, const float (*cs_s)[64], const float (*sn_s)[64],
-                                           RowChunk& r, int64_t& row) {
-  const int c = it & 7, rr = it >> 3, tt = rr / heads;
+                                           int heads, const GridWalk& gw, const float (*cs_s)[64],
+                                           const float (*sn_s)[64], RowChunk& r, int64_t& row) {
+  const int c = gw.c, tt = gw.tt;
   const int64_t t = t0 + tt;
-  row = t * heads + rr % heads;
+  row = t * heads + gw.h;
   const bool ok = t < tokens;
   load_chunk(x + row * 128, c, ok, r);
   rotate_chunk(r, cs_s[tt], sn_s[tt], c);
@@ -420,15 +480,16 @@ __global__ void __launch_bounds__(256) rope_quant_rows_kernel(const __nv_bfloat1
   const int64_t t0 = (int64_t)blockIdx.x * NT;
   angle_tables<NT, 64>(cs_s, sn_s, t0, tokens, 64, pos, f);
   const int items = NT * heads * 8;
+  GridWalk gw(threadIdx.x, blockDim.x, 8, heads);
 #pragma unroll 2
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+  for (int it = threadIdx.x; it < items; it += blockDim.x, gw.next()) {
     RowChunk r;
     int64_t row;
-    const bool ok = rope_chunk<NT>(x, t0, tokens, heads, it, cs_s, sn_s, r, row);
+    const bool ok = rope_chunk(x, t0, tokens, heads, gw, cs_s, sn_s, r, row);
     const float sc = chunk_amax(r) / 448.0f;
     if (ok) {
-      chunk_store(r, sc, codes + row * 128, it & 7);
-      if ((it & 7) == 0) scales[row] = sc;
+      chunk_store(r, sc, codes + row * 128, gw.c);
+      if (gw.c == 0) scales[row] = sc;
     }
   }
 }
@@ -451,13 +512,14 @@ __global__ void __launch_bounds__(256) rope_amax_heads_kernel(const __nv_bfloat1
     const int64_t t0 = g * NT;
     __syncthreads();  // the previous group's angles are no longer read
     angle_tables<NT, 64>(cs_s, sn_s, t0, tokens, 64, pos, f);  // its barrier also publishes hmax
+    GridWalk gw(threadIdx.x, blockDim.x, 8, heads);
 #pragma unroll 2
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    for (int it = threadIdx.x; it < items; it += blockDim.x, gw.next()) {
       RowChunk r;
       int64_t row;
-      const bool ok = rope_chunk<NT>(x, t0, tokens, heads, it, cs_s, sn_s, r, row);
+      const bool ok = rope_chunk(x, t0, tokens, heads, gw, cs_s, sn_s, r, row);
       const float m = chunk_amax(r);  // 0 for rows past the end
-      if (ok && (it & 7) == 0) atomicMax(&hmax[(it >> 3) % heads], __float_as_uint(m));
+      if (ok && gw.c == 0) atomicMax(&hmax[gw.h], __float_as_uint(m));
     }
   }
   __syncthreads();
@@ -477,12 +539,13 @@ __global__ void __launch_bounds__(256) rope_quant_heads_kernel(const __nv_bfloat
   if (blockIdx.x == 0)
     for (int h = threadIdx.x; h < heads; h += blockDim.x) scales[h] = __uint_as_float(amax_bits[h]) / 448.0f;
   const int items = NT * heads * 8;
+  GridWalk gw(threadIdx.x, blockDim.x, 8, heads);
 #pragma unroll 2
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+  for (int it = threadIdx.x; it < items; it += blockDim.x, gw.next()) {
     RowChunk r;
     int64_t row;
-    if (rope_chunk<NT>(x, t0, tokens, heads, it, cs_s, sn_s, r, row))
-      chunk_store(r, __uint_as_float(__ldg(amax_bits + (it >> 3) % heads)) / 448.0f, codes + row * 128, it & 7);
+    if (rope_chunk(x, t0, tokens, heads, gw, cs_s, sn_s, r, row))
+      chunk_store(r, __uint_as_float(__ldg(amax_bits + gw.h)) / 448.0f, codes + row * 128, gw.c);
   }
 }
 
