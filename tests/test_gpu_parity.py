@@ -87,6 +87,25 @@ def test_rope_fp32_matches_oracle():
 
 
 
+@pytest.mark.parametrize("dtype,d,H", [(torch.bfloat16, 96, 40), (torch.float32, 40, 3), (torch.bfloat16, 224, 5)])
+def test_rope_head_dims_with_odd_chunk_counts(dtype, d, H):
+    """Head sizes whose half is not a power-of-two number of 16-byte chunks (6, 5
+    and 14 chunks) and head counts that leave partial passes: the kernels walk
+    (chunk, head, token) by constant steps, which must match the oracle here too."""
+    T = 203
+    x = synth.randn((T, H, d), 104 + d, 0.7071, dtype=dtype)
+    pos = np.arange(T, dtype=np.int32) * 31 + 7
+    xd = x.to(DEV)
+    atc.rope_apply(xd, torch.from_numpy(pos).to(DEV))
+    atc.attn_device_status()
+    got = synth.as_f64(xd.cpu())
+    if dtype == torch.bfloat16:
+        want = rotated_bf16(x, pos)
+        assert (np.abs(got - want) <= np.abs(want) * 2.0 ** -7 + 2e-6).all()
+    else:
+        assert np.abs(got - oracle.rope(synth.as_f64(x), pos)).max() < 2e-6
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_rope_apply_qk_equals_two_rope_apply_calls(dtype):
     """Queries and keys rotated in one launch equal two rope_apply calls bit for
