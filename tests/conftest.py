@@ -10,7 +10,7 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
-    config.addinivalue_line("markers", "slow: full-size workload parity (GPU box only)")
+    config.addinivalue_line("markers", "slow: full-size workload parity (needs a GPU and a few minutes)")
 
 
 def pytest_collection_modifyitems(config, items):
