@@ -824,10 +824,7 @@ def main():
         line.update({"value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
                      "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                     "config": {"workload": wl.name + " (RoPE of Q and K + attention, O and LSE)",
-                                "batch": wl.batch, "seq_len": wl.seq, "q_heads": wl.hq, "kv_heads": wl.hkv,
-                                "head_dim": wl.d, "flops_per_step": res["flops"], "l2_flush": True,
-                                "parallelism": f"replicas x{ws}"},
+                     "config": prefill_config(wl, ws),
                      "roofline": res["roofline"], "e2e": res["e2e"], "clocks": clocks,
                      "launch": res["launch"], "gpu_launches": res["launches_per_step"] * args.steps})
     else:
@@ -849,6 +846,13 @@ def main():
     if pg:
         pg.destroy_process_group()
     return 0
+
+
+def prefill_config(wl, ws):
+    """The headline workload's `config`, the same for both arms."""
+    return {"workload": wl.name + " (RoPE of Q and K + attention, O and LSE)", "batch": wl.batch,
+            "seq_len": wl.seq, "q_heads": wl.hq, "kv_heads": wl.hkv, "head_dim": wl.d, "flops_per_step": wl.flops(),
+            "l2_flush": True, "parallelism": f"replicas x{ws}"}
 
 
 def reference_arm(args, synth):
@@ -873,8 +877,7 @@ def reference_arm(args, synth):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name + " (RoPE of Q and K + attention, O and LSE)", "batch": wl.batch,
-                       "seq_len": wl.seq, "q_heads": wl.hq, "kv_heads": wl.hkv, "head_dim": wl.d},
+            "config": prefill_config(wl, dist_env()[0]),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                              "kind": "oracle",
                              "sample": f"each step: {rows} seeded query rows x 64 heads of the 8192-token "
