@@ -75,10 +75,11 @@ int get_encode(EncodeTiledFn* fn) {
   return ATTN_OK;
 }
 
-// bf16 tensor map, 128-byte swizzle, box of 64 elements along the innermost dim.
+// Tensor map of element type dt with a 128-byte swizzle (boxes whose innermost
+// extent is 128 bytes: 64 bf16 or 128 one-byte elements).
 int encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank, const cuuint64_t* dims,
                  const cuuint64_t* strides_bytes, const cuuint32_t* box) {
-  EncodeTiledFn fn;
+  EncodeTiledFn fn = nullptr;
   int rc = get_encode(&fn);
   if (rc) return rc;
   cuuint32_t es[3] = {1, 1, 1};
