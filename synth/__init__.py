@@ -17,7 +17,7 @@ random draw comes from a torch CPU generator seeded per tensor.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 from typing import Optional
 
 import numpy as np
