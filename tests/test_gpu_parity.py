@@ -1077,3 +1077,28 @@ def test_prefill_fp8_misaligned_key_sequence_is_reported():
     assert "0x204" in str(e.value)
     assert torch.isnan(out[8:].float()).all()
     assert not torch.isnan(out[:8].float()).any()
+
+
+def test_prefill_fp8_zero_length_sequences_and_masked_rows():
+    """Zero-length sequences in the batch, and queries placed before every key
+    (no visible key: O = 0, LSE = -inf), on the e4m3 path."""
+    lens = [0, 160, 0, 37]
+    q, k, v, pos, cu = _fp8_case(lens, 8, 1, [0, 0, 0, 0], 914)
+    out, lse = _run_fp8(q, k, v, pos, cu, lens)
+    want_o, want_l, vh = _fp8_oracle(q, k, v, pos, cu, lens)
+    check(out, lse, want_o, want_l, tol_max=_fp8_max_tol(vh), tol_mean=FP8_MEAN, what="fp8 zero-length")
+
+    qd = synth.randn((10, 8, 128), 915, 0.7).to(DEV)
+    kd = synth.randn((208, 1, 128), 916, 0.7).to(DEV)
+    vd = synth.randn((208, 1, 128), 917, 0.7).to(DEV)
+    cq, sq = atc.quant_fp8_rows(qd)
+    ck, sk = atc.quant_fp8_heads(kd)
+    cv, sv = atc.quant_fp8_heads(vd, transposed=True)
+    qpos = torch.arange(10, dtype=torch.int32, device=DEV)
+    kpos = torch.arange(50, 258, dtype=torch.int32, device=DEV)
+    out = torch.full((10, 8, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((10, 8), dtype=torch.float32, device=DEV)
+    atc.attn_prefill_fp8(cq, sq, ck, sk, cv, sv, out, lse, torch.tensor([0, 10], dtype=torch.int32, device=DEV),
+                         qpos, 10, torch.tensor([0, 208], dtype=torch.int32, device=DEV), kpos)
+    atc.attn_device_status()
+    assert torch.all(out == 0) and torch.all(lse == -math.inf)
