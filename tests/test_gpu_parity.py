@@ -1102,3 +1102,50 @@ def test_prefill_fp8_zero_length_sequences_and_masked_rows():
                          qpos, 10, torch.tensor([0, 208], dtype=torch.int32, device=DEV), kpos)
     atc.attn_device_status()
     assert torch.all(out == 0) and torch.all(lse == -math.inf)
+
+
+@pytest.mark.parametrize("d", [64, 30])
+def test_lse_merge_other_head_sizes(d):
+    """Head sizes that take the general merge kernels: 64 (16-byte vectors, not
+    the 128-wide kernel) and 30 (scalar), with an empty part and a row with none."""
+    P, R, H = 3, 21, 5
+    rng = np.random.default_rng(30 + d)
+    po = rng.normal(0, 1, (P, R, H, d)).astype(np.float32)
+    pl = rng.normal(0, 2, (P, R, H)).astype(np.float32)
+    pl[1, :, 1] = -np.inf
+    pl[:, 4, 3] = -np.inf
+    want_o, want_l = oracle.lse_merge(po.astype(np.float64), pl.astype(np.float64))
+    out = torch.empty((R, H, d), dtype=torch.float32, device=DEV)
+    lse = torch.empty((R, H), dtype=torch.float32, device=DEV)
+    atc.attn_lse_merge(torch.from_numpy(po).to(DEV), torch.from_numpy(pl).to(DEV), out, lse)
+    check(out, lse, want_o, want_l, tol_max=1e-5, tol_mean=1e-6, tol_lse=1e-5, what=f"merge d={d}")
+    assert torch.all(out[4, 3] == 0)
+
+
+def test_paged_prefill_fp32_output_head_slice_matches_oracle():
+    """The paged (prefix) source with fp32 output for query heads 8..15 only: the
+    prefix part of chunked prefill on one rank of a head split."""
+    prefix, chunk, B, hq, hkv = 300, 130, 2, 16, 2
+    table, num_pages, kc, vc, q, k, v = _chunked_case(prefix, chunk, B, hq, hkv, 930)
+    qpos = synth.positions([chunk] * B, [prefix] * B)
+    qd = q.to(DEV)
+    atc.rope_apply(qd, torch.from_numpy(qpos).to(DEV))
+    out = torch.full((B * chunk, hq, 128), float("nan"), dtype=torch.float32, device=DEV)
+    lse = torch.full((B * chunk, hq), float("nan"), dtype=torch.float32, device=DEV)
+    atc.attn_prefill(qd, kc.to(DEV), vc.to(DEV), out, lse, torch.from_numpy(synth.cu_seqlens([chunk] * B)).to(DEV),
+                     torch.from_numpy(qpos).to(DEV), chunk, page_table=torch.from_numpy(table).to(DEV),
+                     k_lens=torch.full((B,), prefix, dtype=torch.int32, device=DEV), num_pages=num_pages,
+                     h_lo=8, h_hi=16)
+    atc.attn_device_status()
+    qr = rotated_bf16(q, qpos)
+    kcf, vcf = synth.as_f64(kc), synth.as_f64(vc)
+    keys = [np.stack([oracle.gather_pages(kcf, table, num_pages, g, b, prefix) for g in range(hkv)], 1)
+            for b in range(B)]
+    vals = [np.stack([oracle.gather_pages(vcf, table, num_pages, g, b, prefix) for g in range(hkv)], 1)
+            for b in range(B)]
+    kpos = np.concatenate([np.arange(prefix, dtype=np.int32)] * B)
+    want_o, want_l = oracle.attention(qr, seq_ids([chunk] * B), qpos, np.concatenate(keys), np.concatenate(vals),
+                                      synth.cu_seqlens([prefix] * B), kpos, 128 ** -0.5, causal=False,
+                                      h_lo=8, h_hi=16)
+    check(out[:, 8:16], lse[:, 8:16], want_o[:, 8:16], want_l[:, 8:16], what="paged fp32 head slice")
+    assert torch.isnan(out[:, :8]).all() and torch.isnan(lse[:, 8:16]).sum() == 0
