@@ -30,6 +30,10 @@ MUTANTS = [
     ("int8 rounding toward zero", "float q = rintf((float)x[i] / s);", "float q = truncf((float)x[i] / s);", False),
     ("e4m3 four mantissa bits", "int q = (e - 1) - 3;", "int q = (e - 1) - 4;", False),
     ("e4m3 no saturation", "if (r > 448.0) r = 448.0;", "if (r > 480.0) r = 480.0;", False),
+    ("e4m3 ties away from zero", "double r = rint(a / ldexp(1.0, q)) * ldexp(1.0, q);",
+     "double r = floor(a / ldexp(1.0, q) + 0.5) * ldexp(1.0, q);", False),
+    ("e4m3 subnormal spacing", "if (q < -9) q = -9;", "if (q < -10) q = -10;", False),
+    ("e4m3 group scale over 480", "float s = amax / 448.0f;", "float s = amax / 480.0f;", False),
     ("append rotates values", "const double *vs = v_new + (t * heads + h) * (int64_t)d;",
      "const double *vs = krow - (int64_t)0 * (t * heads + h);", False),
 ]
