@@ -34,6 +34,7 @@ MUTANTS = [
      "double r = floor(a / ldexp(1.0, q) + 0.5) * ldexp(1.0, q);", False),
     ("e4m3 subnormal spacing", "if (q < -9) q = -9;", "if (q < -10) q = -10;", False),
     ("e4m3 group scale over 480", "float s = amax / 448.0f;", "float s = amax / 480.0f;", False),
+    ("e4m3 quotient in fp64", "round_e4m3((double)((float)xg[i] / s))", "round_e4m3(xg[i] / (double)s)", False),
     ("append rotates values", "const double *vs = v_new + (t * heads + h) * (int64_t)d;",
      "const double *vs = krow - (int64_t)0 * (t * heads + h);", False),
 ]

@@ -631,3 +631,22 @@ def test_quant_e4m3_groups_and_scale():
     c2, s2 = oracle.quant_e4m3(x, [2])
     assert s2.shape == (32,)
     np.testing.assert_array_equal(s2, (np.abs(x).max(axis=(0, 1)).astype(np.float32) / np.float32(448.0)))
+
+
+
+def test_quant_e4m3_decides_codes_in_fp32():
+    """The code of x is e4m3(x / scale) with the quotient rounded to fp32 first.
+    For a group with maximum 400 (scale = 400/448 in fp32), x = 1.171875 gives the
+    fp32 quotient 1.3125 exactly: the midpoint between the e4m3 values 1.25 and
+    1.375, which ties to even, 1.25.  The exact quotient is 1.3125000125..., which
+    would round up to 1.375.  The expected value comes from numpy's fp32 division
+    and torch's float8_e4m3fn conversion, not from the oracle."""
+    x = np.array([[400.0, 1.171875, -1.171875]])
+    codes, scales = oracle.quant_e4m3(x, [0])
+    s32 = np.float32(400.0) / np.float32(448.0)
+    assert scales[0] == s32
+    q32 = np.float32(1.171875) / s32
+    assert float(q32) == 1.3125
+    want = torch.tensor([float(q32)]).to(torch.float8_e4m3fn).float().item()
+    assert want == 1.25
+    np.testing.assert_array_equal(codes[0], [448.0, 1.25, -1.25])
