@@ -28,6 +28,7 @@ MUTANTS = [
     ("int8 scale of the wrong token", "(double)scales[r];", "(double)scales[r > 0 ? r - 1 : r];", False),
     ("int8 scale over 128", "float s = amax / 127.0f;", "float s = amax / 128.0f;", False),
     ("int8 rounding toward zero", "float q = rintf((float)x[i] / s);", "float q = truncf((float)x[i] / s);", False),
+    ("int8 quotient in fp64", "float q = rintf((float)x[i] / s);", "float q = (float)rint(x[i] / (double)s);", False),
     ("e4m3 four mantissa bits", "int q = (e - 1) - 3;", "int q = (e - 1) - 4;", False),
     ("e4m3 no saturation", "if (r > 448.0) r = 448.0;", "if (r > 480.0) r = 480.0;", False),
     ("e4m3 ties away from zero", "double r = rint(a / ldexp(1.0, q)) * ldexp(1.0, q);",

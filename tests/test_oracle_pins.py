@@ -650,3 +650,20 @@ def test_quant_e4m3_decides_codes_in_fp32():
     want = torch.tensor([float(q32)]).to(torch.float8_e4m3fn).float().item()
     assert want == 1.25
     np.testing.assert_array_equal(codes[0], [448.0, 1.25, -1.25])
+
+
+
+def test_int8_codes_are_decided_on_the_fp32_quotient():
+    """Row maximum 37.5 (scale = 37.5/127 in fp32) and x = 18.75: the fp32
+    quotient is exactly 63.5, which rounds to the even 64; the exact quotient is
+    63.49999823..., which would round to 63.  The expectation comes from numpy's
+    fp32 division and rint, not from the oracle."""
+    row = [37.5, 18.75, -18.75, 0.0]
+    k, v, z8, zs = _q_case(row)
+    kc, vc, ks, vs, _ = oracle.kv_append_int8(k, v, None, [0], z8, z8, zs, zs, base=0.0)
+    s = np.float32(37.5) / np.float32(127.0)
+    q = np.float32(18.75) / s
+    assert float(q) == 63.5 and np.rint(q) == 64
+    assert abs(18.75 / float(s) - 63.5) > 1e-7
+    np.testing.assert_array_equal(vc[0, 0, 0], [127, 64, -64, 0])
+    np.testing.assert_array_equal(kc[0, 0, 0], [127, 64, -64, 0])
