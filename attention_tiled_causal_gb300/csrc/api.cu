@@ -135,14 +135,6 @@ int map_pages_i8(CUtensorMap* m, const void* base, int hkv, int64_t num_pages) {
   return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box);
 }
 
-// ATTN_GB300_FORCE_SIMT=1 routes bf16 prefill to the CUDA-core kernel, so the
-// two kernels can be compared with each other on problems too large for a
-// CPU check.
-bool force_simt() {
-  const char* e = getenv("ATTN_GB300_FORCE_SIMT");
-  return e && e[0] == '1';
-}
-
 }  // namespace
 
 namespace attn {
@@ -432,7 +424,7 @@ int prefill_impl(const void* q, const void* k, const void* v, void* out, attn_dt
   int rc = device_error_ptr(&a.err);
   if (rc) return rc;
 
-  const bool tc = dtype == ATTN_BF16 && head_dim == 128 && (!paged || page_size == 64) && !force_simt();
+  const bool tc = dtype == ATTN_BF16 && head_dim == 128 && (!paged || page_size == 64);
   if (q_rope_cs && !tc)
     return fail(ATTN_ERR_UNSUPPORTED, "attn_prefill_rope_q: fused RoPE needs bf16, head_dim 128 (tensor-core path)");
   cudaError_t e;

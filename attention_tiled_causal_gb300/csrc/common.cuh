@@ -164,22 +164,12 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, one instruction, issued by one thread.
-// No "memory" clobber: the operands are made visible by mbarrier waits (which
-// carry one), and volatile asm statements keep their order.
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-
-// The same instruction issued by a whole converged warp: every lane computes the
-// (warp-uniform) operands, and elect.sync picks the one lane that issues.  A
-// single lane inside a divergent branch issues far more slowly when the other
-// warps of its sub-partition are busy.
+// D[tmem] (+)= A[smem] * B[smem]^T (kind::f16), issued by a whole converged
+// warp: every lane computes the (warp-uniform) operands, and elect.sync picks
+// the one lane that issues.  A single lane inside a divergent branch issues far
+// more slowly when the other warps of its sub-partition are busy.  No "memory"
+// clobber: the operands are made visible by mbarrier waits (which carry one),
+// and volatile asm statements keep their order.
 __device__ __forceinline__ void tc_mma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                  uint32_t accumulate) {
   asm volatile(
@@ -210,12 +200,6 @@ __device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
-}
-
-// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
 }
 
 // 32 lanes x 32 columns of 32-bit TMEM cells: thread i of the warp receives
@@ -312,18 +296,6 @@ __device__ __forceinline__ void tmem_regs_ready128(uint32_t (&r)[128]) {
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// ------------------------------------------------------------------ register split
-// Warpgroup-wide change of the per-thread register budget (PTX setmaxnreg).
-// The warpgroups' shares must add up to at most the block's launch total.
-template <uint32_t N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
 
 // ------------------------------------------------------------------ packed fp32 pairs
 // sm_100+ executes two fp32 FMAs / adds per instruction (operands are register

@@ -21,7 +21,10 @@
 //    streams, or two host threads) race on the array; serialise them.
 //  - The first call on each device looks up the array's device address with
 //    cudaGetSymbolAddress while that device is current and caches it; make that
-//    first call before any stream capture.
+//    first call before any stream capture.  The address belongs to the context
+//    current at that first call (the device's primary context under the
+//    runtime API); cudaDeviceReset() or another context on the same ordinal
+//    would leave the cached address stale, so neither is supported afterwards.
 #include <cuda_runtime.h>
 
 #include <mutex>

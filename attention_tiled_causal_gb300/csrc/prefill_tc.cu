@@ -40,14 +40,6 @@
 #include "common.cuh"
 #include "kernels.h"
 
-// Timeline hook: expands to nothing in the library build; a profiling build
-// may define it to record clock64() stamps of pipeline events.
-#ifndef ATTN_TC_TRACE
-#define ATTN_TC_TRACE(event, j) \
-  do {                           \
-  } while (0)
-#endif
-
 namespace attn {
 namespace tc {
 
@@ -263,7 +255,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       sm.nkv[t] = (cnt + BN - 1) / BN;
       sm.nfull[t] = cnt_first / BN;
     }
-    if (lane == 0) ATTN_TC_TRACE(27, 0);
   }
   if (warp == WARP_MMA_S) tmem_alloc(sm.tmem_slot, TMEM_COLS);
   // K or V tile j into ring slot `slot` (TMA, completion on kv_full[slot]).
@@ -271,7 +262,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   auto load_kv = [&](int slot, bool is_v, int j) {
     const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
     uint8_t* dst = smem + OFF_KV + slot * TILE;
-    ATTN_TC_TRACE(20 + (is_v ? 1 : 0), j);
     mbar_arrive_expect_tx(&sm.kv_full[slot], TILE);
     if (FP8 && is_v) {  // V^T codes [hkv][128][keys]: one box of 128 keys x 128 dims
       tma_load_3d(dst, tm, &sm.kv_full[slot], k_beg + j * BN, 0, g);
@@ -299,7 +289,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // below publishes the initialised barriers to every other role.
   const bool k0_early = Sk > 0;
   if (warp == WARP_TMA && lane == 0) {
-    ATTN_TC_TRACE(26, 0);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.q_full[t], 1);
       mbar_init(&sm.s_full[t], 1);
@@ -343,7 +332,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
-  if (threadIdx.x == 0) ATTN_TC_TRACE(28, 0);
   const int nkv_a = sm.nkv[0], nkv_b = sm.nkv[1];
   const int nkv = max(nkv_a, nkv_b);
 
@@ -402,14 +390,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int t = 0; t < 2 && ok; ++t)
           if (sm.nkv[t] > 0) ok = wait(p.q_cs ? &sm.q_rot[t] : &sm.q_full[t], 0);
         tc_fence_after();
-        ATTN_TC_TRACE(0, 0);
         const uint64_t dQ = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
         const uint64_t dK = sdesc_sw128(smem_u32(smem + OFF_KV), 16, 1024);
         for (int j = 0; j < nkv && ok; ++j) {
           const int iK = ring_pos_k(j), slotK = iK % NSLOT;
           if (!(ok = wait(&sm.kv_full[slotK], (iK / NSLOT) & 1))) break;
           tc_fence_after();
-          ATTN_TC_TRACE(1, j);
           // S_t(j) overwrites S_t(j-1) in TMEM only after the softmax has
           // signalled (s_free) that S_t(j-1) is in its registers.
           for (int t = 0; t < 2; ++t) {
@@ -418,10 +404,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               if (!(ok = wait(&sm.s_free[t], (j - 1) & 1))) break;
               tc_fence_after();
             }
-            ATTN_TC_TRACE(22 + t, j);
             mma_scores<FP8>(tmem + t * BN, dQ + t * kTile16, dK + slotK * kTile16);
             tc_commit_warp(&sm.s_full[t]);
-            ATTN_TC_TRACE(2 + 3 * t, j);
           }
           if (!ok) break;
           tc_commit_warp(&sm.kv_empty[slotK]);  // K_j consumed
@@ -434,16 +418,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int iV = ring_pos_v(j, nkv), slotV = iV % NSLOT;
           if (!(ok = wait(&sm.kv_full[slotV], (iV / NSLOT) & 1))) break;
           tc_fence_after();
-          ATTN_TC_TRACE(6, j);
           for (int t = 0; t < 2; ++t) {
             if (j >= (t ? nkv_b : nkv_a)) continue;
             if (!(ok = wait(&sm.p_full[t], j & 1))) break;
             tc_fence_after();
-            ATTN_TC_TRACE(7 - 4 * t, j);
-            ATTN_TC_TRACE(24 + t, j);
             mma_values<FP8>(tmem + 2 * BN + t * D, dP + t * kTile16, dV + slotV * kTile16, j > 0);
             tc_commit_warp(&sm.o_done[t]);
-            ATTN_TC_TRACE(8 - 4 * t, j);
           }
           if (!ok) break;
           tc_commit_warp(&sm.kv_empty[slotV]);  // V_j consumed
@@ -518,8 +498,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, p.err, DEV_TIMEOUT_SOFTMAX));
       if (!ok) break;
       tc_fence_after();
-      if (row == 0) ATTN_TC_TRACE(10 + t, j);
-      if (lane == 0) ATTN_TC_TRACE(48 + warp, j);
       // Scores: one row of S_t (128 fp32) per thread, in one TMEM load.
       float s[128];
       float mx[8];
@@ -541,7 +519,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
       }
-      if (row == 0) ATTN_TC_TRACE(12 + t, j);
 
       // Causal mask by absolute position, and keys past the sequence: only the
       // tiles from nfull_t on (the diagonal band and a ragged last tile).  Rows
@@ -597,7 +574,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         m_ref = m_new;
       }
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
-      if (row == 0) ATTN_TC_TRACE(14 + t, j);
 
       // P_t (and O_t) are free once O_t += P_t V_{j-1} finished; in the issue
       // order above that MMA precedes S_t(j), so this wait is already satisfied.
@@ -606,7 +582,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      if (row == 0) ATTN_TC_TRACE(32 + t, j);
       // P = exp2(S * scale*log2e - m*scale*log2e), bf16, into the swizzled K-major
       // tile.  The affine step runs on fp32 pairs; the row sum on eight scalar
       // accumulators (key i goes to accumulator i mod 8), which measured faster
@@ -664,7 +639,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int k = 0; k < 4; ++k) f2_unpack(accp[k], acc[2 * k], acc[2 * k + 1]);
       }
       l += ((acc[0] + acc[2]) + (acc[4] + acc[6])) + ((acc[1] + acc[3]) + (acc[5] + acc[7]));
-      if (row == 0) ATTN_TC_TRACE(16 + t, j);
       if (any_grow && j > 0) {
         // O_t *= alpha in TMEM.  tcgen05.st reads its source registers
         // asynchronously, so all four chunks keep their own registers until
@@ -687,8 +661,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.p_full[t]);
-      if (row == 0) ATTN_TC_TRACE(18 + t, j);
-      if (lane == 0) ATTN_TC_TRACE(40 + warp, j);
     }
 
     // epilogue: O / l to global memory, LSE = scale * m + ln l
@@ -761,12 +733,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     if (rv && p.lse) p.lse[(int64_t)(q_beg + rq) * p.hq + h] = l > 0.f ? m_ref * c_row + logf(l) : -INFINITY;
-    if (row == 0) ATTN_TC_TRACE(30 + t, 0);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) ATTN_TC_TRACE(29, 0);
   if (warp == WARP_MMA_S) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);

@@ -12,7 +12,11 @@ as KV-cache GB/s.  `prefill_64k` times 2 x 65536-token causal prefill over all
 heads and over heads 16..31 alone; `chunked` times chunked prefill of 4 x 8192
 new tokens over a 57344-token paged prefix (prefix call + chunk call + merge).
 `prefill_fp8` times the 8K prefill in the FP8 mode (e4m3 Q/K/V codes with
-per-row / per-head scales; the quantisation is inside the step).
+per-row / per-head scales; the quantisation is inside the step).  The line ends
+with `decode`, the decode half of the metric in brief (GB/s, fraction of the
+HBM copy peak, end to end with the queries uploaded and O/LSE read back each
+step, the INT8-cache variant, and the oracle's decode on the host cores);
+`decode_detail` holds the full decode record.
 Inputs are synthetic and seeded (N(0,1)/sqrt(2) bf16).
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on
@@ -470,10 +474,11 @@ def fp8_prefill_arm(wl, args, timer, peaks, peak_src, inputs=None):
     }
 
 
-def decode_arm(wl, args, timer, peaks, peak_src):
+def decode_arm(wl, args, timer, peaks, peak_src, cpu=True):
     import attention_tiled_causal_gb300 as atc
     inp = wl.make("cuda")
     q = inp["q"]
+    q_raw = q.clone()
     po, pl = atc.decode_workspace(wl.batch, wl.hq, wl.splits, wl.d, "cuda")
     out = torch.empty((wl.batch, wl.hq, wl.d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((wl.batch, wl.hq), dtype=torch.float32, device="cuda")
@@ -488,6 +493,19 @@ def decode_arm(wl, args, timer, peaks, peak_src):
             ev[1].record()
 
     ms, ms_kernel = timer.run(step, args.steps, args.warmup, inner=True)
+    # end to end through the public API: each step uploads the new tokens' queries
+    # from pinned host memory and reads O and LSE back; the cache stays resident
+    hq_ = q_raw.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step(ev=()):
+        q.copy_(hq_, non_blocking=True)
+        step()
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    ms_e2e, _ = timer.run(e2e_step, args.steps, args.warmup)
     # the LSE merge of the 16 splits alone (S7), an HBM stream
     ms_merge = short_ms(timer, lambda ev=(): atc.attn_lse_merge(po.permute(2, 0, 1, 3), pl.permute(2, 0, 1), out, lse),
                             args.steps, args.warmup)
@@ -499,8 +517,7 @@ def decode_arm(wl, args, timer, peaks, peak_src):
     alg_step = kv + qb + 2 * part + outb            # cache + q + partials out and back + result
     peak = peaks["hbm_gbs"]
     achieved = alg_step / (ms_kernel * 1e-3) / 1e9  # split + merge kernels (rope of q is ~0.5 MB)
-    del inp
-    return {
+    res = {
         "metric": "decode KV-read GB/s", "unit": "GB/s", "value": round(kv / (ms * 1e-3) / 1e9, 1),
         "ms_per_step": round(ms, 4), "kv_bytes_per_step": kv,
         "workload": wl.name,
@@ -510,9 +527,17 @@ def decode_arm(wl, args, timer, peaks, peak_src):
                      "traffic_scope": "decode_split_kernel (ncu, scaled from a 4-request capture); merge not included",
                      "kernel": "attn::dec::decode_split_kernel + attn::lse_merge_kernel",
                      "kernel_ms": round(ms_kernel, 4), "peak_source": f"{peak_src} HBM copy"},
+        "e2e": {"value": round(kv / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": hq_.numel() * hq_.element_size(),
+                "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
+                "ms_per_step": round(ms_e2e, 4)},
         "gpu_launches_per_step": 3,
         "merge": hbm_line("attn_lse_merge of the 16 decode splits", part + outb, ms_merge, peaks, peak_src),
     }
+    if cpu:
+        res["cpu_baseline"] = oracle_decode_baseline(wl, inp, q_raw)
+    del inp
+    return res
 
 
 def long_prefill_arm(wl, args, timer, peaks, peak_src):
@@ -728,13 +753,79 @@ def synth_rows(seq, n, seed):
     return synth.sample_rows(seq, n, seed)
 
 
-def cpu_baseline(wl, inputs, rows=4096):
+def cpu_baseline(wl, inputs, rows=2048):
     import oracle
     dt, flops = oracle_sample(wl, inputs, rows, 99)
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{rows} seeded query rows x all 64 heads of the 8192-token prefill "
                       f"(RoPE + bf16 rounding + fp64 three-pass attention), {dt:.1f} s"}
+
+
+def oracle_decode_baseline(wl, inp, q_raw, n_req=4, seed=31):
+    """The oracle's decode on n_req seeded requests of the decode workload: RoPE of
+    their queries, bf16 rounding, and the fp64 decode over their pages (gathered
+    from the device cache into logical order first, outside the timed part).
+    Reported in the metric's unit, KV-cache GB/s (bf16 bytes of the pages read)."""
+    import oracle
+    ctx = wl.ctx_lens()
+    picks = np.sort(np.random.default_rng(seed).choice(wl.batch, min(n_req, wl.batch), replace=False))
+    table = inp["page_table"].cpu().numpy()
+    qpos = inp["q_pos"].cpu().numpy()
+    dt, kv = 0.0, 0
+    for b in picks:
+        n = (int(ctx[b]) + 63) // 64
+        pages = torch.from_numpy(table[b, :n].astype(np.int64)).to(inp["k_cache"].device)
+        kc = inp["k_cache"][:, pages].cpu().to(torch.float64).numpy()
+        vc = inp["v_cache"][:, pages].cpu().to(torch.float64).numpy()
+        qb = q_raw[b:b + 1].cpu().to(torch.float64).numpy()
+        t0 = time.perf_counter()
+        qr = oracle.round_bf16(oracle.rope(qb, qpos[b:b + 1], wl.base))
+        oracle.decode_paged(qr, kc, vc, np.arange(n, dtype=np.int32)[None, :], ctx[b:b + 1], n, wl.scale)
+        dt += time.perf_counter() - t0
+        kv += int(ctx[b]) * wl.hkv * wl.d * 2 * 2
+        del kc, vc
+    return {"value": round(kv / dt / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(picks)} seeded requests of the 32 (contexts {', '.join(str(int(ctx[b])) for b in picks)}): "
+                      f"RoPE + bf16 rounding of the query, fp64 decode over all their cached tokens, {dt:.1f} s"}
+
+
+def oracle_tiny_timing(reps=200):
+    """The tiny fp32 workload (B1 S64, 8/2 heads, d64), every row, on one thread
+    and on all threads, repeated `reps` times: RoPE of Q and K plus the fp64
+    three-pass attention."""
+    import oracle
+    import synth
+    w = synth.TINY
+    inp = w.make()
+    q, k, v = (synth.as_f64(inp[n]) for n in ("q", "k", "v"))
+    pos, cu = inp["pos"].numpy(), inp["cu"].numpy()
+    seq = np.zeros(w.seq, np.int32)
+    out = {}
+    nmax = oracle.num_threads()
+    for label, n in (("one_thread", 1), ("all_threads", nmax)):
+        oracle.set_num_threads(n)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle.attention(oracle.rope(q, pos, w.base), seq, pos, oracle.rope(k, pos, w.base), v, cu, pos, w.scale)
+        dt = time.perf_counter() - t0
+        out[label] = {"value": round(w.flops() * reps / dt / 1e9, 3), "unit": "GFLOP/s", "cores": n,
+                      "ms_per_pass": round(dt / reps * 1e3, 3)}
+    oracle.set_num_threads(nmax)
+    out["sample"] = f"all 64 rows x 8 heads of the tiny workload, {reps} passes per thread count"
+    return out
+
+
+def compact_decode(dec):
+    """The decode half of the metric in a few keys, for the end of the line."""
+    i8 = dec.get("int8_cache", {})
+    return {"metric": "decode KV-read GB/s (% HBM peak)", "workload": "B32 ctx U[16K,128K] 64/8 d128, 16 splits",
+            "value": dec["value"], "unit": "GB/s", "frac_of_hbm": round(dec["value"] / dec["roofline"]["peak"], 4),
+            "ms_per_step": dec["ms_per_step"], "kernel_ms": dec["roofline"]["kernel_ms"],
+            "kernel_frac": dec["roofline"]["frac"],
+            "e2e": {k: dec["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+            "int8_cache": {"value": i8.get("value"), "frac": (i8.get("roofline") or {}).get("frac")},
+            "cpu_baseline": dec.get("cpu_baseline")}
 
 
 # ------------------------------------------------------------------ main
@@ -786,7 +877,7 @@ def main():
             import dataclasses
             dwl = dataclasses.replace(dwl, batch=args.decode_requests,
                                       name=dwl.name.replace("B32", f"B{args.decode_requests}"))
-        dec = decode_arm(dwl, args, timer, peaks, peak_src)
+        dec = decode_arm(dwl, args, timer, peaks, peak_src, cpu=not args.no_cpu_baseline)
         torch.cuda.empty_cache()
         dwl8 = synth.DECODE_INT8
         if args.decode_requests:
@@ -826,21 +917,24 @@ def main():
                      "config": prefill_config(wl, ws),
                      "roofline": res["roofline"], "e2e": res["e2e"], "clocks": clocks,
                      "launch": res["launch"], "gpu_launches": res["launches_per_step"] * args.steps})
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl, res["inputs"])
+        line["rope"] = res["rope"]
     else:
         line.update({"value": dec["value"], "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
                      "warmup": args.warmup, "ms_per_step": dec["ms_per_step"], "higher_is_better": True,
                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                     "config": {"workload": dec["workload"]}, "roofline": dec["roofline"],
-                     "gpu_launches": dec["gpu_launches_per_step"] * args.steps,
-                     "merge": dec["merge"], "cached_tokens_per_s": dec["cached_tokens_per_s"],
-                     "int8_cache": dec["int8_cache"]})
-    if res:
-        line["rope"] = res["rope"]
-    if dec and res:
-        line["decode"] = dec
+                     "config": {"workload": dec["workload"]}, "roofline": dec["roofline"], "e2e": dec["e2e"],
+                     "gpu_launches": dec["gpu_launches_per_step"] * args.steps})
+        if "cpu_baseline" in dec:
+            line["cpu_baseline"] = dec["cpu_baseline"]
     line.update(extra)
-    if res and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, res["inputs"])
+    if dec:
+        line["decode_detail"] = dec
+    if not args.no_cpu_baseline:
+        line["oracle_tiny"] = oracle_tiny_timing()
+    if dec:
+        line["decode"] = compact_decode(dec)  # last: the decode half of the metric in brief
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()

@@ -6,7 +6,9 @@
  * --------------------------------
  *  - All tensor and table pointers are DEVICE pointers owned by the caller.
  *    The library never allocates or frees caller memory and keeps no state
- *    between calls apart from cached per-device constants.
+ *    between calls apart from cached per-device constants -- except
+ *    attn_decode_paged_noalloc, whose calls share one static scratch array per
+ *    device and leave their partials in it.
  *  - Tensors are packed row-major with the head dimension contiguous:
  *    Q/K/V/O as [tokens][heads][head_dim] ("Ulysses sequence parallelism for
  *    inference", section 2.2: Q/K/V shaped [seq, heads, head_dim]).
@@ -17,7 +19,15 @@
  *  - Faults found on the device (a page id outside the cache, a pipeline wait
  *    that ran out of time) never trap: the kernel records a code that
  *    attn_device_status() returns after the work has finished.
- *  - Calls on different streams may run concurrently; they share no scratch.
+ *  - Calls on different streams may run concurrently and share no scratch,
+ *    except attn_decode_paged_noalloc: its calls share one static array per
+ *    device, so overlapping calls of it must be serialised.
+ *  - Cached per-device addresses (the device error word, the no-alloc scratch)
+ *    are looked up once per device ordinal in the context current at the
+ *    first call -- the device's primary context, under the CUDA runtime.
+ *    cudaDeviceReset() or a switch to another context on that ordinal
+ *    invalidates them; the library does not support either after its first
+ *    call on a device.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -70,8 +80,11 @@ ATTN_API int attn_device_status(int clear);
  *     a = positions[t] * base^(-2i/head_dim)
  *     x[i]          <- x[i] cos a - x[i + head_dim/2] sin a
  *     x[i + d/2]    <- x[i + d/2] cos a + x[i] sin a
- * The rotation is computed in fp32 from an angle reduced in fp64, and the
- * result is stored back in the tensor's dtype (bf16: round to nearest even).
+ * The angle is reduced exactly: base^(-2i/d) / 2pi is held as a 64-bit
+ * fixed-point fraction of a turn, the phase of position p is the low 64 bits
+ * of the integer product p * theta_i, and its top 32 bits give the angle in
+ * turns for sincospif.  The rotation itself is computed in fp32 and stored back
+ * in the tensor's dtype (bf16: round to nearest even).
  *
  *  x            [tokens][heads][head_dim] of `dtype`, row t at x + t*stride_token
  *               elements; 16-byte aligned; rotated in place.
@@ -351,7 +364,11 @@ ATTN_API int attn_decode_paged(const void *q, const void *k_cache, const void *v
  *  contents (no part of it needs to start at zero); calls that overlap on the
  *  GPU race on it, so serialise them.  The first call on a device looks up the
  *  scratch's device address (cudaGetSymbolAddress) with that device current;
- *  make that first call before any stream capture.
+ *  make that first call before any stream capture.  The address found is that
+ *  of the context current then (the primary context under the runtime API) and
+ *  is kept for the device ordinal: after cudaDeviceReset(), or under another
+ *  context on the same ordinal, it is stale, so neither is supported once this
+ *  call has run on a device.
  */
 ATTN_API int attn_decode_paged_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                        const int32_t *page_table, const int32_t *ctx_lens, int batch,

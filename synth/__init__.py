@@ -106,6 +106,29 @@ def shuffled_page_table(ctx_lens, seed: int, page: int = PAGE, max_pages: Option
     return table, total
 
 
+def shard_rows(seq_len: int, world: int, rank: int, kind: str) -> np.ndarray:
+    """Token rows that rank `rank` of `world` holds when one sequence is split
+    along the sequence axis (SGLang partitioning page, section 3.5):
+
+      contiguous  rows [rank*c, (rank+1)*c), c = seq_len / world;
+      striped     rows rank, rank + world, rank + 2*world, ...;
+      zigzag      the sequence cut into 2*world chunks of c = seq_len / (2*world)
+                  rows; rank r holds chunks r and 2*world-1-r, so every rank
+                  gets one early and one late chunk of the causal triangle.
+
+    Rows come back sorted, so their positions stay non-decreasing."""
+    if kind == "contiguous":
+        c = seq_len // world
+        return np.arange(rank * c, (rank + 1) * c, dtype=np.int64)
+    if kind == "striped":
+        return np.arange(rank, seq_len, world, dtype=np.int64)
+    if kind == "zigzag":
+        c = seq_len // (2 * world)
+        a, b = rank, 2 * world - 1 - rank
+        return np.concatenate([np.arange(a * c, (a + 1) * c), np.arange(b * c, (b + 1) * c)]).astype(np.int64)
+    raise ValueError(f"unknown partition {kind!r}")
+
+
 def sample_rows(seq_len: int, n: int, seed: int) -> np.ndarray:
     """`n` distinct sorted rows of [0, seq_len), always holding the first and last
     row and the rows on either side of the first few 128-row tile edges."""

@@ -9,7 +9,6 @@ bf16-rounded rotated Q/K; the oracle models that step by rounding its own fp64
 rotation to bf16 (ties to even) before its three-pass attention.
 """
 import math
-import os
 
 import numpy as np
 import pytest
@@ -246,24 +245,16 @@ def _bf16_case(lens, hq, hkv, starts, seed, d=128):
     return q, k, v, pos, cu
 
 
-def _run_prefill(q, k, v, pos, cu, lens, causal=True, h_lo=0, h_hi=None, out_dtype=None, simt=False):
+def _run_prefill(q, k, v, pos, cu, lens, causal=True, h_lo=0, h_hi=None, out_dtype=None):
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
     posd, cud = torch.from_numpy(pos).to(DEV), torch.from_numpy(cu).to(DEV)
     atc.rope_apply(qd, posd)
     atc.rope_apply(kd, posd)
     out = torch.full(q.shape, float("nan"), dtype=out_dtype or q.dtype, device=DEV)
     lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
-    old = os.environ.get("ATTN_GB300_FORCE_SIMT")
-    os.environ["ATTN_GB300_FORCE_SIMT"] = "1" if simt else "0"
-    try:
-        atc.attn_prefill(qd, kd, vd, out, lse, cud, posd, max(lens), cu_k=cud, k_pos=posd, h_lo=h_lo, h_hi=h_hi,
-                         causal=causal)
-        atc.attn_device_status()
-    finally:
-        if old is None:
-            del os.environ["ATTN_GB300_FORCE_SIMT"]
-        else:
-            os.environ["ATTN_GB300_FORCE_SIMT"] = old
+    atc.attn_prefill(qd, kd, vd, out, lse, cud, posd, max(lens), cu_k=cud, k_pos=posd, h_lo=h_lo, h_hi=h_hi,
+                     causal=causal)
+    atc.attn_device_status()
     return out, lse
 
 
@@ -297,12 +288,14 @@ def test_prefill_tc_non_causal_and_fp32_output():
     check(out, lse, want_o, want_l, what="tc non-causal fp32 out")
 
 
-def test_prefill_simt_bf16_matches_oracle():
+@pytest.mark.parametrize("d", [64, 256])
+def test_prefill_simt_bf16_matches_oracle(d):
+    """bf16 at head sizes other than 128 runs on the CUDA-core kernel."""
     lens = [150, 77]
-    q, k, v, pos, cu = _bf16_case(lens, 16, 2, [0, 3], 302)
-    out, lse = _run_prefill(q, k, v, pos, cu, lens, simt=True)
-    want_o, want_l = _oracle_prefill(q, k, v, pos, cu, lens, 128 ** -0.5)
-    check(out, lse, want_o, want_l, what="simt bf16")
+    q, k, v, pos, cu = _bf16_case(lens, 16, 2, [0, 3], 302, d=d)
+    out, lse = _run_prefill(q, k, v, pos, cu, lens)
+    want_o, want_l = _oracle_prefill(q, k, v, pos, cu, lens, d ** -0.5)
+    check(out, lse, want_o, want_l, what=f"simt bf16 d{d}")
 
 
 def test_prefill_tc_head_slices_are_bit_identical_to_full_call():
@@ -1149,3 +1142,147 @@ def test_paged_prefill_fp32_output_head_slice_matches_oracle():
                                       h_lo=8, h_hi=16)
     check(out[:, 8:16], lse[:, 8:16], want_o[:, 8:16], want_l[:, 8:16], what="paged fp32 head slice")
     assert torch.isnan(out[:, :8]).all() and torch.isnan(lse[:, 8:16]).sum() == 0
+
+
+# ------------------------------------------------------------------ key shards with position gaps
+
+def _shard_case(T, hq, hkv, seed):
+    q = synth.randn((T, hq, 128), seed, 0.7071)
+    k = synth.randn((T, hkv, 128), seed + 1, 0.7071)
+    v = synth.randn((T, hkv, 128), seed + 2, 0.7071)
+    return q, k, v, np.arange(T, dtype=np.int32)
+
+
+def _rows_call(fn, q, k, v, pos, qrows, krows, out_dtype=torch.float32):
+    """One attn_prefill(-like) call of the queries `qrows` against the keys
+    `krows` of one sequence (both sorted), at their absolute positions."""
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(DEV)
+    qi, ki = torch.from_numpy(qrows).to(DEV), torch.from_numpy(krows).to(DEV)
+    cu_q, cu_k = i32([0, len(qrows)]), i32([0, len(krows)])
+    return fn(q[qi].contiguous(), k[ki].contiguous(), v[ki].contiguous(), cu_q, i32(pos[qrows]), len(qrows), cu_k,
+              i32(pos[krows]), out_dtype)
+
+
+def _bf16_call(q, k, v, cu_q, qpos, maxq, cu_k, kpos, out_dtype):
+    out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=DEV)
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    atc.attn_prefill(q, k, v, out, lse, cu_q, qpos, maxq, cu_k=cu_k, k_pos=kpos)
+    atc.attn_device_status()
+    return out, lse
+
+
+@pytest.mark.parametrize("kind,world", [("striped", 2), ("zigzag", 2), ("striped", 3), ("zigzag", 3)])
+def test_prefill_tc_key_shards_with_position_gaps(kind, world):
+    """Ring-attention steps (SGLang page, section 3.5): the queries of one rank's
+    shard against the keys of every rank's shard, striped (token % N) or zigzag
+    (blocks r and 2N-1-r of 2N).  Key positions jump inside 128-key tiles, so the
+    kernel's extent search leaves its consecutive-position guess for the
+    warp-wide search and the per-tile mask meets the gaps; some shard pairs leave
+    rows with no visible key.  Every partial matches the oracle on the same rows
+    and keys, and the shards' partials merged by attn_lse_merge match the oracle's
+    unsplit result for those queries."""
+    T = 2 * world * 300  # zigzag blocks of 300 rows: a gap falls inside a key tile
+    q, k, v, pos = _shard_case(T, 16, 2, 1200 + world)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    posd = torch.from_numpy(pos).to(DEV)
+    atc.rope_apply_qk(qd, kd, posd)
+    qr, kr, vf = rotated_bf16(q, pos), rotated_bf16(k, pos), synth.as_f64(v)
+    for rq in range(world):
+        qrows = synth.shard_rows(T, world, rq, kind)
+        po, pl = [], []
+        for rk in range(world):
+            krows = synth.shard_rows(T, world, rk, kind)
+            o, l = _rows_call(_bf16_call, qd, kd, vd, pos, qrows, krows)
+            wo, wl = oracle.attention(qr[qrows], np.zeros(len(qrows), np.int32), pos[qrows], kr[krows], vf[krows],
+                                      [0, len(krows)], pos[krows], 128 ** -0.5)
+            check(o, l, wo, wl, what=f"{kind} q{rq} k{rk}")
+            po.append(o)
+            pl.append(l)
+        out = torch.empty_like(po[0])
+        lse = torch.empty_like(pl[0])
+        atc.attn_lse_merge(torch.stack(po), torch.stack(pl), out, lse)
+        atc.attn_device_status()
+        wo, wl = oracle.attention(qr[qrows], np.zeros(len(qrows), np.int32), pos[qrows], kr, vf, [0, T], pos,
+                                  128 ** -0.5)
+        check(out, lse, wo, wl, what=f"{kind} q{rq} merged over {world} key shards")
+
+
+def test_prefill_tc_gapped_shards_in_one_varlen_call():
+    """Two sequences in one call, each a different rank's shard with gaps (a
+    striped one, then a zigzag one whose key count is not a multiple of 128), so
+    the search runs on a key range that starts inside the packed buffer."""
+    T = 1320
+    q, k, v, pos = _shard_case(T, 64, 8, 1210)
+    s_rows = synth.shard_rows(T, 4, 1, "striped")
+    z_rows = synth.shard_rows(T, 2, 1, "zigzag")
+    qrows = np.concatenate([s_rows, z_rows])
+    krows = np.concatenate([synth.shard_rows(T, 4, 3, "striped"), synth.shard_rows(T, 2, 0, "zigzag")])
+    nq = [len(s_rows), len(z_rows)]
+    nk = [len(krows) - len(z_rows), len(z_rows)]
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    posd = torch.from_numpy(pos).to(DEV)
+    atc.rope_apply_qk(qd, kd, posd)
+    qi, ki = torch.from_numpy(qrows).to(DEV), torch.from_numpy(krows).to(DEV)
+    cu_q, cu_k = synth.cu_seqlens(nq), synth.cu_seqlens(nk)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(DEV)
+    out, lse = _bf16_call(qd[qi].contiguous(), kd[ki].contiguous(), vd[ki].contiguous(), i32(cu_q), i32(pos[qrows]),
+                          max(nq), i32(cu_k), i32(pos[krows]), torch.bfloat16)
+    qr, kr = rotated_bf16(q, pos), rotated_bf16(k, pos)
+    wo, wl = oracle.attention(qr[qrows], seq_ids(nq), pos[qrows], kr[krows], synth.as_f64(v)[krows], cu_k,
+                              pos[krows], 128 ** -0.5)
+    check(out, lse, wo, wl, what="gapped shards, varlen")
+
+
+def _fp8_call(q, k, v, cu_q, qpos, maxq, cu_k, kpos, out_dtype):
+    cq, sq = atc.quant_fp8_rows(q)
+    ck, sk = atc.quant_fp8_heads(k)
+    cv, sv = atc.quant_fp8_heads(v, transposed=True)
+    out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=DEV)
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    atc.attn_prefill_fp8(cq, sq, ck, sk, cv, sv, out, lse, cu_q, qpos, maxq, cu_k, kpos)
+    atc.attn_device_status()
+    return out, lse
+
+
+@pytest.mark.parametrize("kind", ["striped", "zigzag"])
+def test_prefill_fp8_key_shards_with_position_gaps(kind):
+    """The striped / zigzag ring steps on the e4m3 kernel: each shard's rotated
+    Q, K, V quantised on their own (a key shard has its own per-head scales),
+    compared with the oracle over the dequantised shard inputs; the merged shards
+    equal the oracle over every shard's dequantised keys and values at once."""
+    world, T = 2, 1200
+    q, k, v, pos = _shard_case(T, 16, 2, 1220)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    posd = torch.from_numpy(pos).to(DEV)
+    atc.rope_apply_qk(qd, kd, posd)
+    qb, kb, vb = (synth.as_f64(t.cpu()) for t in (qd, kd, vd))  # the rotated bf16 inputs both sides quantise
+    deq = {}
+    for r in range(world):
+        rows = synth.shard_rows(T, world, r, kind)
+        ck, sk = oracle.quant_e4m3(kb[rows], [1])
+        cv, sv = oracle.quant_e4m3(vb[rows], [1])
+        deq[r] = (rows, ck * sk.astype(np.float64)[None, :, None], cv * sv.astype(np.float64)[None, :, None])
+    for rq in range(world):
+        qrows = synth.shard_rows(T, world, rq, kind)
+        cq, sq = oracle.quant_e4m3(qb[qrows], [0, 1])
+        qh = cq * sq.astype(np.float64)[:, :, None]
+        po, pl = [], []
+        for rk in range(world):
+            krows, kh, vh = deq[rk]
+            o, l = _rows_call(_fp8_call, qd, kd, vd, pos, qrows, krows)
+            wo, wl = oracle.attention(qh, np.zeros(len(qrows), np.int32), pos[qrows], kh, vh, [0, len(krows)],
+                                      pos[krows], 128 ** -0.5)
+            check(o, l, wo, wl, tol_max=_fp8_max_tol(vh), tol_mean=FP8_MEAN, what=f"fp8 {kind} q{rq} k{rk}")
+            po.append(o)
+            pl.append(l)
+        out = torch.empty_like(po[0])
+        lse = torch.empty_like(pl[0])
+        atc.attn_lse_merge(torch.stack(po), torch.stack(pl), out, lse)
+        atc.attn_device_status()
+        krows = np.concatenate([deq[r][0] for r in range(world)])
+        kh = np.concatenate([deq[r][1] for r in range(world)])
+        vh = np.concatenate([deq[r][2] for r in range(world)])
+        order = np.argsort(krows, kind="stable")
+        wo, wl = oracle.attention(qh, np.zeros(len(qrows), np.int32), pos[qrows], kh[order], vh[order], [0, T],
+                                  pos[krows[order]], 128 ** -0.5)
+        check(out, lse, wo, wl, tol_max=_fp8_max_tol(vh), tol_mean=FP8_MEAN, what=f"fp8 {kind} q{rq} merged")

@@ -6,9 +6,15 @@ partials in a scratch array the library holds statically, and must give the
 same answer as attn_decode_paged with a caller-supplied workspace -- also on a
 second call, after the first call has left its own data in that scratch.
 
-This file is named to be collected last; it also runs alone in a fresh process.
+This file is named to be collected last, so a run that stops at the first
+failure has run every other test before it.  One test repeats the two-call
+check in a fresh Python process, so the entry point's first call on a device
+(the scratch address lookup) is covered without anything loaded before it.
 """
 import ctypes as C
+import os
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -68,7 +74,7 @@ def _close(out, lse, ref_o, ref_l):
     assert (lse[~inf] - ref_l[~inf]).abs().max().item() <= TOL_LSE
 
 
-def test_noalloc_decode_matches_workspace_decode_on_two_calls_in_a_row():
+def _two_calls_in_a_row():
     atc.attn_device_status(clear=True)
     lib, f = _entry()
     # first call: many splits over long contexts fills a large part of the scratch
@@ -81,6 +87,45 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls_in_a_row():
         out, lse = _noalloc(f, lib, wl, inp, q)
         atc.attn_device_status()
         _close(out, lse, ref_o, ref_l)
+
+
+def test_noalloc_decode_matches_workspace_decode_on_two_calls_in_a_row():
+    _two_calls_in_a_row()
+
+
+def test_noalloc_decode_in_a_fresh_process():
+    """The same two calls as the first thing a new process does on the GPU."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys; sys.path.insert(0, %r); sys.path.insert(0, %r); "
+            "import test_zz_no_alloc as t; t._two_calls_in_a_row(); print('fresh ok')"
+            % (root, os.path.join(root, "tests")))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "fresh ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+def test_noalloc_decode_allocates_no_device_memory():
+    """After a first call (module load, scratch address lookup), further calls
+    leave both the caching allocator's count and the device's free memory as
+    they were: the entry point calls no allocator."""
+    lib, f = _entry()
+    wl, inp, q = _case([3000, 64, 9000], 64, 8, 16, 703)
+    out = torch.empty((wl.batch, wl.hq, wl.d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((wl.batch, wl.hq), dtype=torch.float32, device=DEV)
+    table = inp["page_table"]
+    args = (q.data_ptr(), inp["k_cache"].data_ptr(), inp["v_cache"].data_ptr(), table.data_ptr(),
+            inp["ctx_lens"].data_ptr(), wl.batch, table.shape[1], 64, inp["num_pages"], wl.hq, wl.hkv, wl.d,
+            wl.splits, wl.scale, out.data_ptr(), 0, lse.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert f(*args) == 0, lib.attn_last_error().decode()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for _ in range(3):
+        assert f(*args) == 0, lib.attn_last_error().decode()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+    atc.attn_device_status()
 
 
 def test_noalloc_decode_rejects_calls_beyond_the_static_scratch():
