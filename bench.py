@@ -762,7 +762,7 @@ def cpu_baseline(wl, inputs, rows=2048):
                       f"(RoPE + bf16 rounding + fp64 three-pass attention), {dt:.1f} s"}
 
 
-def oracle_decode_baseline(wl, inp, q_raw, n_req=4, seed=31):
+def oracle_decode_baseline(wl, inp, q_raw, n_req=16, seed=31):
     """The oracle's decode on n_req seeded requests of the decode workload: RoPE of
     their queries, bf16 rounding, and the fp64 decode over their pages (gathered
     from the device cache into logical order first, outside the timed part).
