@@ -1,7 +1,8 @@
 """Benchmark of the attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload all|prefill|decode|long|chunked|fp8] [--no-cpu-baseline] [--decode-requests N]
+                    [--workload all|prefill|decode|long|chunked|fp8|append] [--no-cpu-baseline]
+                    [--decode-requests N]
 
 Headline (the JSON `value`): causal GQA prefill, batch 1 x 8192 tokens, 64 query /
 8 KV heads, head_dim 128, bf16 -- one step = RoPE of Q and K at absolute
@@ -675,6 +676,41 @@ def chunked_arm(wl, args, timer, peaks, peak_src):
                                         append8_bytes, ms_a8, peaks, peak_src)}}
 
 
+def append_arm(wl, args, timer, peaks, peak_src):
+    """The chunked workload's cache appends alone: 4 x 8192 new tokens' keys
+    (rotated at positions 57344..65535) and values written through a shuffled
+    page table into a bf16 cache (attn_kv_append_paged) and into an INT8 cache
+    (attn_kv_append_paged_int8).  Small enough for a profiler capture."""
+    import attention_tiled_causal_gb300 as atc
+    import synth
+    B, P, C = wl.batch, wl.prefix, wl.chunk
+    T = B * C
+    table, npg = synth.shuffled_page_table([P + C] * B, wl.seed * 16 + 10)
+    k_raw = synth.randn((T, wl.hkv, wl.d), wl.seed * 16 + 2, wl.std, device="cuda")
+    v = synth.randn((T, wl.hkv, wl.d), wl.seed * 16 + 3, wl.std, device="cuda")
+    qpos = torch.arange(P, P + C, dtype=torch.int32).repeat(B)
+    pages = torch.from_numpy(table).long()[torch.arange(B).repeat_interleave(C), (qpos // synth.PAGE).long()]
+    slots = (pages * synth.PAGE + (qpos % synth.PAGE).long()).to(torch.int32).cuda()
+    qposd = qpos.cuda()
+    kc = torch.zeros((wl.hkv, npg, synth.PAGE, wl.d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    kc8 = torch.zeros((wl.hkv, npg, synth.PAGE, wl.d), dtype=torch.int8, device="cuda")
+    vc8 = torch.zeros_like(kc8)
+    ks8 = torch.zeros((wl.hkv, npg, synth.PAGE), dtype=torch.float32, device="cuda")
+    vs8 = torch.zeros_like(ks8)
+    ms_a = short_ms(timer, lambda ev=(): atc.attn_kv_append_paged(k_raw, v, qposd, slots, kc, vc), args.steps,
+                    args.warmup)
+    ms_a8 = short_ms(timer, lambda ev=(): atc.attn_kv_append_paged_int8(k_raw, v, qposd, slots, kc8, vc8, ks8, vs8),
+                     args.steps, args.warmup)
+    atc.attn_device_status()
+    append_bytes = 2 * 2 * k_raw.numel() * 2
+    append8_bytes = 2 * k_raw.numel() * 2 + 2 * (k_raw.numel() + k_raw.numel() // wl.d * 4)
+    return {"append": hbm_line("attn_kv_append_paged (4 x 8192 tokens, 8 KV heads)", append_bytes, ms_a, peaks,
+                               peak_src),
+            "append_int8": hbm_line("attn_kv_append_paged_int8 (the same chunk into an INT8 cache)", append8_bytes,
+                                    ms_a8, peaks, peak_src)}
+
+
 def decode_int8_arm(wl, args, timer, peaks, peak_src):
     """The decode workload over an INT8 cache (codes + one fp32 scale per KV head and
     token): half the bytes per cached token."""
@@ -836,7 +872,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="all", choices=["all", "prefill", "decode", "long", "chunked", "fp8"])
+    ap.add_argument("--workload", default="all", choices=["all", "prefill", "decode", "long", "chunked", "fp8", "append"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-requests", type=int, default=None,
                     help="decode workload with fewer requests (first N of the seeded 32); for small profiler captures")
@@ -897,6 +933,8 @@ def main():
     if args.workload in ("all", "chunked"):
         extra["chunked"] = chunked_arm(synth.CHUNKED, args, timer, peaks, peak_src)
         torch.cuda.empty_cache()
+    if args.workload == "append":
+        extra["append"] = append_arm(synth.CHUNKED, args, timer, peaks, peak_src)
     if not res and not dec:  # a single secondary workload (profiling): print its own object
         if rank == 0:
             print(json.dumps(extra), flush=True)
