@@ -21,14 +21,19 @@ Entry points (same names as the C ABI):
     attn_decode_paged(q, k_cache, v_cache, ...)         split-KV decode over a paged cache
     attn_decode_paged_int8(q, k_codes, v_codes, k_scale, v_scale, ...)   the same over an INT8 cache
     attn_lse_merge(part_out, part_lse, out, lse, ...)   log-sum-exp merge of partials
+
+Sequence parallelism around the kernels (host code over torch.distributed):
+    sp.ulysses_attention / sp.seq_to_heads / sp.heads_to_seq   the Ulysses all-to-all
+    sp.ring_attention / sp.shard_rows                          ring context parallelism
 """
 from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_decode_paged_int8,
                        attn_device_status,
                        attn_kv_append_paged, attn_kv_append_paged_int8, attn_lse_merge, attn_prefill, attn_prefill_fp8,
                        decode_workspace, lib_path, library, prefill, quant_fp8_heads, quant_fp8_rows, rope_apply, rope_apply_qk, rope_quant_fp8_heads,
                        rope_quant_fp8_rows, rope_table)
+from . import sp
 
 __all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_decode_paged_int8", "attn_device_status",
            "attn_kv_append_paged", "attn_kv_append_paged_int8", "attn_lse_merge", "attn_prefill", "attn_prefill_fp8", "decode_workspace", "lib_path", "library",
            "prefill", "quant_fp8_heads", "quant_fp8_rows", "rope_apply", "rope_apply_qk", "rope_quant_fp8_heads",
-           "rope_quant_fp8_rows", "rope_table"]
+           "rope_quant_fp8_rows", "rope_table", "sp"]

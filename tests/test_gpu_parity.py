@@ -1286,3 +1286,28 @@ def test_prefill_fp8_key_shards_with_position_gaps(kind):
         wo, wl = oracle.attention(qh, np.zeros(len(qrows), np.int32), pos[qrows], kh[order], vh[order], [0, T],
                                   pos[krows[order]], 128 ** -0.5)
         check(out, lse, wo, wl, tol_max=_fp8_max_tol(vh), tol_mean=FP8_MEAN, what=f"fp8 {kind} q{rq} merged")
+
+
+# ------------------------------------------------------------------ sequence-parallel callables
+
+def test_sp_kernel_callables_single_rank():
+    """attention_tiled_causal_gb300.sp on one rank (no exchange): Ulysses with the
+    tensor-core kernel as its per-rank attention, and the ring with the kernel's
+    fp32 partials and the merge kernel, over a zigzag shard's queries, match the
+    oracle."""
+    from attention_tiled_causal_gb300 import sp
+    T = 600
+    q, k, v, pos = _shard_case(T, 16, 2, 1230)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    posd = torch.from_numpy(pos).to(DEV)
+    atc.rope_apply_qk(qd, kd, posd)
+    out, lse = sp.ulysses_attention(qd, kd, vd, posd)
+    atc.attn_device_status()
+    qr, kr, vf = rotated_bf16(q, pos), rotated_bf16(k, pos), synth.as_f64(v)
+    wo, wl = oracle.attention(qr, np.zeros(T, np.int32), pos, kr, vf, [0, T], pos, 128 ** -0.5)
+    check(out, lse, wo, wl, what="sp.ulysses_attention, one rank")
+    rows = sp.shard_rows(T, 2, 1, "zigzag")
+    ri = torch.from_numpy(rows).to(DEV)
+    out, lse = sp.ring_attention(qd[ri].contiguous(), kd, vd, posd[ri].contiguous(), posd)
+    atc.attn_device_status()
+    check(out, lse, wo[rows], wl[rows], what="sp.ring_attention, one rank")
