@@ -44,23 +44,32 @@ namespace attn {
 namespace tc {
 
 constexpr int BM = 128, BN = 128, D = 128;
-constexpr int NSLOT = 3;
-constexpr int NBAR = 18;
 constexpr int HALF = 16384;  // one 128-byte-swizzled TMA box: 128 rows x 128 bytes
 
 // Tile geometry of the two element types.  bf16: a 128 x 128 tile is two
 // boxes of 64 elements (32 KB); an MMA k-step is 16 elements.  e4m3: one box of
 // 128 elements (16 KB); a k-step is 32 elements.  Both step through a
 // 128-byte swizzle row 32 bytes at a time.
+//
+// PBUF is the number of P buffers per query tile.  With two, the softmax could
+// write P_t(j) while O_t += P_t(j-1) V_{j-1} still reads the other; the e4m3
+// tiles leave room for that (bf16 does not: 224 KB of 227 are in use), but it
+// measured slower (1755 against 1881 TFLOP/s on the 8K workload), so both
+// kernels keep one.  The barriers are indexed per buffer either way.
 template <bool FP8>
 struct Cfg {
   static constexpr int TILE = FP8 ? 16384 : 32768;
   static constexpr int NBOX = FP8 ? 1 : 2;
   static constexpr int KSTEPS = FP8 ? 4 : 8;
+  static constexpr int NSLOT = 3;
+  static constexpr int PBUF = 1;
+  // barriers: q_full[2], k_full[NSLOT], v_full[NSLOT], kv_empty[NSLOT],
+  // s_full[2], s_free[2], p_full[2][PBUF], o_done[2][PBUF], q_rot[2]
+  static constexpr int NBAR = 2 + 3 * NSLOT + 2 + 2 + 4 * PBUF + 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * TILE;
   static constexpr int OFF_P = OFF_KV + NSLOT * TILE;
-  static constexpr int OFF_BAR = OFF_P + 2 * TILE;
+  static constexpr int OFF_BAR = OFF_P + 2 * PBUF * TILE;
   static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 32 + 1024;
 };
 // 12 warps = 3 warpgroups.  The register file is split across the SM's four
@@ -76,15 +85,31 @@ constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);    // P K-majo
 // P V reads V^T rows (values stored transposed), since 8-bit MMA operands are K-major.
 constexpr uint32_t IDESC_FP8 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 constexpr float kRescaleLog2 = 8.f;
+// The e4m3 kernel's lazy reference (see the softmax loop) keeps a tile whose
+// weight sum is at most this: every weight is then <= 256, inside e4m3's 448.
+constexpr float kLazySumFp8 = 256.f;
+// Register split of the e4m3 kernel: the producer / issuer warpgroup drops to
+// REGS_SIDE so the two softmax warpgroups can hold a tile's scores through the
+// lazy pass (2 x REGS_SOFTMAX + REGS_SIDE <= 3 x REGS_LAUNCH per thread).
+constexpr uint32_t REGS_SOFTMAX = 200, REGS_SIDE = 88;
+static_assert(2 * REGS_SOFTMAX + REGS_SIDE <= 3 * 168, "register split exceeds the launch total");
 
+// Every mbarrier below is waited on by one role only, and that role waits for
+// every phase in turn, so no barrier ever runs two phases ahead of its waiter
+// (a parity wait cannot tell phase k from phase k+2).  That is why a ring slot
+// has one "full" barrier for K tiles and one for V tiles: the slot alternates
+// between K and V, whose consumers are different warps, and one shared
+// barrier could run ahead of the warp that skipped the other kind's fills.
+// For the same reason p_full and o_done have one barrier per P buffer.
 struct Smem {
   uint64_t* q_full;    // [2]  TMA -> MMA: Q tile landed
-  uint64_t* kv_full;   // [3]  TMA -> MMA: ring slot landed
-  uint64_t* kv_empty;  // [3]  MMA -> TMA: ring slot consumed
+  uint64_t* k_full;    // [NSLOT]  TMA -> score MMA: a K tile landed in the slot
+  uint64_t* v_full;    // [NSLOT]  TMA -> value MMA: a V tile landed in the slot
+  uint64_t* kv_empty;  // [NSLOT]  MMA -> TMA: ring slot consumed
   uint64_t* s_full;    // [2]  MMA -> softmax: S_t ready in TMEM
   uint64_t* s_free;    // [2]  softmax -> MMA: S_t read out of TMEM (128 arrivals)
-  uint64_t* p_full;    // [2]  softmax -> MMA: P_t written, O_t rescaled (128 arrivals)
-  uint64_t* o_done;    // [2]  MMA -> softmax: O_t += P_t V_j finished
+  uint64_t* p_full;    // [2][PBUF]  softmax -> MMA: P_t written, O_t rescaled (128 arrivals)
+  uint64_t* o_done;    // [2][PBUF]  MMA -> softmax: O_t += P_t V_j finished (buffer j % PBUF)
   uint64_t* q_rot;     // [2]  softmax -> MMA: Q_t rotated in place (128 arrivals; only when RoPE is fused)
   uint32_t* tmem_slot;
   int* nkv;            // [2]  K/V tiles each query tile needs
@@ -141,6 +166,64 @@ __device__ int count_le_warp(const int32_t* k_pos, int n, int qp, int lane) {
   return lo;
 }
 
+// Row max of 128 scores over eight independent chains of 3-input maxima.
+__device__ __forceinline__ float row_max128(const float (&s)[128]) {
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+#pragma unroll
+  for (int c = 24; c < 120; c += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[120 + i]);
+  return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+}
+
+// One row of e4m3 softmax weights P = exp2(S * c*log2e - mb), sixteen keys per
+// 16-byte chunk of the swizzled K-major P tile (prow = this row's 128-byte
+// line); returns their sum, taken on four fp32 pairs (pair k holds
+// accumulators 2k and 2k+1).
+__device__ __forceinline__ float weights_e4m3(const float (&s)[128], float sl2, float mb, uint8_t* prow, int row) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), nmbx2 = f2_pack(-mb, -mb);
+  uint64_t accp[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) accp[k] = f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int c16 = 0; c16 < 8; ++c16) {
+    float e[16];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(s[c16 * 16 + i], s[c16 * 16 + i + 1]), sl2x2, nmbx2), x0, x1);
+      e[i] = fast_exp2(x0);
+      e[i + 1] = fast_exp2(x1);
+      accp[(i >> 1) & 3] = f2_add(accp[(i >> 1) & 3], f2_pack(e[i], e[i + 1]));
+    }
+    uint4 v;
+    v.x = (uint32_t)pack_e4m3x2(e[0], e[1]) | ((uint32_t)pack_e4m3x2(e[2], e[3]) << 16);
+    v.y = (uint32_t)pack_e4m3x2(e[4], e[5]) | ((uint32_t)pack_e4m3x2(e[6], e[7]) << 16);
+    v.z = (uint32_t)pack_e4m3x2(e[8], e[9]) | ((uint32_t)pack_e4m3x2(e[10], e[11]) << 16);
+    v.w = (uint32_t)pack_e4m3x2(e[12], e[13]) | ((uint32_t)pack_e4m3x2(e[14], e[15]) << 16);
+    *reinterpret_cast<uint4*>(prow + ((c16 ^ (row & 7)) << 4)) = v;
+  }
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) f2_unpack(accp[k], acc[2 * k], acc[2 * k + 1]);
+  return ((acc[0] + acc[2]) + (acc[4] + acc[6])) + ((acc[1] + acc[3]) + (acc[5] + acc[7]));
+}
+
+// Warpgroup-wide change of the per-thread register budget (PTX setmaxnreg);
+// each call sits at the top of its warpgroup's role branch.
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // K/V ring order.  K runs one tile ahead of V: K0, K1, V0, K2, V1, ...,
 // K_{n-1}, V_{n-2}, V_{n-1}, matching the MMA order S(j) then PV(j-1), so
 // slots are consumed and released first in, first out.
@@ -186,6 +269,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   using C = Cfg<FP8>;
   constexpr int TILE = C::TILE, OFF_Q = C::OFF_Q, OFF_KV = C::OFF_KV, OFF_P = C::OFF_P, OFF_BAR = C::OFF_BAR;
+  constexpr int NSLOT = C::NSLOT, PBUF = C::PBUF, NBAR = C::NBAR;
 
   // Work item: query head h, pair of 128-row query tiles (longest first), sequence b.
   const int h = p.h_lo + blockIdx.x;
@@ -214,13 +298,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   Smem sm;
   uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
   sm.q_full = bars;
-  sm.kv_full = bars + 2;
-  sm.kv_empty = bars + 5;
-  sm.s_full = bars + 8;
-  sm.s_free = bars + 10;
-  sm.p_full = bars + 12;
-  sm.o_done = bars + 14;
-  sm.q_rot = bars + 16;
+  sm.k_full = sm.q_full + 2;
+  sm.v_full = sm.k_full + NSLOT;
+  sm.kv_empty = sm.v_full + NSLOT;
+  sm.s_full = sm.kv_empty + NSLOT;
+  sm.s_free = sm.s_full + 2;
+  sm.p_full = sm.s_free + 2;
+  sm.o_done = sm.p_full + 2 * PBUF;
+  sm.q_rot = sm.o_done + 2 * PBUF;
   sm.tmem_slot = (uint32_t*)(bars + NBAR);
   sm.nkv = (int*)(sm.tmem_slot + 4);
   sm.nfull = sm.nkv + 2;
@@ -257,17 +342,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
   if (warp == WARP_MMA_S) tmem_alloc(sm.tmem_slot, TMEM_COLS);
-  // K or V tile j into ring slot `slot` (TMA, completion on kv_full[slot]).
+  // K or V tile j into ring slot `slot` (TMA, completion on k_full[slot] or v_full[slot]).
   const int32_t* table = PAGED ? p.page_table + (int64_t)b * p.max_pages : nullptr;
   auto load_kv = [&](int slot, bool is_v, int j) {
     const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
     uint8_t* dst = smem + OFF_KV + slot * TILE;
-    mbar_arrive_expect_tx(&sm.kv_full[slot], TILE);
+    uint64_t* full = is_v ? &sm.v_full[slot] : &sm.k_full[slot];
+    mbar_arrive_expect_tx(full, TILE);
     if (FP8 && is_v) {  // V^T codes [hkv][128][keys]: one box of 128 keys x 128 dims
-      tma_load_3d(dst, tm, &sm.kv_full[slot], k_beg + j * BN, 0, g);
+      tma_load_3d(dst, tm, full, k_beg + j * BN, 0, g);
     } else if (!PAGED) {
       for (int hf = 0; hf < C::NBOX; ++hf)
-        tma_load_3d(dst + hf * HALF, tm, &sm.kv_full[slot], hf * 64, g, k_beg + j * BN);
+        tma_load_3d(dst + hf * HALF, tm, full, hf * 64, g, k_beg + j * BN);
     } else {
       for (int pp = 0; pp < 2; ++pp) {  // two 64-token pages per tile
         const int lp = j * 2 + pp;
@@ -278,7 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const int row0 = (int)(((int64_t)g * p.num_pages + pid) * 64);
         for (int hf = 0; hf < 2; ++hf)
-          tma_load_2d(dst + hf * HALF + pp * (HALF / 2), tm, &sm.kv_full[slot], hf * 64, row0);
+          tma_load_2d(dst + hf * HALF + pp * (HALF / 2), tm, full, hf * 64, row0);
       }
     }
   };
@@ -293,12 +379,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&sm.q_full[t], 1);
       mbar_init(&sm.s_full[t], 1);
       mbar_init(&sm.s_free[t], 128);
-      mbar_init(&sm.p_full[t], 128);
-      mbar_init(&sm.o_done[t], 1);
+      for (int b = 0; b < PBUF; ++b) {
+        mbar_init(&sm.p_full[t * PBUF + b], 128);
+        mbar_init(&sm.o_done[t * PBUF + b], 1);
+      }
       mbar_init(&sm.q_rot[t], 128);
     }
     for (int i = 0; i < NSLOT; ++i) {
-      mbar_init(&sm.kv_full[i], 1);
+      mbar_init(&sm.k_full[i], 1);
+      mbar_init(&sm.v_full[i], 1);
       mbar_init(&sm.kv_empty[i], 1);
     }
     fence_mbar_init();
@@ -336,10 +425,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int nkv = max(nkv_a, nkv_b);
 
   if (warp >= 8) {
+   if constexpr (FP8) regs_dec<REGS_SIDE>();
    if (warp == WARP_TMA) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = k0_early ? 1 : 0;
+      // Per slot (bit s): the parity of the K and of the V fills issued so far,
+      // whether the last fill was a V tile, and whether the slot was used --
+      // what the final drain needs to wait for each slot's last load.
+      uint32_t kpar = 0, vpar = 0, lastv = 0, used = 0;
+      auto note = [&](int i, bool is_v) {
+        const uint32_t bit = 1u << (i % NSLOT);
+        if (is_v) {
+          vpar ^= bit;
+          lastv |= bit;
+        } else {
+          kpar ^= bit;
+          lastv &= ~bit;
+        }
+        used |= bit;
+      };
+      int issued = 0;
+      if (k0_early) {
+        note(0, false);
+        issued = 1;
+      }
       for (int i = issued; i < 2 * nkv; ++i) {
         // load i of the ring order (see ring_pos_k / ring_pos_v)
         bool is_v;
@@ -354,12 +463,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int slot = i % NSLOT;
         if (i >= NSLOT && !mbar_wait(&sm.kv_empty[slot], ((i / NSLOT) - 1) & 1, p.err, DEV_TIMEOUT_TMA)) break;
         load_kv(slot, is_v, j);
+        note(i, is_v);
         issued = i + 1;
       }
-      // Leave no copy in flight: wait (bounded) for the last slots issued and
-      // for the Q tiles (loaded even when a tile turns out to need no keys).
-      for (int i = max(0, issued - NSLOT); i < issued; ++i)
-        mbar_wait(&sm.kv_full[i % NSLOT], (i / NSLOT) & 1, nullptr, 0);
+      // Leave no copy in flight: wait (bounded) for the last load of each slot
+      // (the phase of its kind's barrier that it completes has the parity of
+      // that kind's fill count minus one) and for the Q tiles (loaded even
+      // when a tile turns out to need no keys).
+#pragma unroll
+      for (int sl = 0; sl < NSLOT; ++sl) {
+        if (!((used >> sl) & 1u)) continue;
+        const bool v = (lastv >> sl) & 1u;
+        mbar_wait(v ? &sm.v_full[sl] : &sm.k_full[sl], (((v ? vpar : kpar) >> sl) & 1u) ^ 1u, nullptr, 0);
+      }
       for (int t = 0; t < 2; ++t)
         if (q0 + t * BM < Sq) mbar_wait(&sm.q_full[t], 0, nullptr, 0);
     }
@@ -392,9 +508,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         const uint64_t dQ = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
         const uint64_t dK = sdesc_sw128(smem_u32(smem + OFF_KV), 16, 1024);
+        uint32_t kph = 0;  // bit s: parity of the next K fill of slot s
         for (int j = 0; j < nkv && ok; ++j) {
           const int iK = ring_pos_k(j), slotK = iK % NSLOT;
-          if (!(ok = wait(&sm.kv_full[slotK], (iK / NSLOT) & 1))) break;
+          if (!(ok = wait(&sm.k_full[slotK], (kph >> slotK) & 1u))) break;
+          kph ^= 1u << slotK;
           tc_fence_after();
           // S_t(j) overwrites S_t(j-1) in TMEM only after the softmax has
           // signalled (s_free) that S_t(j-1) is in its registers.
@@ -414,16 +532,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint64_t dP = sdesc_sw128(smem_u32(smem + OFF_P), 16, 1024);
         const uint64_t dV = sdesc_sw128(smem_u32(smem + OFF_KV), FP8 ? 16 : HALF, 1024);
         bool ok = true;
+        uint32_t vph = 0;  // bit s: parity of the next V fill of slot s
         for (int j = 0; j < nkv && ok; ++j) {
           const int iV = ring_pos_v(j, nkv), slotV = iV % NSLOT;
-          if (!(ok = wait(&sm.kv_full[slotV], (iV / NSLOT) & 1))) break;
+          if (!(ok = wait(&sm.v_full[slotV], (vph >> slotV) & 1u))) break;
+          vph ^= 1u << slotV;
           tc_fence_after();
           for (int t = 0; t < 2; ++t) {
             if (j >= (t ? nkv_b : nkv_a)) continue;
-            if (!(ok = wait(&sm.p_full[t], j & 1))) break;
+            if (!(ok = wait(&sm.p_full[t * PBUF + j % PBUF], (j / PBUF) & 1))) break;
             tc_fence_after();
-            mma_values<FP8>(tmem + 2 * BN + t * D, dP + t * kTile16, dV + slotV * kTile16, j > 0);
-            tc_commit_warp(&sm.o_done[t]);
+            mma_values<FP8>(tmem + 2 * BN + t * D, dP + (t * PBUF + j % PBUF) * kTile16, dV + slotV * kTile16,
+                            j > 0);
+            tc_commit_warp(&sm.o_done[t * PBUF + j % PBUF]);
           }
           if (!ok) break;
           tc_commit_warp(&sm.kv_empty[slotV]);  // V_j consumed
@@ -433,6 +554,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
    }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
+    if constexpr (FP8) regs_inc<REGS_SOFTMAX>();
     const int t = warp >> 2, wq = warp & 3;
     const int row = wq * 32 + lane;
     const int rq = q0 + t * BM + row;  // row index inside the sequence
@@ -452,7 +574,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * BN;
     const uint32_t tO = tmem + lane_base + 2 * BN + t * D;
-    uint8_t* prow = smem + OFF_P + t * TILE + (row >> 3) * 1024 + (row & 7) * 128;
+    uint8_t* const prow0 = smem + OFF_P + t * PBUF * TILE + (row >> 3) * 1024 + (row & 7) * 128;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
 
@@ -498,6 +620,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, p.err, DEV_TIMEOUT_SOFTMAX));
       if (!ok) break;
       tc_fence_after();
+      uint8_t* const prow = prow0 + (j % PBUF) * TILE;
       // Scores: one row of S_t (128 fp32) per thread, in one TMEM load.
       float s[128];
       float mx[8];
@@ -511,7 +634,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(&sm.s_free[t]);  // S_t may now be overwritten by S_t(j+1)
-      if (j < nfull_t) {  // no mask on this tile: reduce the first half right away
+      if (!FP8 && j < nfull_t) {  // no mask on this tile: reduce the first half right away
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[i], s[8 + i], s[16 + i]);
 #pragma unroll
@@ -550,47 +673,67 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (c > lim) s[c] = -INFINITY;
         }
       }
-      // row max over eight independent chains of 3-input maxima
-      if (j >= nfull_t) {  // masked tile: the first half was not reduced yet
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[i], s[8 + i], s[16 + i]);
-#pragma unroll
-        for (int c = 24; c < 64; c += 16)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
-      }
-#pragma unroll
-      for (int c = 64; c < 128; c += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
-      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      const float m_new = fmaxf(m_ref, mt);
-      const bool grow = (m_new - m_ref) * sl2 > kRescaleLog2;  // false when both are -inf
-      const bool any_grow = __any_sync(0xffffffffu, grow);
-      float alpha = 1.f;
-      if (any_grow && m_new > m_ref) {
-        alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2((m_ref - m_new) * sl2);
-        l *= alpha;
-        m_ref = m_new;
-      }
-      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
 
-      // P_t (and O_t) are free once O_t += P_t V_{j-1} finished; in the issue
-      // order above that MMA precedes S_t(j), so this wait is already satisfied.
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], (j - 1) & 1, p.err, DEV_TIMEOUT_SOFTMAX));
+      float alpha = 1.f;
+      bool any_grow = false;
+      // The e4m3 kernel checks its reference lazily: once every row of the
+      // warp has one (its first tile with a visible key), the weights are
+      // computed against the reference as it stands, with no row-max pass; the
+      // tile's weight sum bounds every weight, and only a sum above
+      // kLazySumFp8 sends the warp back for the row max, a new reference, an O
+      // rescale and a second pass.  Until then -- and always in the bf16
+      // kernel -- the row max comes first and moves the reference when it
+      // grows by more than 2^8 in exp2 units.  Either way every weight stays
+      // <= 2^8, and the final O / l is exact for whatever reference was used.
+      const bool need_ref = !FP8 || __any_sync(0xffffffffu, m_ref == -INFINITY);
+      if (need_ref) {
+        float mt;
+        if constexpr (FP8) {
+          mt = row_max128(s);
+        } else {
+          if (j >= nfull_t) {  // masked tile: the first half was not reduced yet
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+#pragma unroll
+            for (int c = 24; c < 64; c += 16)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+          }
+#pragma unroll
+          for (int c = 64; c < 128; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+          mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        }
+        const float m_new = fmaxf(m_ref, mt);
+        const bool grow = (m_new - m_ref) * sl2 > kRescaleLog2;  // false when both are -inf
+        any_grow = __any_sync(0xffffffffu, grow);
+        if (any_grow && m_new > m_ref) {
+          alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2((m_ref - m_new) * sl2);
+          l *= alpha;
+          m_ref = m_new;
+        }
+      }
+
+      // P_t's buffer j % PBUF is free once O_t += P_t V finished for tile
+      // j - PBUF (its barrier o_done[t][j % PBUF] completes once per use).
+      if (j >= PBUF) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t * PBUF + j % PBUF], (j / PBUF - 1) & 1, p.err,
+                                               DEV_TIMEOUT_SOFTMAX));
         if (!ok) break;
         tc_fence_after();
       }
-      // P = exp2(S * scale*log2e - m*scale*log2e), bf16, into the swizzled K-major
-      // tile.  The affine step runs on fp32 pairs; the row sum on eight scalar
-      // accumulators (key i goes to accumulator i mod 8), which measured faster
-      // than paired adds and gives the same sums.
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nmbx2 = f2_pack(-mb, -mb);
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      float tsum;
       if constexpr (!FP8) {
+        // P = exp2(S * scale*log2e - m*scale*log2e), bf16, into the swizzled
+        // K-major tile.  The affine step runs on fp32 pairs; the row sum on
+        // eight scalar accumulators (key i goes to accumulator i mod 8), which
+        // measured faster than paired adds and gives the same sums.
+        const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nmbx2 = f2_pack(-mb, -mb);
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
         for (int c8 = 0; c8 < 16; ++c8) {
           float e[8];
@@ -610,39 +753,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           v.w = pack_bf16x2(e[6], e[7]);
           *reinterpret_cast<uint4*>(prow + (c8 >> 3) * HALF + (((c8 & 7) ^ (row & 7)) << 4)) = v;
         }
+        tsum = ((acc[0] + acc[2]) + (acc[4] + acc[6])) + ((acc[1] + acc[3]) + (acc[5] + acc[7]));
       } else {
-        // e4m3 P: 16 keys per 16-byte chunk of the single box (P <= 256 < 448).
-        // Here the row sum on fp32 pairs measured faster than scalar adds; pair
-        // k holds accumulators 2k and 2k+1, so the sums are the same.
-        uint64_t accp[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) accp[k] = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {
-          float e[16];
-#pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(s[c16 * 16 + i], s[c16 * 16 + i + 1]), sl2x2, nmbx2), x0, x1);
-            e[i] = fast_exp2(x0);
-            e[i + 1] = fast_exp2(x1);
-            accp[(i >> 1) & 3] = f2_add(accp[(i >> 1) & 3], f2_pack(e[i], e[i + 1]));
+        for (int pass = 0;; ++pass) {
+          tsum = weights_e4m3(s, sl2, (m_ref == -INFINITY) ? 0.f : m_ref * sl2, prow, row);
+          if (need_ref || pass > 0) break;
+          const bool over = !(tsum <= kLazySumFp8);  // also true for inf and NaN
+          if (!__any_sync(0xffffffffu, over)) break;
+          const float m_new = fmaxf(m_ref, row_max128(s));
+          const bool grew = m_new > m_ref;
+          if (grew) {
+            alpha = fast_exp2((m_ref - m_new) * sl2);
+            l *= alpha;
+            m_ref = m_new;
           }
-          uint4 v;
-          v.x = (uint32_t)pack_e4m3x2(e[0], e[1]) | ((uint32_t)pack_e4m3x2(e[2], e[3]) << 16);
-          v.y = (uint32_t)pack_e4m3x2(e[4], e[5]) | ((uint32_t)pack_e4m3x2(e[6], e[7]) << 16);
-          v.z = (uint32_t)pack_e4m3x2(e[8], e[9]) | ((uint32_t)pack_e4m3x2(e[10], e[11]) << 16);
-          v.w = (uint32_t)pack_e4m3x2(e[12], e[13]) | ((uint32_t)pack_e4m3x2(e[14], e[15]) << 16);
-          *reinterpret_cast<uint4*>(prow + ((c16 ^ (row & 7)) << 4)) = v;
+          any_grow = __any_sync(0xffffffffu, grew);
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) f2_unpack(accp[k], acc[2 * k], acc[2 * k + 1]);
       }
-      l += ((acc[0] + acc[2]) + (acc[4] + acc[6])) + ((acc[1] + acc[3]) + (acc[5] + acc[7]));
+      l += tsum;
       if (any_grow && j > 0) {
-        // O_t *= alpha in TMEM.  tcgen05.st reads its source registers
-        // asynchronously, so all four chunks keep their own registers until
-        // the single wait::st.
+        // O_t *= alpha in TMEM, once the last O_t += P_t V finished (with one
+        // P buffer the wait above already covered it).  tcgen05.st reads its
+        // source registers asynchronously, so all four chunks keep their own
+        // registers until the single wait::st.
+        if (PBUF > 1) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t * PBUF + (j - 1) % PBUF], ((j - 1) / PBUF) & 1, p.err,
+                                                 DEV_TIMEOUT_SOFTMAX));
+          if (!ok) break;
+          tc_fence_after();
+        }
         uint32_t o[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tO + c * 32, o[c]);
@@ -660,27 +799,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&sm.p_full[t]);
+      mbar_arrive(&sm.p_full[t * PBUF + j % PBUF]);
     }
 
     // epilogue: O / l to global memory, LSE = scale * m + ln l
     if (ok && nkv_t > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], (nkv_t - 1) & 1, p.err, DEV_TIMEOUT_SOFTMAX));
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t * PBUF + (nkv_t - 1) % PBUF], ((nkv_t - 1) / PBUF) & 1,
+                                             p.err, DEV_TIMEOUT_SOFTMAX));
       tc_fence_after();
     }
     const bool have_o = ok && nkv_t > 0;
     const float inv = l > 0.f ? (FP8 ? __ldg(p.v_scale + g) : 1.f) / l : 0.f;
     const int64_t orow = ((int64_t)(q_beg + rq) * p.hq + h) * D;
-    // bf16 output of the bf16 kernel goes through shared memory the tile no
-    // longer reads -- the two 16 KB boxes of Q_t, dims 0-63 and 64-127 of each
-    // row as 128-byte rows with the 16-byte chunks XOR-swizzled by row -- and
-    // then out two whole 256-byte rows per warp store instruction.  Stored
-    // straight from each thread's row, a warp instruction touches 32 rows; that
-    // cost 4% of the kernel.  (In the e4m3 kernel the staging measured slower.)
+    // The bf16 kernel's output goes through shared memory the tile no longer
+    // reads, then out whole rows per warp store instruction; stored straight
+    // from each thread's row, a warp instruction would touch 32 rows (that
+    // cost 4% of the kernel with bf16 output).
+    //  - bf16 output: the two 16 KB boxes of Q_t hold dims 0-63 and 64-127 of
+    //    each row as 128-byte rows, 16-byte chunks XOR-swizzled by row; a warp
+    //    instruction stores two 256-byte rows.
+    //  - fp32 output (partials for a merge): Q_t (32 KB) holds dims 0-63 and
+    //    P_t (32 KB, free once the last P V finished) dims 64-127, as 256-byte
+    //    rows swizzled by row; a warp instruction stores one 512-byte row.
+    // (In the e4m3 kernel the tiles are half the size, and staging bf16 output
+    // measured slower.)
     constexpr bool kStage = !FP8;
-    const bool stage = kStage && !p.out_f32;
+    const bool stage = kStage;
     uint8_t* const stg0 = smem + OFF_Q + t * TILE;
-    uint8_t* const stg1 = stg0 + HALF;
+    uint8_t* const stg1 = p.out_f32 ? smem + OFF_P + t * PBUF * TILE : stg0 + HALF;
     // a tile that saw no key had no score MMA wait for its Q: let that copy land first
     if (stage && nkv_t == 0 && q0 + t * BM < Sq)
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[t], 0, p.err, DEV_TIMEOUT_SOFTMAX)) && ok;
@@ -696,12 +842,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = 0; i < 32; ++i) o[i] = 0u;
       }
       if (p.out_f32) {
-        if (rv) {
-          float4* dst = reinterpret_cast<float4*>((float*)p.out + orow + c * 32);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                 __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        for (int i = 0; i < 8; ++i) {
+          const float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                       __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+          const int k = c * 8 + i;  // 16-byte chunk of the 512-byte row, 0..31
+          if (stage)
+            *reinterpret_cast<float4*>((k < 16 ? stg0 : stg1) + row * 256 + (((k & 15) ^ (row & 15)) << 4)) = v;
+          else if (rv)
+            reinterpret_cast<float4*>((float*)p.out + orow)[k] = v;
         }
       } else if (stage || rv) {
 #pragma unroll
@@ -720,16 +869,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     if (stage) {
-      // the warp's 32 staged rows go out two 256-byte rows per store instruction
       __syncwarp();
-      const int chunk = lane & 15;
+      if (p.out_f32) {
+        // the warp's 32 staged rows go out one 512-byte row per store instruction
 #pragma unroll 4
-      for (int it = 0; it < 16; ++it) {
-        const int r = wq * 32 + 2 * it + (lane >> 4);
-        const uint4 v =
-            *reinterpret_cast<const uint4*>((chunk < 8 ? stg0 : stg1) + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
-        const int rq_r = q0 + t * BM + r;
-        if (rq_r < Sq) reinterpret_cast<uint4*>((__nv_bfloat16*)p.out + ((int64_t)(q_beg + rq_r) * p.hq + h) * D)[chunk] = v;
+        for (int r = wq * 32; r < wq * 32 + 32; ++r) {
+          const float4 v = *reinterpret_cast<const float4*>((lane < 16 ? stg0 : stg1) + r * 256 +
+                                                            (((lane & 15) ^ (r & 15)) << 4));
+          const int rq_r = q0 + t * BM + r;
+          if (rq_r < Sq) reinterpret_cast<float4*>((float*)p.out + ((int64_t)(q_beg + rq_r) * p.hq + h) * D)[lane] = v;
+        }
+      } else {
+        // the warp's 32 staged rows go out two 256-byte rows per store instruction
+        const int chunk = lane & 15;
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {
+          const int r = wq * 32 + 2 * it + (lane >> 4);
+          const uint4 v =
+              *reinterpret_cast<const uint4*>((chunk < 8 ? stg0 : stg1) + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
+          const int rq_r = q0 + t * BM + r;
+          if (rq_r < Sq)
+            reinterpret_cast<uint4*>((__nv_bfloat16*)p.out + ((int64_t)(q_beg + rq_r) * p.hq + h) * D)[chunk] = v;
+        }
       }
     }
     if (rv && p.lse) p.lse[(int64_t)(q_beg + rq) * p.hq + h] = l > 0.f ? m_ref * c_row + logf(l) : -INFINITY;
@@ -764,7 +925,9 @@ cudaError_t launch_variant(const tc::Params& p, dim3 grid, const CUtensorMap& tq
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, tc::prefill_tc_kernel<PAGED, FP8>);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs > tc::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
+    // the e4m3 kernel's register split hands out exactly the launch total, so
+    // it must be launched with 168 registers per thread
+    if (FP8 ? fa.numRegs != tc::REGS_LAUNCH : fa.numRegs > tc::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
     ready[dev] = 1;
   }
   tc::prefill_tc_kernel<PAGED, FP8><<<grid, tc::NTHREADS, tc::Cfg<FP8>::SMEM_BYTES, s>>>(tq, tk, tv, p);

@@ -150,18 +150,54 @@ __global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t to
 
 // New tokens' K and V into the head-major paged cache (SGLang page, sections
 // 2.1-2.2), K rotated as rope_kernel rotates it.  Each block takes NT tokens:
-// angle tables first, then one 16-byte vector of the first half of a key head
-// with its partner vector of the second half per thread (rotated, written to
-// the cache row and optionally to k_rot_out), then the value rows copied as
-// 16-byte vectors.  Slots are checked per token: -1 skips, out of range is
+// angle tables first, then per thread one 16-byte vector of the first half of
+// a head's key and value rows with its partner vector of the second half (the
+// key pair rotated), written to the cache rows and optionally the rotated keys
+// to k_rot_out.  Slots are checked per token: -1 skips, out of range is
 // recorded and skipped.
 template <int NT>
-__global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const InvFreq f) {
+__global__ void __launch_bounds__(256, 4) kv_append_kernel(AppendLaunch a, const InvFreq f) {
   constexpr int V = 8;  // bf16 per 16-byte vector
   __shared__ float cs_s[NT][128], sn_s[NT][128];
   __shared__ int64_t slot_s[NT];
   const int d = a.head_dim, half = d / 2;
   const int64_t t0 = (int64_t)blockIdx.x * NT;
+  const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
+  const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
+  __nv_bfloat16* kc = (__nv_bfloat16*)a.k_cache;
+  __nv_bfloat16* vc = (__nv_bfloat16*)a.v_cache;
+  __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
+  // One item is one (token, head, chunk pair): chunk c of the first half of the
+  // key and value rows with its partner chunk of the second half.  Items go in
+  // batches of kB whose loads (four 16-byte vectors each) are all issued before
+  // the first store: the compiler may not move loads above stores to memory it
+  // cannot tell apart.  The first batch is requested before the slots and the
+  // angle tables, which its loads do not need.
+  const int chunks = half / V;
+  const int items = NT * a.heads * chunks;
+  constexpr int kB = 2;
+  GridWalk gw(threadIdx.x, blockDim.x, chunks, a.heads);
+  uint4 k1[kB], k2[kB], v1[kB], v2[kB];
+  int64_t src[kB];
+  int tts[kB], cc[kB], hh[kB];
+  auto load_batch = [&](int w0) {
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      tts[u] = gw.tt;
+      cc[u] = gw.c;
+      hh[u] = gw.h;
+      src[u] = -1;
+      if (w0 + u * (int)blockDim.x < items && t0 + gw.tt < a.tokens) {
+        src[u] = ((t0 + gw.tt) * a.heads + gw.h) * d + gw.c * V;
+        k1[u] = __ldg(reinterpret_cast<const uint4*>(kn + src[u]));
+        k2[u] = __ldg(reinterpret_cast<const uint4*>(kn + src[u] + half));
+        v1[u] = __ldg(reinterpret_cast<const uint4*>(vn + src[u]));
+        v2[u] = __ldg(reinterpret_cast<const uint4*>(vn + src[u] + half));
+      }
+      gw.next();
+    }
+  };
+  load_batch(threadIdx.x);
   if (threadIdx.x < NT) {
     const int64_t t = t0 + threadIdx.x;
     int64_t sl = -1;
@@ -177,86 +213,40 @@ __global__ void __launch_bounds__(256) kv_append_kernel(AppendLaunch a, const In
   const bool rotate = a.base > 0.0;
   if (rotate) angle_tables<NT, 128>(cs_s, sn_s, t0, a.tokens, half, a.positions, f);
   __syncthreads();
-  const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
-  const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
-  __nv_bfloat16* kc = (__nv_bfloat16*)a.k_cache;
-  __nv_bfloat16* vc = (__nv_bfloat16*)a.v_cache;
-  __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
-  const int chunks = half / V;
-  const int kitems = NT * a.heads * chunks;
-  // Items go in batches whose loads are all issued before the first store: the
-  // compiler may not move loads above stores to memory it cannot tell apart.
-  constexpr int kKB = 2, kVB = 4;
-  GridWalk gk(threadIdx.x, blockDim.x, chunks, a.heads);
-  for (int w0 = threadIdx.x; w0 < kitems; w0 += kKB * blockDim.x) {
-    uint4 u1[kKB], u2[kKB];
-    int64_t src[kKB], dst[kKB];
-    int tts[kKB], cc[kKB];
+  for (int w0 = threadIdx.x; w0 < items; w0 += kB * blockDim.x) {
+    if (w0 != (int)threadIdx.x) load_batch(w0);
 #pragma unroll
-    for (int k = 0; k < kKB; ++k) {
-      dst[k] = -1;
-      tts[k] = gk.tt;
-      cc[k] = gk.c;
-      if (w0 + k * (int)blockDim.x < kitems) {
-        const int64_t sl = slot_s[gk.tt];
-        if (sl >= 0) {
-          src[k] = ((t0 + gk.tt) * a.heads + gk.h) * d + gk.c * V;
-          dst[k] = ((int64_t)gk.h * a.cache_rows + sl) * d + gk.c * V;
-          u1[k] = __ldg(reinterpret_cast<const uint4*>(kn + src[k]));
-          u2[k] = __ldg(reinterpret_cast<const uint4*>(kn + src[k] + half));
-        }
-      }
-      gk.next();
-    }
-#pragma unroll
-    for (int k = 0; k < kKB; ++k) {
-      if (dst[k] < 0) continue;
+    for (int u = 0; u < kB; ++u) {
+      if (src[u] < 0) continue;
+      const int64_t sl = slot_s[tts[u]];
+      if (sl < 0) continue;
+      const int64_t dst = ((int64_t)hh[u] * a.cache_rows + sl) * d + cc[u] * V;
       if (rotate) {
-        const __nv_bfloat16* a1 = reinterpret_cast<const __nv_bfloat16*>(&u1[k]);
-        const __nv_bfloat16* a2 = reinterpret_cast<const __nv_bfloat16*>(&u2[k]);
+        const __nv_bfloat16* a1 = reinterpret_cast<const __nv_bfloat16*>(&k1[u]);
+        const __nv_bfloat16* a2 = reinterpret_cast<const __nv_bfloat16*>(&k2[u]);
         uint4 w1, w2;
         __nv_bfloat16* b1 = reinterpret_cast<__nv_bfloat16*>(&w1);
         __nv_bfloat16* b2 = reinterpret_cast<__nv_bfloat16*>(&w2);
 #pragma unroll
         for (int e = 0; e < V; ++e) {
-          const float cs = cs_s[tts[k]][cc[k] * V + e], sn = sn_s[tts[k]][cc[k] * V + e];
+          const float cs = cs_s[tts[u]][cc[u] * V + e], sn = sn_s[tts[u]][cc[u] * V + e];
           float y1, y2;
           rope_rotate(to_f(a1[e]), to_f(a2[e]), cs, sn, y1, y2);
           from_f(y1, b1[e]);
           from_f(y2, b2[e]);
         }
-        u1[k] = w1;
-        u2[k] = w2;
+        k1[u] = w1;
+        k2[u] = w2;
       }
-      *reinterpret_cast<uint4*>(kc + dst[k]) = u1[k];
-      *reinterpret_cast<uint4*>(kc + dst[k] + half) = u2[k];
+      *reinterpret_cast<uint4*>(kc + dst) = k1[u];
+      *reinterpret_cast<uint4*>(kc + dst + half) = k2[u];
+      *reinterpret_cast<uint4*>(vc + dst) = v1[u];
+      *reinterpret_cast<uint4*>(vc + dst + half) = v2[u];
       if (ko) {
-        *reinterpret_cast<uint4*>(ko + src[k]) = u1[k];
-        *reinterpret_cast<uint4*>(ko + src[k] + half) = u2[k];
+        *reinterpret_cast<uint4*>(ko + src[u]) = k1[u];
+        *reinterpret_cast<uint4*>(ko + src[u] + half) = k2[u];
       }
     }
-  }
-  const int vchunks = d / V;
-  const int vitems = NT * a.heads * vchunks;
-  GridWalk gv(threadIdx.x, blockDim.x, vchunks, a.heads);
-  for (int w0 = threadIdx.x; w0 < vitems; w0 += kVB * blockDim.x) {
-    uint4 u[kVB];
-    int64_t dst[kVB];
-#pragma unroll
-    for (int k = 0; k < kVB; ++k) {
-      dst[k] = -1;
-      if (w0 + k * (int)blockDim.x < vitems) {
-        const int64_t sl = slot_s[gv.tt];
-        if (sl >= 0) {
-          u[k] = __ldg(reinterpret_cast<const uint4*>(vn + ((t0 + gv.tt) * a.heads + gv.h) * d + gv.c * V));
-          dst[k] = ((int64_t)gv.h * a.cache_rows + sl) * d + gv.c * V;
-        }
-      }
-      gv.next();
-    }
-#pragma unroll
-    for (int k = 0; k < kVB; ++k)
-      if (dst[k] >= 0) *reinterpret_cast<uint4*>(vc + dst[k]) = u[k];
   }
 }
 
@@ -297,6 +287,37 @@ __device__ __forceinline__ void load_chunk(const __nv_bfloat16* __restrict__ row
   }
 }
 
+// The raw 16-byte vectors of a chunk pair (chunk c of the first half of a
+// 128-value row and its partner chunk of the second half), before widening.
+struct RawPair {
+  uint4 lo, hi;
+};
+
+// Loads the key and value chunk pairs of the walker's current item (token
+// t0 + gw.tt, head gw.h, pair gw.c); tokens past the end read as zeros.
+__device__ __forceinline__ void load_raw(const __nv_bfloat16* __restrict__ kn, const __nv_bfloat16* __restrict__ vn,
+                                         int64_t t0, const GridWalk& gw, int heads, int64_t tokens, RawPair& k,
+                                         RawPair& v) {
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  k.lo = k.hi = v.lo = v.hi = z;
+  if (t0 + gw.tt < tokens) {
+    const int64_t src = ((t0 + gw.tt) * heads + gw.h) * 128 + 8 * gw.c;
+    k.lo = __ldg(reinterpret_cast<const uint4*>(kn + src));
+    k.hi = __ldg(reinterpret_cast<const uint4*>(kn + src + 64));
+    v.lo = __ldg(reinterpret_cast<const uint4*>(vn + src));
+    v.hi = __ldg(reinterpret_cast<const uint4*>(vn + src + 64));
+  }
+}
+
+__device__ __forceinline__ void unpack_chunk(const RawPair& p, RowChunk& r) {
+  const uint32_t w1[4] = {p.lo.x, p.lo.y, p.lo.z, p.lo.w}, w2[4] = {p.hi.x, p.hi.y, p.hi.z, p.hi.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    r.a[e] = __uint_as_float((e & 1) ? (w1[e >> 1] & 0xffff0000u) : (w1[e >> 1] << 16));
+    r.b[e] = __uint_as_float((e & 1) ? (w2[e >> 1] & 0xffff0000u) : (w2[e >> 1] << 16));
+  }
+}
+
 // Rotates the chunk pair exactly as rope_kernel rotates it and rounds to bf16,
 // the value rope_apply stores.  cs, sn: the token's 64 cos / sin values.
 __device__ __forceinline__ void rotate_chunk(RowChunk& r, const float* cs_row, const float* sn_row, int c) {
@@ -306,11 +327,14 @@ __device__ __forceinline__ void rotate_chunk(RowChunk& r, const float* cs_row, c
   const float cs[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
   const float sn[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float y1, y2;
-    rope_rotate(r.a[e], r.b[e], cs[e], sn[e], y1, y2);
-    r.a[e] = __bfloat162float(__float2bfloat16_rn(y1));
-    r.b[e] = __bfloat162float(__float2bfloat16_rn(y2));
+  for (int e = 0; e < 8; e += 2) {
+    float y1[2], y2[2];
+    rope_rotate(r.a[e], r.b[e], cs[e], sn[e], y1[0], y2[0]);
+    rope_rotate(r.a[e + 1], r.b[e + 1], cs[e + 1], sn[e + 1], y1[1], y2[1]);
+    // round each pair to bf16 with one packed conversion, then widen back
+    const uint32_t pa = pack_bf16x2(y1[0], y1[1]), pb = pack_bf16x2(y2[0], y2[1]);
+    r.a[e] = __uint_as_float(pa << 16), r.a[e + 1] = __uint_as_float(pa & 0xffff0000u);
+    r.b[e] = __uint_as_float(pb << 16), r.b[e + 1] = __uint_as_float(pb & 0xffff0000u);
   }
 }
 
@@ -327,20 +351,31 @@ __device__ __forceinline__ float chunk_amax(const RowChunk& r) {
 // Symmetric int8 codes of the chunk pair: code = x / sc rounded to the nearest
 // integer (ties to even) and clamped to [-127, 127], the quotient correctly
 // rounded in fp32 (div_rn_recip for normal scales); 0 for a zero scale.  The
-// quotient is clamped first (the same codes: anything beyond +-127 rounds to
-// +-127 or past it) and rounded by adding 1.5 * 2^23, where an fp32 add rounds
-// to an integer, ties to even, whose two's complement sits in the low bits --
-// on the FMA and integer pipes rather than the conversion unit.
+// quotient is rounded by adding 1.5 * 2^23: an fp32 add then rounds it to an
+// integer, ties to even, whose two's complement is the low byte of the sum's
+// bits, and three byte permutes pack four such bytes -- no conversion
+// instruction and no shifts or masks per code.
+//
+// With sc = RN(amax / 127) >= (amax / 127)(1 - 2^-24) and |x| <= amax, the
+// correctly rounded quotient is at most 127 (1 + 2^-24) rounded, 127 + 2^-17 <
+// 127.5, so its nearest integer never leaves [-127, 127] and the fast path
+// needs no clamp.  The full division (scales below 2^-90, where sc may be
+// subnormal and carry a large relative error) clamps.
+__device__ __forceinline__ uint32_t code_bits(float q) { return (uint32_t)__float_as_int(__fadd_rn(q, 12582912.0f)); }
+
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
 template <bool FAST>
 __device__ __forceinline__ uint32_t int8x4(const float* x, float sc, float rc) {
-  uint32_t p = 0;
+  uint32_t b[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float q = fminf(fmaxf(FAST ? div_rn_recip(x[e], sc, rc) : x[e] / sc, -127.0f), 127.0f);
-    const uint32_t code = (uint32_t)__float_as_int(__fadd_rn(q, 12582912.0f)) - 0x4B400000u;
-    p |= (code & 0xffu) << (8 * e);
+    const float q = FAST ? div_rn_recip(x[e], sc, rc) : fminf(fmaxf(x[e] / sc, -127.0f), 127.0f);
+    b[e] = code_bits(q);
   }
-  return p;
+  return pack_low_bytes(b[0], b[1], b[2], b[3]);
 }
 
 __device__ __forceinline__ void chunk_store_int8(const RowChunk& r, float sc, int8_t* row_codes, int c) {
@@ -357,17 +392,28 @@ __device__ __forceinline__ void chunk_store_int8(const RowChunk& r, float sc, in
   *reinterpret_cast<uint2*>(row_codes + 64 + 8 * c) = b;
 }
 
-// kv_append_kernel for an INT8 cache, in the chunk-pair layout: a block takes
-// kAppendTok tokens, first every key row (rotated and rounded to bf16 -- the
-// value a bf16 cache would hold), then every value row, each quantised with one
-// fp32 scale per cache row: scale = max|x| / 127.  NT * heads * 8 is a multiple
-// of 32, so every warp covers whole rows and runs each loop as often as the others.
-constexpr int kAppendTok = 8;
-
-__global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendLaunch a, const InvFreq f) {
+// kv_append_kernel for an INT8 cache, in the chunk-pair layout.  One thread
+// takes one (token, head, chunk pair) for both the key row and the value row:
+// it issues the four 16-byte loads first, then rotates the key chunks (rounded
+// to bf16 -- the value a bf16 cache would hold), takes each row's max |x| over
+// the eight lanes that hold it, and writes both rows' codes, each row with one
+// fp32 scale = max|x| / 127.  A block holds kAppendTok tokens, so each of its
+// loops covers 32 * heads items: every warp takes whole rows and runs the loop
+// as often as the others.
+constexpr int kAppendTok = 4;
+__global__ void __launch_bounds__(256, 4) kv_append_int8_kernel(AppendLaunch a, const InvFreq f) {
   __shared__ __align__(16) float cs_s[kAppendTok][64], sn_s[kAppendTok][64];
   __shared__ int64_t slot_s[kAppendTok];
   const int64_t t0 = (int64_t)blockIdx.x * kAppendTok;
+  const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
+  const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
+  __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
+  const int items = kAppendTok * a.heads * 8;
+  GridWalk gw(threadIdx.x, blockDim.x, 8, a.heads);
+  // The first item's key and value chunks are requested before anything else:
+  // they depend on neither the slots nor the angle tables.
+  RawPair kraw, vraw;
+  if (threadIdx.x < items) load_raw(kn, vn, t0, gw, a.heads, a.tokens, kraw, vraw);
   if (threadIdx.x < kAppendTok) {
     const int64_t t = t0 + threadIdx.x;
     int64_t sl = -1;
@@ -383,35 +429,34 @@ __global__ void __launch_bounds__(256) kv_append_int8_kernel(AppendLaunch a, con
   const bool rotate = a.base > 0.0;
   if (rotate) angle_tables<kAppendTok, 64>(cs_s, sn_s, t0, a.tokens, 64, a.positions, f);
   __syncthreads();
-  const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
-  const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
-  __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
-  const int items = kAppendTok * a.heads * 8;
-  for (int pass = 0; pass < 2; ++pass) {  // keys, then values
-    const bool is_v = pass == 1;
-    GridWalk gw(threadIdx.x, blockDim.x, 8, a.heads);
-    for (int it = threadIdx.x; it < items; it += blockDim.x, gw.next()) {
-      const int c = gw.c, tt = gw.tt, h = gw.h;
-      const int64_t sl = slot_s[tt];
-      const bool ok = sl >= 0;  // tokens past the end carry slot -1
-      const int64_t src = ((t0 + tt) * a.heads + h) * 128;
-      RowChunk r;
-      load_chunk((is_v ? vn : kn) + src, c, ok, r);
-      if (!is_v && rotate) rotate_chunk(r, cs_s[tt], sn_s[tt], c);
-      if (!is_v && ko && ok) {
-        uint4 o1, o2;
-        o1.x = pack_bf16x2(r.a[0], r.a[1]), o1.y = pack_bf16x2(r.a[2], r.a[3]);
-        o1.z = pack_bf16x2(r.a[4], r.a[5]), o1.w = pack_bf16x2(r.a[6], r.a[7]);
-        o2.x = pack_bf16x2(r.b[0], r.b[1]), o2.y = pack_bf16x2(r.b[2], r.b[3]);
-        o2.z = pack_bf16x2(r.b[4], r.b[5]), o2.w = pack_bf16x2(r.b[6], r.b[7]);
-        *reinterpret_cast<uint4*>(ko + src + 8 * c) = o1;
-        *reinterpret_cast<uint4*>(ko + src + 64 + 8 * c) = o2;
-      }
-      const float sc = chunk_amax(r) / 127.0f;
-      if (ok) {
-        const int64_t row = (int64_t)h * a.cache_rows + sl;
-        chunk_store_int8(r, sc, (int8_t*)(is_v ? a.v_cache : a.k_cache) + row * 128, c);
-        if (c == 0) (is_v ? a.v_scale : a.k_scale)[row] = sc;
+  for (int it = threadIdx.x; it < items; it += blockDim.x, gw.next()) {
+    const int c = gw.c, tt = gw.tt, h = gw.h;
+    if (it != (int)threadIdx.x) load_raw(kn, vn, t0, gw, a.heads, a.tokens, kraw, vraw);
+    const int64_t sl = slot_s[tt];
+    const bool ok = sl >= 0;  // tokens past the end carry slot -1
+    const int64_t src = ((t0 + tt) * a.heads + h) * 128;
+    RowChunk rk, rv;
+    unpack_chunk(kraw, rk);
+    unpack_chunk(vraw, rv);
+    if (rotate) rotate_chunk(rk, cs_s[tt], sn_s[tt], c);
+    if (ko && ok) {
+      uint4 o1, o2;
+      o1.x = pack_bf16x2(rk.a[0], rk.a[1]), o1.y = pack_bf16x2(rk.a[2], rk.a[3]);
+      o1.z = pack_bf16x2(rk.a[4], rk.a[5]), o1.w = pack_bf16x2(rk.a[6], rk.a[7]);
+      o2.x = pack_bf16x2(rk.b[0], rk.b[1]), o2.y = pack_bf16x2(rk.b[2], rk.b[3]);
+      o2.z = pack_bf16x2(rk.b[4], rk.b[5]), o2.w = pack_bf16x2(rk.b[6], rk.b[7]);
+      *reinterpret_cast<uint4*>(ko + src + 8 * c) = o1;
+      *reinterpret_cast<uint4*>(ko + src + 64 + 8 * c) = o2;
+    }
+    const float sk = chunk_amax(rk) / 127.0f;
+    const float sv = chunk_amax(rv) / 127.0f;
+    if (ok) {
+      const int64_t row = (int64_t)h * a.cache_rows + sl;
+      chunk_store_int8(rk, sk, (int8_t*)a.k_cache + row * 128, c);
+      chunk_store_int8(rv, sv, (int8_t*)a.v_cache + row * 128, c);
+      if (c == 0) {
+        a.k_scale[row] = sk;
+        a.v_scale[row] = sv;
       }
     }
   }
