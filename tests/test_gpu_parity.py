@@ -1311,3 +1311,33 @@ def test_sp_kernel_callables_single_rank():
     out, lse = sp.ring_attention(qd[ri].contiguous(), kd, vd, posd[ri].contiguous(), posd)
     atc.attn_device_status()
     check(out, lse, wo[rows], wl[rows], what="sp.ring_attention, one rank")
+
+
+def test_prefill_fused_query_rope_on_gapped_shards():
+    """The fused query RoPE on a zigzag query shard against the other rank's zigzag
+    key shard (SGLang page, section 3.5): positions jump inside both the query and
+    the key tiles.  Bit-identical to rope_apply followed by attn_prefill, and
+    within tolerance of the oracle."""
+    T, world = 1200, 2
+    q, k, v, pos = _shard_case(T, 16, 2, 1240)
+    qrows = synth.shard_rows(T, world, 1, "zigzag")
+    krows = synth.shard_rows(T, world, 0, "zigzag")
+    qs, ks, vs = q[qrows].contiguous(), k[krows].contiguous(), v[krows].contiguous()
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(DEV)
+    qpos, kpos = i32(pos[qrows]), i32(pos[krows])
+    cu_q, cu_k = i32([0, len(qrows)]), i32([0, len(krows)])
+    kd = ks.to(DEV)
+    atc.rope_apply(kd, kpos)
+    vd = vs.to(DEV)
+    qr = qs.to(DEV)
+    atc.rope_apply(qr, qpos)
+    ref_o, ref_l = atc.prefill(qr, kd, vd, cu_q, qpos, len(qrows), cu_k=cu_k, k_pos=kpos)
+    qd = qs.to(DEV)
+    tab = atc.rope_table(qpos, 128)
+    out, lse = atc.prefill(qd, kd, vd, cu_q, qpos, len(qrows), cu_k=cu_k, k_pos=kpos, q_rope_cs=tab)
+    atc.attn_device_status()
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    wo, wl = oracle.attention(rotated_bf16(qs, pos[qrows]), np.zeros(len(qrows), np.int32), pos[qrows],
+                              rotated_bf16(ks, pos[krows]), synth.as_f64(vs), [0, len(krows)], pos[krows],
+                              128 ** -0.5)
+    check(out, lse, wo, wl, what="fused query RoPE, zigzag shards")
