@@ -894,6 +894,8 @@ def main():
         pg = dist
     peaks, peak_src = load_peaks()
     timer = Timer()
+    # the oracle baselines run on the host cores once: rank 0 of a single-GPU run
+    cpu_leg = not args.no_cpu_baseline and ws == 1 and rank == 0
     wl = synth.PREFILL_8K
     res = None
     if args.workload in ("all", "prefill"):
@@ -913,7 +915,7 @@ def main():
             import dataclasses
             dwl = dataclasses.replace(dwl, batch=args.decode_requests,
                                       name=dwl.name.replace("B32", f"B{args.decode_requests}"))
-        dec = decode_arm(dwl, args, timer, peaks, peak_src, cpu=not args.no_cpu_baseline)
+        dec = decode_arm(dwl, args, timer, peaks, peak_src, cpu=cpu_leg)
         torch.cuda.empty_cache()
         dwl8 = synth.DECODE_INT8
         if args.decode_requests:
@@ -955,7 +957,7 @@ def main():
                      "config": prefill_config(wl, ws),
                      "roofline": res["roofline"], "e2e": res["e2e"], "clocks": clocks,
                      "launch": res["launch"], "gpu_launches": res["launches_per_step"] * args.steps})
-        if not args.no_cpu_baseline:
+        if cpu_leg:
             line["cpu_baseline"] = cpu_baseline(wl, res["inputs"])
         line["rope"] = res["rope"]
     else:
@@ -969,7 +971,7 @@ def main():
     line.update(extra)
     if dec:
         line["decode_detail"] = dec
-    if not args.no_cpu_baseline:
+    if cpu_leg:
         line["oracle_tiny"] = oracle_tiny_timing()
     if dec:
         line["decode"] = compact_decode(dec)  # last: the decode half of the metric in brief
