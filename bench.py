@@ -541,13 +541,19 @@ def decode_arm(wl, args, timer, peaks, peak_src, cpu=True):
     return res
 
 
-def long_prefill_arm(wl, args, timer, peaks, peak_src):
+def long_prefill_arm(wl, args, timer, peaks, peak_src, cpu=False):
     """2 x 65536-token causal prefill: all 64 heads, and heads 16..31 alone (one
     Ulysses rank's share of a 4-way head split).  Attention only: RoPE is applied
     once before the timed calls."""
     import attention_tiled_causal_gb300 as atc
+    import synth
     inp = wl.make("cuda")
     q, k, v, pos, cu = inp["q"], inp["k"], inp["v"], inp["pos"], inp["cu"]
+    sample = None
+    if cpu:  # the oracle's inputs, taken before the in-place RoPE
+        rows = np.concatenate([synth.sample_rows(wl.seq, 16, 77 + b) + b * wl.seq for b in range(wl.batch)])
+        sample = (rows, q[torch.from_numpy(rows).to(q.device)].cpu(), k.cpu(), v.cpu(), pos.cpu().numpy(),
+                  cu.cpu().numpy())
     atc.rope_apply(q, pos)
     atc.rope_apply(k, pos)
     out = torch.empty_like(q)
@@ -567,10 +573,67 @@ def long_prefill_arm(wl, args, timer, peaks, peak_src):
                                    "peak_source": f"{peak_src} bf16 dense (burst)"}
     atc.attn_device_status()
     del inp, q, k, v, out
+    if sample is not None:
+        res["cpu_baseline"] = oracle_long_baseline(wl, *sample)
     return res
 
 
-def chunked_arm(wl, args, timer, peaks, peak_src):
+def oracle_long_baseline(wl, rows, qs, k, v, pos, cu):
+    """The oracle on 16 seeded query rows per sequence of the 2 x 65536-token
+    workload, all 64 heads: RoPE of those rows and of every key, bf16 rounding,
+    fp64 three-pass attention (input widening outside the timed part)."""
+    import oracle
+    qf, kf, vf = (t.to(torch.float64).numpy() for t in (qs, k, v))
+    t0 = time.perf_counter()
+    qr = oracle.round_bf16(oracle.rope(qf, pos[rows], wl.base))
+    kr = oracle.round_bf16(oracle.rope(kf, pos, wl.base))
+    oracle.attention(qr, (rows // wl.seq).astype(np.int32), pos[rows], kr, vf, cu, pos, wl.scale)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * wl.d * wl.hq * float(np.sum(pos[rows] + 1))
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} seeded query rows (16 per sequence) x 64 heads of the 2 x 65536-token prefill "
+                      f"(RoPE + bf16 rounding + fp64 three-pass attention), {dt:.1f} s"}
+
+
+def oracle_chunked_baseline(wl, inp, rows, q_raw, k_raw):
+    """The oracle on 16 seeded chunk rows per request of the chunked workload,
+    all 64 heads: each row over its request's 57344 cached keys (gathered through
+    the page table) and the causal part of its chunk; RoPE of the rows and the
+    chunk keys, bf16 rounding, fp64 three-pass attention.  Page gathers and input
+    widening are outside the timed part."""
+    import oracle
+    B, P, C = wl.batch, wl.prefix, wl.chunk
+    table = inp["page_table"].cpu().numpy()
+    qpos = inp["q_pos"].cpu().numpy()
+    dt, flops = 0.0, 0.0
+    for b in range(B):
+        sel = np.nonzero((rows // C) == b)[0]
+        n = (P + 63) // 64
+        pages = torch.from_numpy(table[b, :n].astype(np.int64)).to(inp["k_cache"].device)
+        kc = inp["k_cache"][:, pages].cpu().to(torch.float64).numpy().transpose(1, 2, 0, 3).reshape(n * 64, wl.hkv,
+                                                                                                    wl.d)[:P]
+        vc = inp["v_cache"][:, pages].cpu().to(torch.float64).numpy().transpose(1, 2, 0, 3).reshape(n * 64, wl.hkv,
+                                                                                                    wl.d)[:P]
+        kch = k_raw[b * C:(b + 1) * C].to(torch.float64).numpy()
+        vch = inp["v"][b * C:(b + 1) * C].cpu().to(torch.float64).numpy()
+        qb = q_raw[sel].to(torch.float64).numpy()
+        rp = qpos[rows[sel]]
+        t0 = time.perf_counter()
+        qr = oracle.round_bf16(oracle.rope(qb, rp, wl.base))
+        kr = oracle.round_bf16(oracle.rope(kch, qpos[b * C:(b + 1) * C], wl.base))
+        K = np.concatenate([kc, kr])
+        V = np.concatenate([vc, vch])
+        KP = np.concatenate([np.arange(P, dtype=np.int32), qpos[b * C:(b + 1) * C]])
+        oracle.attention(qr, np.zeros(len(sel), np.int32), rp, K, V, [0, P + C], KP, wl.scale)
+        dt += time.perf_counter() - t0
+        flops += 4.0 * wl.d * wl.hq * float(np.sum(rp + 1))
+        del kc, vc, K, V
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} seeded chunk rows (16 per request) x 64 heads of the chunked prefill over the "
+                      f"57344-token paged prefix (RoPE + bf16 rounding + fp64 three-pass attention), {dt:.1f} s"}
+
+
+def chunked_arm(wl, args, timer, peaks, peak_src, cpu=False):
     """Chunked prefill: 4 requests, each an 8192-token chunk over a 57344-token
     prefix in a shuffled head-major paged cache.  One step = the paged-prefix
     call + the causal chunk call + the LSE merge of the two partial results.  Also
@@ -581,6 +644,10 @@ def chunked_arm(wl, args, timer, peaks, peak_src):
     inp = wl.make("cuda")
     C = wl.chunk
     q, k, v = inp["q"], inp["k"], inp["v"]
+    sample = None
+    if cpu:  # the oracle's chunk rows and keys, taken before the in-place RoPE
+        rows = np.concatenate([synth.sample_rows(C, 16, 88 + b) + b * C for b in range(wl.batch)])
+        sample = (rows, q[torch.from_numpy(rows).to(q.device)].cpu(), k.cpu())
     atc.rope_apply(q, inp["q_pos"])
     atc.rope_apply(k, inp["q_pos"])
     T, hq, d = q.shape
@@ -610,7 +677,9 @@ def chunked_arm(wl, args, timer, peaks, peak_src):
     ms_c, _ = timer.run(chunk, steps, warmup)
     ms_m = short_ms(timer, merge, steps, warmup)
     merge_bytes = po.numel() * 4 + pl.numel() * 4 + out.numel() * 2 + lse.numel() * 4
-    del po, pl, inp
+    del po, pl
+    cpu_res = oracle_chunked_baseline(wl, inp, *sample) if sample is not None else None
+    del inp
 
     # The serving flow: append the chunk's K (rotated) and V to a paged cache that
     # has room for it, then one paged causal call over prefix + chunk.
@@ -673,7 +742,8 @@ def chunked_arm(wl, args, timer, peaks, peak_src):
                 "append": hbm_line("attn_kv_append_paged (4 x 8192 tokens, 8 KV heads)", append_bytes, ms_a, peaks,
                                    peak_src),
                 "append_int8": hbm_line("attn_kv_append_paged_int8 (the same chunk into an INT8 cache)",
-                                        append8_bytes, ms_a8, peaks, peak_src)}}
+                                        append8_bytes, ms_a8, peaks, peak_src)},
+            **({"cpu_baseline": cpu_res} if cpu_res else {})}
 
 
 def append_arm(wl, args, timer, peaks, peak_src):
@@ -930,10 +1000,10 @@ def main():
         extra["prefill_fp8"] = fp8_prefill_arm(wl, args, timer, peaks, peak_src, res["inputs"] if res else None)
         torch.cuda.empty_cache()
     if args.workload in ("all", "long"):
-        extra["prefill_64k"] = long_prefill_arm(synth.PREFILL_64K, args, timer, peaks, peak_src)
+        extra["prefill_64k"] = long_prefill_arm(synth.PREFILL_64K, args, timer, peaks, peak_src, cpu=cpu_leg)
         torch.cuda.empty_cache()
     if args.workload in ("all", "chunked"):
-        extra["chunked"] = chunked_arm(synth.CHUNKED, args, timer, peaks, peak_src)
+        extra["chunked"] = chunked_arm(synth.CHUNKED, args, timer, peaks, peak_src, cpu=cpu_leg)
         torch.cuda.empty_cache()
     if args.workload == "append":
         extra["append"] = append_arm(synth.CHUNKED, args, timer, peaks, peak_src)
