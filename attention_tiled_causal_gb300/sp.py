@@ -2,6 +2,9 @@
 torch.distributed (any backend with all_to_all_single and isend/irecv: NCCL
 between GPUs, gloo between CPU processes).
 
+Device tensors exchanged over a gloo group (which moves host tensors only) go
+through host memory; over NCCL they move device to device.
+
 Two ways of spreading one long sequence over P ranks:
 
   * Ulysses ("Ulysses sequence parallelism for inference", sections 2.1-2.2):
@@ -81,13 +84,37 @@ def _world(group) -> Tuple[int, int]:
     return dist.get_world_size(group), dist.get_rank(group)
 
 
+def _host_staged(group, t: Tensor) -> bool:
+    """gloo moves host tensors only: device tensors go through host memory."""
+    return t.is_cuda and dist.get_backend(group) == "gloo"
+
+
+def _all_to_all(recv: Tensor, send: Tensor, out_splits, in_splits, group) -> None:
+    if _host_staged(group, send):
+        rh = torch.empty(recv.shape, dtype=recv.dtype)
+        dist.all_to_all_single(rh, send.cpu(), output_split_sizes=out_splits, input_split_sizes=in_splits,
+                               group=group)
+        recv.copy_(rh)
+    else:
+        dist.all_to_all_single(recv, send, output_split_sizes=out_splits, input_split_sizes=in_splits, group=group)
+
+
+def _all_gather(out: Tensor, t: Tensor, group) -> None:
+    if _host_staged(group, t):
+        oh = torch.empty(out.shape, dtype=out.dtype)
+        dist.all_gather_into_tensor(oh, t.cpu(), group=group)
+        out.copy_(oh)
+    else:
+        dist.all_gather_into_tensor(out, t, group=group)
+
+
 def _counts(n_local: int, group, device) -> list:
     """Every rank's local token count, in rank order."""
     world, _ = _world(group)
     if world == 1:
         return [n_local]
     out = torch.zeros(world, dtype=torch.int64, device=device)
-    dist.all_gather_into_tensor(out, torch.tensor([n_local], dtype=torch.int64, device=device), group=group)
+    _all_gather(out, torch.tensor([n_local], dtype=torch.int64, device=device), group)
     return [int(c) for c in out.cpu()]
 
 
@@ -108,7 +135,7 @@ def seq_to_heads(x: Tensor, group=None, counts: Optional[Sequence[int]] = None) 
     # per destination rank r: this rank's tokens for heads [r*hp, (r+1)*hp), contiguous
     send = x.reshape(T, world, hp, *rest).transpose(0, 1).contiguous().reshape(world * T, hp, *rest)
     recv = torch.empty((sum(counts), hp) + rest, dtype=x.dtype, device=x.device)
-    dist.all_to_all_single(recv, send, output_split_sizes=counts, input_split_sizes=[T] * world, group=group)
+    _all_to_all(recv, send, counts, [T] * world, group)
     return recv
 
 
@@ -124,8 +151,7 @@ def heads_to_seq(y: Tensor, counts: Sequence[int], group=None) -> Tensor:
     rest = tuple(y.shape[2:])
     T = counts[rank]
     recv = torch.empty((world * T, hp) + rest, dtype=y.dtype, device=y.device)
-    dist.all_to_all_single(recv, y.contiguous(), output_split_sizes=[T] * world, input_split_sizes=list(counts),
-                           group=group)
+    _all_to_all(recv, y.contiguous(), [T] * world, list(counts), group)
     # recv block r: this rank's tokens for rank r's heads
     return recv.reshape(world, T, hp, *rest).transpose(0, 1).reshape(T, world * hp, *rest)
 
@@ -139,7 +165,7 @@ def gather_positions(pos: Tensor, counts: Sequence[int], group=None) -> Tensor:
     pad = torch.zeros(n, dtype=pos.dtype, device=pos.device)
     pad[:pos.numel()] = pos
     allp = torch.zeros(world * n, dtype=pos.dtype, device=pos.device)
-    dist.all_gather_into_tensor(allp, pad, group=group)
+    _all_gather(allp, pad, group)
     return torch.cat([allp[r * n:r * n + c] for r, c in enumerate(counts)])
 
 
@@ -182,13 +208,17 @@ def ring_attention(q: Tensor, k: Tensor, v: Tensor, q_pos: Tensor, k_pos: Tensor
     merge = merge or kernel_merge
     cur = [k.contiguous(), v.contiguous(), k_pos.contiguous()]
     nxt = [torch.empty_like(t) for t in cur] if world > 1 else None
+    staged = world > 1 and _host_staged(group, k)
     outs, lses = [], []
     for step in range(world):
         reqs = []
         if step < world - 1:
             dst, src = (rank + 1) % world, (rank - 1) % world
-            ops = [dist.P2POp(dist.irecv, t, src, group) for t in nxt] + \
-                  [dist.P2POp(dist.isend, t, dst, group) for t in cur]
+            # through host buffers when the backend moves host tensors only
+            send = [t.cpu() for t in cur] if staged else cur
+            recv = [torch.empty(t.shape, dtype=t.dtype) for t in nxt] if staged else nxt
+            ops = [dist.P2POp(dist.irecv, t, src, group) for t in recv] + \
+                  [dist.P2POp(dist.isend, t, dst, group) for t in send]
             reqs = dist.batch_isend_irecv(ops)
         o, l = partial(q, cur[0], cur[1], q_pos, cur[2])
         outs.append(o)
@@ -196,6 +226,9 @@ def ring_attention(q: Tensor, k: Tensor, v: Tensor, q_pos: Tensor, k_pos: Tensor
         for r in reqs:
             r.wait()
         if step < world - 1:
+            if staged:
+                for d, h in zip(nxt, recv):
+                    d.copy_(h)
             cur, nxt = nxt, cur
     return merge(torch.stack(outs), torch.stack(lses))
 

@@ -1,0 +1,107 @@
+"""The sequence-parallel host code with the CUDA kernels doing each rank's
+attention: two gloo ranks, spawned as two processes sharing the one GPU (their
+exchanges go through host memory; no kernel waits on the other process).  Ring
+attention over zigzag shards (SGLang page, section 3.5) and Ulysses attention
+over contiguous shards (Ulysses page, section 2.2) are compared, rank by rank,
+with the fp64 oracle's unsplit result at the bf16 tolerances."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL_MAX, TOL_MEAN, TOL_LSE = 1e-2, 1e-3, 1e-3
+T, HQ, HKV, D, WORLD = 1200, 16, 2, 128, 2
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _inputs():
+    q = synth.randn((T, HQ, D), 1400, 0.7071)
+    k = synth.randn((T, HKV, D), 1401, 0.7071)
+    v = synth.randn((T, HKV, D), 1402, 0.7071)
+    return q, k, v, np.arange(T, dtype=np.int32)
+
+
+def _rank(rank, world, port, out_q):
+    import torch.distributed as dist
+
+    import attention_tiled_causal_gb300 as atc
+    from attention_tiled_causal_gb300 import sp
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(0)
+    q, k, v, pos = _inputs()
+    dev = "cuda"
+    res = {}
+    # ring over zigzag shards: each rank holds its shard's rows, rotated at their positions
+    rows = sp.shard_rows(T, world, rank, "zigzag")
+    ri = torch.from_numpy(rows)
+    qd, kd, vd = q[ri].to(dev), k[ri].to(dev), v[ri].to(dev)
+    pd = torch.from_numpy(pos[rows]).to(dev)
+    atc.rope_apply_qk(qd, kd, pd)
+    o, l = sp.ring_attention(qd, kd, vd, pd, pd)
+    atc.attn_device_status()
+    res["ring"] = (rows, o.cpu().numpy(), l.cpu().numpy())
+    # Ulysses over contiguous shards
+    rows = sp.shard_rows(T, world, rank, "contiguous")
+    ri = torch.from_numpy(rows)
+    qd, kd, vd = q[ri].to(dev), k[ri].to(dev), v[ri].to(dev)
+    pd = torch.from_numpy(pos[rows]).to(dev)
+    atc.rope_apply_qk(qd, kd, pd)
+    o, l = sp.ulysses_attention(qd, kd, vd, pd)
+    atc.attn_device_status()
+    res["ulysses"] = (rows, o.float().cpu().numpy(), l.cpu().numpy())
+    out_q.put((rank, res))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def _check(o, l, wo, wl, what):
+    d = np.abs(o - wo)
+    assert np.isfinite(o).all(), what
+    assert d.max() <= TOL_MAX, f"{what}: max |dO| = {d.max():.3g}"
+    assert d.mean() <= TOL_MEAN, f"{what}: mean |dO| = {d.mean():.3g}"
+    inf = np.isinf(wl)
+    assert np.array_equal(np.isinf(l), inf), what
+    assert np.abs(l[~inf] - wl[~inf]).max() <= TOL_LSE, what
+
+
+def test_ring_and_ulysses_attention_on_two_processes():
+    ctx = mp.get_context("spawn")
+    out_q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, WORLD, port, out_q)) for r in range(WORLD)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(WORLD):
+        r, res = out_q.get(timeout=600)
+        got[r] = res
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    q, k, v, pos = _inputs()
+    qr = oracle.round_bf16(oracle.rope(synth.as_f64(q), pos))
+    kr = oracle.round_bf16(oracle.rope(synth.as_f64(k), pos))
+    wo, wl = oracle.attention(qr, np.zeros(T, np.int32), pos, kr, synth.as_f64(v), [0, T], pos, D ** -0.5)
+    for kind in ("ring", "ulysses"):
+        seen = []
+        for r in range(WORLD):
+            rows, o, l = got[r][kind]
+            _check(o, l, wo[rows], wl[rows], f"{kind} rank {r}")
+            seen += rows.tolist()
+        assert sorted(seen) == list(range(T))
