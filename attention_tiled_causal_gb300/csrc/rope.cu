@@ -82,23 +82,25 @@ struct GridWalk {
   }
 };
 
-// cos and sin of pos * base^(-2i/d) for the block's NT tokens, i < d/2, into
-// shared memory.  The angle is reduced modulo one turn exactly, in integers
-// (InvFreq); its top 32 bits, as a signed fraction of a turn in [-1/2, 1/2),
-// go to sincospif.  No fp64 arithmetic, which runs at a small fraction of the
-// fp32 rate on this GPU.  Every kernel that rotates calls this, so their
-// results agree bit for bit.
+// sin and cos of p * base^(-2i/d) (turns = InvFreq::turns[i]).  The angle is
+// reduced modulo one turn exactly, in integers; its top 32 bits, as a signed
+// fraction of a turn in [-1/2, 1/2), go to sincospif.  No fp64 arithmetic,
+// which runs at a small fraction of the fp32 rate on this GPU.  Every kernel
+// that rotates takes its angles from here, so their results agree bit for bit.
+__device__ __forceinline__ void pair_sincos(int32_t p, uint64_t turns, float& sn, float& cs) {
+  const uint64_t phase = (uint64_t)(int64_t)p * turns;  // mod 2^64: the fraction of a turn
+  const int32_t hi = (int32_t)(phase >> 32);            // turns * 2^32 in [-2^31, 2^31)
+  sincospif((float)hi * 0x1p-31f, &sn, &cs);            // angle = 2 pi * turns
+}
+
+// The block's NT tokens' tables (cos and sin for i < d/2) in shared memory.
 template <int NT = kTok, int W = 128>
 __device__ __forceinline__ void angle_tables(float (*cs_s)[W], float (*sn_s)[W], int64_t t0, int64_t tokens,
                                              int half, const int32_t* __restrict__ pos, const InvFreq& f) {
   for (int i = threadIdx.x; i < NT * half; i += blockDim.x) {
     const int tt = i / half, ii = i % half;
     const int64_t t = t0 + tt;
-    if (t < tokens) {
-      const uint64_t phase = (uint64_t)(int64_t)__ldg(pos + t) * f.turns[ii];  // mod 2^64: the fraction of a turn
-      const int32_t hi = (int32_t)(phase >> 32);                               // turns * 2^32 in [-2^31, 2^31)
-      sincospif((float)hi * 0x1p-31f, &sn_s[tt][ii], &cs_s[tt][ii]);           // angle = 2 pi * turns
-    }
+    if (t < tokens) pair_sincos(__ldg(pos + t), f.turns[ii], sn_s[tt][ii], cs_s[tt][ii]);
   }
   __syncthreads();
 }
@@ -338,7 +340,33 @@ __device__ __forceinline__ void rotate_chunk(RowChunk& r, const float* cs_row, c
   }
 }
 
-// max |x| over the row (the eight lanes holding it).
+// rotate_chunk on packed pairs of lanes e, e + 1: y1 = x1 cos + RN(x2 * -sin)
+// and y2 = x2 cos + RN(x1 sin), each one two-lane FMA after a two-lane
+// product.  x2 * -sin is -(x2 * sin) exactly, so the bits are rope_rotate's.
+// nsn_row: the token's sines with the sign flipped.
+__device__ __forceinline__ void rotate_chunk_packed(RowChunk& r, const float* cs_row, const float* sn_row,
+                                                    const float* nsn_row, int c) {
+  const float4* c4 = reinterpret_cast<const float4*>(cs_row) + 2 * c;
+  const float4* s4 = reinterpret_cast<const float4*>(sn_row) + 2 * c;
+  const float4* n4 = reinterpret_cast<const float4*>(nsn_row) + 2 * c;
+  const float4 ca = c4[0], cb = c4[1], sa = s4[0], sb = s4[1], na = n4[0], nb = n4[1];
+  const uint64_t cs[4] = {f2_pack(ca.x, ca.y), f2_pack(ca.z, ca.w), f2_pack(cb.x, cb.y), f2_pack(cb.z, cb.w)};
+  const uint64_t sn[4] = {f2_pack(sa.x, sa.y), f2_pack(sa.z, sa.w), f2_pack(sb.x, sb.y), f2_pack(sb.z, sb.w)};
+  const uint64_t ns[4] = {f2_pack(na.x, na.y), f2_pack(na.z, na.w), f2_pack(nb.x, nb.y), f2_pack(nb.z, nb.w)};
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const uint64_t x1 = f2_pack(r.a[e], r.a[e + 1]), x2 = f2_pack(r.b[e], r.b[e + 1]);
+    float y10, y11, y20, y21;
+    f2_unpack(f2_fma(x1, cs[e >> 1], f2_mul(x2, ns[e >> 1])), y10, y11);
+    f2_unpack(f2_fma(x2, cs[e >> 1], f2_mul(x1, sn[e >> 1])), y20, y21);
+    const uint32_t pa = pack_bf16x2(y10, y11), pb = pack_bf16x2(y20, y21);
+    r.a[e] = __uint_as_float(pa << 16), r.a[e + 1] = __uint_as_float(pa & 0xffff0000u);
+    r.b[e] = __uint_as_float(pb << 16), r.b[e + 1] = __uint_as_float(pb & 0xffff0000u);
+  }
+}
+
+// max |x| over the row (the eight lanes holding it).  Its shuffles take all 32
+// lanes of the warp, so every caller runs it warp-uniformly.
 __device__ __forceinline__ float chunk_amax(const RowChunk& r) {
   float m = 0.f;
 #pragma unroll
@@ -363,18 +391,40 @@ __device__ __forceinline__ float chunk_amax(const RowChunk& r) {
 // subnormal and carry a large relative error) clamps.
 __device__ __forceinline__ uint32_t code_bits(float q) { return (uint32_t)__float_as_int(__fadd_rn(q, 12582912.0f)); }
 
+// RN(m / 127), the row scale: div_rn_recip with RN(1/127) for maxima whose
+// quotient is a normal number far from overflow (Markstein's conditions hold
+// there), the division otherwise (zero, tiny, infinite or NaN maxima).
+__device__ __forceinline__ float scale127(float m) {
+  constexpr float kRcp127 = 0x1.020408p-7f;  // RN(1/127)
+  return (m >= 0x1p-80f && m <= 0x1p120f) ? div_rn_recip(m, 127.0f, kRcp127) : m / 127.0f;
+}
+
 __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
   return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
 }
 
-template <bool FAST>
-__device__ __forceinline__ uint32_t int8x4(const float* x, float sc, float rc) {
+// Fast path, two lanes per instruction: q = x rc, then div_rn_recip's one
+// correction q + (x - q sc) rc with the remainder formed as fma(q, -sc, x) (the
+// same exact value), then the rounding add.  nsc2 = (-sc, -sc), rc2 = (rc, rc).
+__device__ __forceinline__ uint32_t int8x4_fast(const float* x, uint64_t nsc2, uint64_t rc2) {
+  const uint64_t m2 = f2_pack(12582912.0f, 12582912.0f);
   uint32_t b[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float q = FAST ? div_rn_recip(x[e], sc, rc) : fminf(fmaxf(x[e] / sc, -127.0f), 127.0f);
-    b[e] = code_bits(q);
+  for (int e = 0; e < 4; e += 2) {
+    const uint64_t xx = f2_pack(x[e], x[e + 1]);
+    const uint64_t q = f2_mul(xx, rc2);
+    float lo, hi;
+    f2_unpack(f2_add(f2_fma(f2_fma(q, nsc2, xx), rc2, q), m2), lo, hi);
+    b[e] = __float_as_uint(lo), b[e + 1] = __float_as_uint(hi);
   }
+  return pack_low_bytes(b[0], b[1], b[2], b[3]);
+}
+
+// The full division, clamped, for scales below the fast path's range.
+__device__ __forceinline__ uint32_t int8x4_full(const float* x, float sc) {
+  uint32_t b[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) b[e] = code_bits(fminf(fmaxf(x[e] / sc, -127.0f), 127.0f));
   return pack_low_bytes(b[0], b[1], b[2], b[3]);
 }
 
@@ -382,11 +432,12 @@ __device__ __forceinline__ void chunk_store_int8(const RowChunk& r, float sc, in
   uint2 a = make_uint2(0u, 0u), b = a;
   if (sc >= kFastDivMinScale) {
     const float rc = __frcp_rn(sc);
-    a = make_uint2(int8x4<true>(r.a, sc, rc), int8x4<true>(r.a + 4, sc, rc));
-    b = make_uint2(int8x4<true>(r.b, sc, rc), int8x4<true>(r.b + 4, sc, rc));
+    const uint64_t rc2 = f2_pack(rc, rc), nsc2 = f2_pack(-sc, -sc);
+    a = make_uint2(int8x4_fast(r.a, nsc2, rc2), int8x4_fast(r.a + 4, nsc2, rc2));
+    b = make_uint2(int8x4_fast(r.b, nsc2, rc2), int8x4_fast(r.b + 4, nsc2, rc2));
   } else if (sc != 0.0f) {
-    a = make_uint2(int8x4<false>(r.a, sc, 0.f), int8x4<false>(r.a + 4, sc, 0.f));
-    b = make_uint2(int8x4<false>(r.b, sc, 0.f), int8x4<false>(r.b + 4, sc, 0.f));
+    a = make_uint2(int8x4_full(r.a, sc), int8x4_full(r.a + 4, sc));
+    b = make_uint2(int8x4_full(r.b, sc), int8x4_full(r.b + 4, sc));
   }
   *reinterpret_cast<uint2*>(row_codes + 8 * c) = a;
   *reinterpret_cast<uint2*>(row_codes + 64 + 8 * c) = b;
@@ -399,7 +450,9 @@ __device__ __forceinline__ void chunk_store_int8(const RowChunk& r, float sc, in
 // the eight lanes that hold it, and writes both rows' codes, each row with one
 // fp32 scale = max|x| / 127.  A block holds kAppendTok tokens, so each of its
 // loops covers 32 * heads items: every warp takes whole rows and runs the loop
-// as often as the others.
+// as often as the others, as chunk_amax's shuffles require.  The launcher takes
+// this kernel only where the staged one below does not apply (more than 64
+// heads); both write the same bits.
 constexpr int kAppendTok = 4;
 __global__ void __launch_bounds__(256, 4) kv_append_int8_kernel(AppendLaunch a, const InvFreq f) {
   __shared__ __align__(16) float cs_s[kAppendTok][64], sn_s[kAppendTok][64];
@@ -448,8 +501,8 @@ __global__ void __launch_bounds__(256, 4) kv_append_int8_kernel(AppendLaunch a, 
       *reinterpret_cast<uint4*>(ko + src + 8 * c) = o1;
       *reinterpret_cast<uint4*>(ko + src + 64 + 8 * c) = o2;
     }
-    const float sk = chunk_amax(rk) / 127.0f;
-    const float sv = chunk_amax(rv) / 127.0f;
+    const float sk = scale127(chunk_amax(rk));
+    const float sv = scale127(chunk_amax(rv));
     if (ok) {
       const int64_t row = (int64_t)h * a.cache_rows + sl;
       chunk_store_int8(rk, sk, (int8_t*)a.k_cache + row * 128, c);
@@ -462,9 +515,202 @@ __global__ void __launch_bounds__(256, 4) kv_append_int8_kernel(AppendLaunch a, 
   }
 }
 
+// A wait for a staged copy that ends on the phase or on its own time limit
+// only: an error another block records (a bad slot, which is skipped) must not
+// stop the append, as it would through mbar_wait.
+__device__ __forceinline__ bool append_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
+// Contiguous global bytes into shared memory (cp.async.bulk), counted on bar.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// kv_append_int8_kernel with the new rows staged through shared memory.  A
+// persistent block walks groups of G whole tokens, whose G * heads key rows
+// (and value rows) are contiguous in k_new (v_new); its thread 0 keeps the
+// next group's bytes in flight (two cp.async.bulk per group into one of two
+// buffers, counted on that buffer's mbarrier) while the block rotates and
+// quantises the current group, so the memory system never waits on the
+// arithmetic.  Per item the arithmetic is kv_append_int8_kernel's, on packed
+// lane pairs where it can be.
+//
+// Shared memory: four buffers of G * heads * 256 bytes (K and V of buffers 0
+// and 1), then cos, sin and -sin tables [G][64] and the group's slots [G].
+// The item loop runs over whole warps (chunk_amax's shuffles take all 32
+// lanes); the lanes past G * heads * 8 items form whole 8-lane rows, take
+// zeros and store nothing.  A copy that does not land within the wait limit
+// records DEV_TIMEOUT_APPEND; the block then lets the copies it has in flight
+// land (bounded) and returns.
+__global__ void __launch_bounds__(256, 4) kv_append_int8_staged_kernel(AppendLaunch a, const InvFreq f, int G,
+                                                                       int64_t groups) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ uint64_t full[2];
+  const int heads = a.heads;
+  const uint32_t gbytes = (uint32_t)G * heads * 256;  // one group of K (or V)
+  float (*cs_s)[64] = reinterpret_cast<float (*)[64]>(dsm + 4 * gbytes);
+  float (*sn_s)[64] = cs_s + G;
+  float (*nsn_s)[64] = sn_s + G;
+  int64_t* slot_s = reinterpret_cast<int64_t*>(nsn_s + G);
+  const char* kn = (const char*)a.k_new;
+  const char* vn = (const char*)a.v_new;
+  __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
+  auto issue = [&](int64_t g, int b) {
+    const int64_t t0 = g * G;
+    const uint32_t bytes = (uint32_t)(min((int64_t)G, a.tokens - t0) * heads * 256);
+    mbar_arrive_expect_tx(&full[b], 2 * bytes);
+    bulk_copy_g2s(dsm + (2 * b) * gbytes, kn + t0 * heads * 256, bytes, &full[b]);
+    bulk_copy_g2s(dsm + (2 * b + 1) * gbytes, vn + t0 * heads * 256, bytes, &full[b]);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    issue(blockIdx.x, 0);
+    if (blockIdx.x + gridDim.x < groups) issue(blockIdx.x + gridDim.x, 1);
+  }
+  const int items = G * heads * 8;
+  const int items_w = (items + 31) & ~31;
+  const GridWalk gw0(threadIdx.x, blockDim.x, 8, heads);
+  const bool rotate = a.base > 0.0;
+  int i = 0;
+  bool failed = false;
+  for (int64_t g = blockIdx.x; g < groups; g += gridDim.x, ++i) {
+    const int b = i & 1;
+    const int64_t t0 = g * G;
+    if (threadIdx.x < G) {
+      const int64_t t = t0 + threadIdx.x;
+      int64_t sl = -1;
+      if (t < a.tokens) {
+        sl = __ldg(a.slots + t);
+        if (sl < -1 || sl >= a.cache_rows) {
+          record_error(a.err, DEV_BAD_SLOT);
+          sl = -1;
+        }
+      }
+      slot_s[threadIdx.x] = sl;
+    }
+    if (rotate)
+      for (int j = threadIdx.x; j < G * 64; j += blockDim.x) {
+        const int tt = j >> 6, ii = j & 63;
+        if (t0 + tt < a.tokens) {
+          float sn, cs;
+          pair_sincos(__ldg(a.positions + t0 + tt), f.turns[ii], sn, cs);
+          sn_s[tt][ii] = sn;
+          nsn_s[tt][ii] = -sn;
+          cs_s[tt][ii] = cs;
+        }
+      }
+    // one barrier publishes the tables and slots and agrees on the wait
+    if (!__syncthreads_and(append_wait(&full[b], (i >> 1) & 1))) {
+      failed = true;
+      break;
+    }
+    const uint8_t* kb = dsm + (2 * b) * gbytes;
+    const uint8_t* vb = kb + gbytes;
+    GridWalk gw = gw0;
+    for (int it = threadIdx.x; it < items_w; it += blockDim.x, gw.next()) {
+      const bool live = it < items;
+      const int c = gw.c, tt = gw.tt, h = gw.h;
+      const int64_t sl = live ? slot_s[tt] : -1;
+      const bool ok = sl >= 0;  // tokens past the end carry slot -1
+      RawPair kraw, vraw;
+      kraw.lo = kraw.hi = vraw.lo = vraw.hi = make_uint4(0u, 0u, 0u, 0u);
+      if (live) {
+        const uint32_t off = (uint32_t)((tt * heads + h) * 256 + 16 * c);
+        kraw.lo = *reinterpret_cast<const uint4*>(kb + off);
+        kraw.hi = *reinterpret_cast<const uint4*>(kb + off + 128);
+        vraw.lo = *reinterpret_cast<const uint4*>(vb + off);
+        vraw.hi = *reinterpret_cast<const uint4*>(vb + off + 128);
+      }
+      RowChunk rk, rv;
+      unpack_chunk(kraw, rk);
+      unpack_chunk(vraw, rv);
+      if (rotate && live) rotate_chunk_packed(rk, cs_s[tt], sn_s[tt], nsn_s[tt], c);
+      if (ko && ok) {
+        const int64_t src = ((t0 + tt) * heads + h) * 128;
+        uint4 o1, o2;
+        o1.x = pack_bf16x2(rk.a[0], rk.a[1]), o1.y = pack_bf16x2(rk.a[2], rk.a[3]);
+        o1.z = pack_bf16x2(rk.a[4], rk.a[5]), o1.w = pack_bf16x2(rk.a[6], rk.a[7]);
+        o2.x = pack_bf16x2(rk.b[0], rk.b[1]), o2.y = pack_bf16x2(rk.b[2], rk.b[3]);
+        o2.z = pack_bf16x2(rk.b[4], rk.b[5]), o2.w = pack_bf16x2(rk.b[6], rk.b[7]);
+        *reinterpret_cast<uint4*>(ko + src + 8 * c) = o1;
+        *reinterpret_cast<uint4*>(ko + src + 64 + 8 * c) = o2;
+      }
+      const float sk = scale127(chunk_amax(rk));
+      const float sv = scale127(chunk_amax(rv));
+      if (ok) {
+        const int64_t row = (int64_t)h * a.cache_rows + sl;
+        chunk_store_int8(rk, sk, (int8_t*)a.k_cache + row * 128, c);
+        chunk_store_int8(rv, sv, (int8_t*)a.v_cache + row * 128, c);
+        if (c == 0) {
+          a.k_scale[row] = sk;
+          a.v_scale[row] = sv;
+        }
+      }
+    }
+    __syncthreads();  // buffer b, the tables and the slots are free again
+    if (threadIdx.x == 0 && g + 2 * gridDim.x < groups) issue(g + 2 * gridDim.x, b);
+  }
+  if (failed && threadIdx.x == 0) {
+    record_error(a.err, DEV_TIMEOUT_APPEND);
+    for (int k = i; k < i + 2; ++k)
+      if (blockIdx.x + (int64_t)k * gridDim.x < groups) append_wait(&full[k & 1], (k >> 1) & 1);
+  }
+}
+
+// Heads the staged kernel takes: its four group buffers then stay within 64 KB.
+constexpr int kStagedMaxHeads = 64;
+
+static size_t staged_smem_bytes(int heads, int G) {
+  return (size_t)4 * G * heads * 256 + (size_t)3 * G * 64 * sizeof(float) + (size_t)G * sizeof(int64_t);
+}
+
 cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s) {
   const InvFreq f = make_inv_freq(a.base, 128);
   if (a.tokens == 0) return cudaSuccess;
+  if (a.heads <= kStagedMaxHeads) {
+    // G tokens per group: 32 rows (one item per thread) where the heads divide
+    // into 32, else whole tokens below that; one token from 32 heads up.  The
+    // group copies start at multiples of 256 bytes of k_new and v_new, whose
+    // 16-byte alignment the C-ABI checks.
+    static int sms[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && sms[dev] == 0) {
+      int n = 0;
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(kv_append_int8_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)staged_smem_bytes(kStagedMaxHeads, 1));
+      if (e != cudaSuccess) return e;
+      sms[dev] = n;
+    }
+    const int G = a.heads >= 32 ? 1 : 32 / a.heads;
+    const int64_t groups = (a.tokens + G - 1) / G;
+    const size_t smem = staged_smem_bytes(a.heads, G);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_append_int8_staged_kernel, 256, smem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && per_sm > 0) {
+      const int64_t grid = std::min<int64_t>(groups, (int64_t)sms[dev] * per_sm);
+      kv_append_int8_staged_kernel<<<(unsigned)grid, 256, smem, s>>>(a, f, G, groups);
+      return cudaGetLastError();
+    }
+  }
   const int64_t blocks = (a.tokens + kAppendTok - 1) / kAppendTok;
   kv_append_int8_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, f);
   return cudaGetLastError();

@@ -62,12 +62,12 @@ ATTN_API const char *attn_last_error(void);
 /* Synchronises the current device, then returns ATTN_OK, or ATTN_ERR_DEVICE if
  * a kernel recorded a fault since the last clear (the code is in the message),
  * or ATTN_ERR_CUDA if the synchronisation itself failed.  clear != 0 resets
- * the recorded code.  Device codes: 0x101-0x104 a pipeline wait ran out of
- * time (TMA producer, MMA issuer, softmax, decode); 0x201 a page id outside
- * [0, num_pages); 0x202 a cache slot outside the cache; 0x203 an INT8 decode
- * operand beyond the fp16 range; 0x204 an FP8 prefill key sequence not starting
- * at a multiple of 16 tokens.  When several faults happen, the first code
- * recorded is kept. */
+ * the recorded code.  Device codes: 0x101-0x105 a pipeline wait ran out of
+ * time (TMA producer, MMA issuer, softmax, decode, INT8 cache append); 0x201 a
+ * page id outside [0, num_pages); 0x202 a cache slot outside the cache; 0x203
+ * an INT8 decode operand beyond the fp16 range; 0x204 an FP8 prefill key
+ * sequence not starting at a multiple of 16 tokens.  When several faults
+ * happen, the first code recorded is kept. */
 ATTN_API int attn_device_status(int clear);
 
 /*

@@ -841,6 +841,81 @@ def test_kv_append_int8_matches_oracle(rotate):
         assert torch.equal(ko[valid], kr[valid])
 
 
+@pytest.mark.parametrize("hkv", [8, 3, 9, 40, 96])
+def test_kv_append_int8_many_groups_matches_oracle(hkv):
+    """A chunk long enough that the append's blocks each take many groups of
+    tokens in turn (so each staging buffer is refilled several times), at head
+    counts whose groups hold 4, 10 and 1 token(s), and at one above what the
+    staged path takes.  The slots are a shuffled set of cache rows, with two
+    padding tokens (-1) and one slot past the cache in the middle. The bad slot
+    is recorded and skipped, and every other row is written as the oracle writes
+    it (keys rotated)."""
+    d = 128
+    tokens = {8: 20011, 3: 40003, 9: 30011, 40: 6007, 96: 2003}[hkv]
+    num_pages = (tokens + 63) // 64 + 2
+    rows = num_pages * 64
+    table, _ = synth.shuffled_page_table([rows], 700 + hkv)
+    slots = (table[0][np.arange(tokens) // 64] * 64 + np.arange(tokens) % 64).astype(np.int32)
+    slots[tokens // 3] = rows          # past the cache
+    slots[[5, tokens - 2]] = -1        # padding
+    pos = np.arange(tokens, dtype=np.int32) + 1000
+    kn = synth.randn((tokens, hkv, d), 710 + hkv, 0.7071)
+    vn = synth.randn((tokens, hkv, d), 720 + hkv, 0.7071)
+    kc0, vc0, ks0, vs0 = _int8_cache(hkv, num_pages, 730 + hkv)
+    kc, vc, ks, vs = kc0.to(DEV), vc0.to(DEV), ks0.to(DEV), vs0.to(DEV)
+    ko = torch.empty(kn.shape, dtype=torch.bfloat16, device=DEV)
+    atc.attn_kv_append_paged_int8(kn.to(DEV), vn.to(DEV), torch.from_numpy(pos).to(DEV),
+                                  torch.from_numpy(slots).to(DEV), kc, vc, ks, vs, k_rot_out=ko, base=10000.0)
+    with pytest.raises(atc.AttnError) as e:
+        atc.attn_device_status(clear=True)
+    assert e.value.status == 6
+    atc.attn_device_status(clear=True)
+    wkc, wvc, wks, wvs, bad = oracle.kv_append_int8(synth.as_f64(kn), synth.as_f64(vn), pos, slots, kc0.numpy(),
+                                                    vc0.numpy(), ks0.numpy(), vs0.numpy(), base=10000.0)
+    assert bad == 1
+    np.testing.assert_array_equal(vc.cpu().numpy(), wvc)
+    np.testing.assert_array_equal(vs.cpu().numpy(), wvs)
+    diff = np.abs(kc.cpu().numpy().astype(np.int32) - wkc.astype(np.int32))
+    assert diff.max() <= 1 and (diff > 0).mean() < 0.01
+    assert np.allclose(ks.cpu().numpy(), wks, rtol=2 ** -7, atol=0)
+    valid = torch.from_numpy((slots >= 0) & (slots < rows)).to(DEV)
+    kr = kn.to(DEV).clone()
+    atc.rope_apply(kr, torch.from_numpy(pos).to(DEV))
+    assert torch.equal(ko[valid], kr[valid])
+
+
+def test_kv_append_int8_row_scales_across_the_bf16_range():
+    """Rows whose max |x| runs over the whole bf16 range (each token's rows
+    scaled by 2^e, e = -133 .. 125, plus an all-zero token), unrotated: every
+    scale is max|x| / 127 rounded in fp32, and every code the fp32 quotient
+    rounded, bit for bit as the oracle decides them -- through both the
+    one-correction division and the full one, for scales and for codes."""
+    hkv, d = 2, 128
+    exps = np.arange(-133, 126)
+    tokens = len(exps) + 1
+    num_pages = (tokens + 63) // 64
+    slots = np.arange(tokens, dtype=np.int32)
+    scale = torch.from_numpy(np.concatenate([np.exp2(exps.astype(np.float64)), [0.0]]).astype(np.float32))
+    kn = (synth.randn((tokens, hkv, d), 760, 1.0).float() * scale[:, None, None]).to(torch.bfloat16)
+    vn = (synth.randn((tokens, hkv, d), 761, 1.0).float() * scale[:, None, None]).to(torch.bfloat16)
+    assert torch.isfinite(kn.float()).all() and torch.isfinite(vn.float()).all()
+    kc0, vc0, ks0, vs0 = _int8_cache(hkv, num_pages, 770)
+    kc, vc, ks, vs = kc0.to(DEV), vc0.to(DEV), ks0.to(DEV), vs0.to(DEV)
+    atc.attn_kv_append_paged_int8(kn.to(DEV), vn.to(DEV), None, torch.from_numpy(slots).to(DEV), kc, vc, ks, vs,
+                                  base=0.0)
+    atc.attn_device_status()
+    wkc, wvc, wks, wvs, bad = oracle.kv_append_int8(synth.as_f64(kn), synth.as_f64(vn), np.zeros(tokens, np.int32),
+                                                    slots, kc0.numpy(), vc0.numpy(), ks0.numpy(), vs0.numpy(),
+                                                    base=0.0)
+    assert bad == 0
+    np.testing.assert_array_equal(kc.cpu().numpy(), wkc)
+    np.testing.assert_array_equal(vc.cpu().numpy(), wvc)
+    np.testing.assert_array_equal(ks.cpu().numpy(), wks)
+    np.testing.assert_array_equal(vs.cpu().numpy(), wvs)
+    assert (wks.reshape(hkv, -1)[:, tokens - 1] == 0).all()
+    assert wks.reshape(hkv, -1)[:, 0].max() < 2.0 ** -90 < wks.reshape(hkv, -1)[:, tokens - 2].min()
+
+
 def test_decode_over_int8_append_matches_oracle():
     """Serving flow on an INT8 cache: the chunk appended (rotated, quantised), then
     the decode of the last position of each request over the whole cache."""
