@@ -166,7 +166,7 @@ int attn_device_status(int clear) {
                        : v == 0x202 ? "cache slot outside the cache"
                        : v == 0x203 ? "INT8 decode value beyond the fp16 range"
                        : v == 0x204 ? "FP8 prefill key sequence not starting at a multiple of 16"
-                       : v == 0x105 ? "INT8 cache append: a staged copy did not land in time"
+                       : v == 0x105 ? "cache append: a staged copy of new rows did not land in time"
                                     : "pipeline wait timed out";
     return fail(ATTN_ERR_DEVICE, "device error 0x%x (%s)", v, what);
   }

@@ -20,7 +20,7 @@ enum DeviceError : unsigned {
   DEV_TIMEOUT_MMA = 0x102,      // MMA issuer waited too long for data or softmax
   DEV_TIMEOUT_SOFTMAX = 0x103,  // softmax waited too long for the tensor core
   DEV_TIMEOUT_DECODE = 0x104,   // decode consumer / producer wait ran out
-  DEV_TIMEOUT_APPEND = 0x105,   // INT8 cache append: a staged copy did not land in time
+  DEV_TIMEOUT_APPEND = 0x105,   // cache append: a staged copy of new rows did not land in time
   DEV_BAD_PAGE = 0x201,         // page-table entry outside [0, num_pages)
   DEV_BAD_SLOT = 0x202,         // cache slot outside [-1, num_pages * page_size)
   DEV_FP16_RANGE = 0x203,       // a value the INT8 decode feeds the fp16 MMAs exceeds 65504

@@ -156,7 +156,9 @@ __global__ void __launch_bounds__(256) rope_kernel(T* __restrict__ x, int64_t to
 // a head's key and value rows with its partner vector of the second half (the
 // key pair rotated), written to the cache rows and optionally the rotated keys
 // to k_rot_out.  Slots are checked per token: -1 skips, out of range is
-// recorded and skipped.
+// recorded and skipped.  kv_append_staged_kernel below does the same per item
+// with the rows staged in shared memory; this kernel serves the shapes whose
+// staged groups would not fit.
 template <int NT>
 __global__ void __launch_bounds__(256, 4) kv_append_kernel(AppendLaunch a, const InvFreq f) {
   constexpr int V = 8;  // bf16 per 16-byte vector
@@ -252,9 +254,9 @@ __global__ void __launch_bounds__(256, 4) kv_append_kernel(AppendLaunch a, const
   }
 }
 
-cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s) {
-  const InvFreq f = make_inv_freq(a.base, a.head_dim);
-  if (a.tokens == 0) return cudaSuccess;
+// kv_append_kernel, for the shapes whose staged groups would not fit in 64 KB
+// of shared memory.
+static cudaError_t launch_kv_append_unstaged(const AppendLaunch& a, const InvFreq& f, cudaStream_t s) {
   // enough rows per block that the angle tables and the block's start-up are
   // amortised: 16 tokens for up to 16 heads, else 4
   if (a.heads <= 16) {
@@ -669,6 +671,167 @@ __global__ void __launch_bounds__(256, 4) kv_append_int8_staged_kernel(AppendLau
     for (int k = i; k < i + 2; ++k)
       if (blockIdx.x + (int64_t)k * gridDim.x < groups) append_wait(&full[k & 1], (k >> 1) & 1);
   }
+}
+
+// kv_append_kernel with the new rows staged through shared memory, as
+// kv_append_int8_staged_kernel stages them: a persistent block walks groups of
+// G whole tokens (contiguous in k_new and v_new), thread 0 keeping the next
+// group's bytes in flight on one of two mbarriers while the block rotates the
+// current group's keys and writes its rows to the cache.  Per item (a key and a
+// value chunk pair) the arithmetic is kv_append_kernel's.  Shared memory: four
+// buffers of G * heads * d * 2 bytes, then cos and sin tables [G][d/2] and the
+// slots [G].
+__global__ void __launch_bounds__(256, 4) kv_append_staged_kernel(AppendLaunch a, const InvFreq f, int G,
+                                                                  int64_t groups) {
+  constexpr int V = 8;  // bf16 per 16-byte vector
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ uint64_t full[2];
+  const int heads = a.heads, d = a.head_dim, half = d / 2, chunks = half / V;
+  const uint32_t rbytes = (uint32_t)d * 2;
+  const uint32_t gbytes = (uint32_t)G * heads * rbytes;  // one group of K (or V)
+  float* cs_s = reinterpret_cast<float*>(dsm + 4 * gbytes);  // [G][half]
+  float* sn_s = cs_s + G * half;
+  int64_t* slot_s = reinterpret_cast<int64_t*>(sn_s + G * half);
+  const char* kn = (const char*)a.k_new;
+  const char* vn = (const char*)a.v_new;
+  __nv_bfloat16* kc = (__nv_bfloat16*)a.k_cache;
+  __nv_bfloat16* vc = (__nv_bfloat16*)a.v_cache;
+  __nv_bfloat16* ko = (__nv_bfloat16*)a.k_rot_out;
+  auto issue = [&](int64_t g, int b) {
+    const int64_t t0 = g * G;
+    const uint32_t bytes = (uint32_t)(min((int64_t)G, a.tokens - t0) * heads * rbytes);
+    mbar_arrive_expect_tx(&full[b], 2 * bytes);
+    bulk_copy_g2s(dsm + (2 * b) * gbytes, kn + t0 * heads * rbytes, bytes, &full[b]);
+    bulk_copy_g2s(dsm + (2 * b + 1) * gbytes, vn + t0 * heads * rbytes, bytes, &full[b]);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    issue(blockIdx.x, 0);
+    if (blockIdx.x + gridDim.x < groups) issue(blockIdx.x + gridDim.x, 1);
+  }
+  const int items = G * heads * chunks;
+  const GridWalk gw0(threadIdx.x, blockDim.x, chunks, heads);
+  const bool rotate = a.base > 0.0;
+  int i = 0;
+  bool failed = false;
+  for (int64_t g = blockIdx.x; g < groups; g += gridDim.x, ++i) {
+    const int b = i & 1;
+    const int64_t t0 = g * G;
+    if (threadIdx.x < G) {
+      const int64_t t = t0 + threadIdx.x;
+      int64_t sl = -1;
+      if (t < a.tokens) {
+        sl = __ldg(a.slots + t);
+        if (sl < -1 || sl >= a.cache_rows) {
+          record_error(a.err, DEV_BAD_SLOT);
+          sl = -1;
+        }
+      }
+      slot_s[threadIdx.x] = sl;
+    }
+    if (rotate)
+      for (int j = threadIdx.x; j < G * half; j += blockDim.x) {
+        const int tt = j / half, ii = j - tt * half;
+        if (t0 + tt < a.tokens) pair_sincos(__ldg(a.positions + t0 + tt), f.turns[ii], sn_s[j], cs_s[j]);
+      }
+    if (!__syncthreads_and(append_wait(&full[b], (i >> 1) & 1))) {
+      failed = true;
+      break;
+    }
+    const uint8_t* kb = dsm + (2 * b) * gbytes;
+    const uint8_t* vb = kb + gbytes;
+    GridWalk gw = gw0;
+    for (int it = threadIdx.x; it < items; it += blockDim.x, gw.next()) {
+      const int c = gw.c, tt = gw.tt, h = gw.h;
+      const int64_t sl = slot_s[tt];
+      if (sl < 0) continue;  // tokens past the end and skipped slots
+      const uint32_t off = (uint32_t)(tt * heads + h) * rbytes + 16u * c;
+      uint4 k1 = *reinterpret_cast<const uint4*>(kb + off);
+      uint4 k2 = *reinterpret_cast<const uint4*>(kb + off + half * 2);
+      const uint4 v1 = *reinterpret_cast<const uint4*>(vb + off);
+      const uint4 v2 = *reinterpret_cast<const uint4*>(vb + off + half * 2);
+      if (rotate) {
+        const __nv_bfloat16* a1 = reinterpret_cast<const __nv_bfloat16*>(&k1);
+        const __nv_bfloat16* a2 = reinterpret_cast<const __nv_bfloat16*>(&k2);
+        uint4 w1, w2;
+        __nv_bfloat16* b1 = reinterpret_cast<__nv_bfloat16*>(&w1);
+        __nv_bfloat16* b2 = reinterpret_cast<__nv_bfloat16*>(&w2);
+        const float* cs = cs_s + tt * half + c * V;
+        const float* sn = sn_s + tt * half + c * V;
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          float y1, y2;
+          rope_rotate(to_f(a1[e]), to_f(a2[e]), cs[e], sn[e], y1, y2);
+          from_f(y1, b1[e]);
+          from_f(y2, b2[e]);
+        }
+        k1 = w1;
+        k2 = w2;
+      }
+      const int64_t dst = ((int64_t)h * a.cache_rows + sl) * d + c * V;
+      *reinterpret_cast<uint4*>(kc + dst) = k1;
+      *reinterpret_cast<uint4*>(kc + dst + half) = k2;
+      *reinterpret_cast<uint4*>(vc + dst) = v1;
+      *reinterpret_cast<uint4*>(vc + dst + half) = v2;
+      if (ko) {
+        const int64_t src = ((t0 + tt) * heads + h) * d + c * V;
+        *reinterpret_cast<uint4*>(ko + src) = k1;
+        *reinterpret_cast<uint4*>(ko + src + half) = k2;
+      }
+    }
+    __syncthreads();  // buffer b, the tables and the slots are free again
+    if (threadIdx.x == 0 && g + 2 * gridDim.x < groups) issue(g + 2 * gridDim.x, b);
+  }
+  if (failed && threadIdx.x == 0) {
+    record_error(a.err, DEV_TIMEOUT_APPEND);
+    for (int k = i; k < i + 2; ++k)
+      if (blockIdx.x + (int64_t)k * gridDim.x < groups) append_wait(&full[k & 1], (k >> 1) & 1);
+  }
+}
+
+// Shared memory of kv_append_staged_kernel for G tokens per group.
+static size_t staged_bf16_smem_bytes(int heads, int d, int G) {
+  return (size_t)4 * G * heads * d * 2 + (size_t)2 * G * (d / 2) * sizeof(float) + (size_t)G * sizeof(int64_t);
+}
+constexpr size_t kStagedMaxSmem = 64 * 1024;
+
+cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s) {
+  const InvFreq f = make_inv_freq(a.base, a.head_dim);
+  if (a.tokens == 0) return cudaSuccess;
+  // G tokens per group: about one item (a key and a value chunk pair) per thread
+  const int per_token = a.heads * (a.head_dim / 16);
+  const int G = std::max(1, 256 / per_token);
+  const size_t smem = staged_bf16_smem_bytes(a.heads, a.head_dim, G);
+  if (smem <= kStagedMaxSmem) {
+    static int sms[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && sms[dev] == 0) {
+      int n = 0;
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(kv_append_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kStagedMaxSmem);
+      if (e != cudaSuccess) return e;
+      sms[dev] = n;
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_append_staged_kernel, 256, smem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && per_sm > 0) {
+      const int64_t groups = (a.tokens + G - 1) / G;
+      const int64_t grid = std::min<int64_t>(groups, (int64_t)sms[dev] * per_sm);
+      kv_append_staged_kernel<<<(unsigned)grid, 256, smem, s>>>(a, f, G, groups);
+      return cudaGetLastError();
+    }
+  }
+  return launch_kv_append_unstaged(a, f, s);
 }
 
 // Heads the staged kernel takes: its four group buffers then stay within 64 KB.

@@ -63,7 +63,7 @@ ATTN_API const char *attn_last_error(void);
  * a kernel recorded a fault since the last clear (the code is in the message),
  * or ATTN_ERR_CUDA if the synchronisation itself failed.  clear != 0 resets
  * the recorded code.  Device codes: 0x101-0x105 a pipeline wait ran out of
- * time (TMA producer, MMA issuer, softmax, decode, INT8 cache append); 0x201 a
+ * time (TMA producer, MMA issuer, softmax, decode, cache append); 0x201 a
  * page id outside [0, num_pages); 0x202 a cache slot outside the cache; 0x203
  * an INT8 decode operand beyond the fp16 range; 0x204 an FP8 prefill key
  * sequence not starting at a multiple of 16 tokens.  When several faults

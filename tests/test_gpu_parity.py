@@ -561,6 +561,57 @@ def test_kv_append_matches_oracle_and_rope_apply():
     assert torch.equal(kc.reshape(hkv, -1, d)[:, rows].permute(1, 0, 2), kr[valid])
 
 
+@pytest.mark.parametrize("hkv,d,tokens", [(8, 128, 20011), (3, 64, 30011), (40, 96, 6007), (1, 16, 70001),
+                                          (64, 256, 2003)])
+def test_kv_append_many_groups_matches_oracle_and_rope_apply(hkv, d, tokens):
+    """A chunk long enough that the append's blocks each take many groups of
+    tokens in turn, over head counts and head dims whose groups hold 4, 21, 1
+    and 256 tokens, and one (64 heads of 256) past what the staged path takes.
+    The slots are a shuffled set of cache rows with two padding tokens (-1) and
+    one slot past the cache. The bad slot is recorded and skipped. Values land
+    bit-exactly, keys bit-identical to rope_apply and within one bf16 ulp of the
+    oracle's rounded rotation, and every other cache row is untouched."""
+    num_pages = (tokens + 63) // 64 + 2
+    rows = num_pages * 64
+    table, _ = synth.shuffled_page_table([rows], 800 + hkv)
+    slots = (table[0][np.arange(tokens) // 64] * 64 + np.arange(tokens) % 64).astype(np.int32)
+    slots[tokens // 3] = rows          # past the cache
+    slots[[5, tokens - 2]] = -1        # padding
+    pos = np.arange(tokens, dtype=np.int32) + 3000
+    kn = synth.randn((tokens, hkv, d), 810 + hkv, 0.7071)
+    vn = synth.randn((tokens, hkv, d), 820 + hkv, 0.7071)
+    kc0 = synth.randn((hkv, num_pages, 64, d), 830 + hkv, 0.7071)
+    vc0 = synth.randn((hkv, num_pages, 64, d), 840 + hkv, 0.7071)
+    kc, vc = kc0.to(DEV), vc0.to(DEV)
+    ko = torch.full((tokens, hkv, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    posd, slotd = torch.from_numpy(pos).to(DEV), torch.from_numpy(slots).to(DEV)
+    atc.attn_kv_append_paged(kn.to(DEV), vn.to(DEV), posd, slotd, kc, vc, k_rot_out=ko)
+    with pytest.raises(atc.AttnError) as e:
+        atc.attn_device_status(clear=True)
+    assert e.value.status == 6
+    atc.attn_device_status(clear=True)
+    wk, wv, bad = oracle.kv_append(synth.as_f64(kn), synth.as_f64(vn), pos, slots, synth.as_f64(kc0),
+                                   synth.as_f64(vc0))
+    assert bad == 1
+    np.testing.assert_array_equal(synth.as_f64(vc.cpu()), wv)
+    got = synth.as_f64(kc.cpu()).reshape(hkv, -1, d)
+    want = wk.reshape(hkv, -1, d)
+    valid_np = (slots >= 0) & (slots < rows)
+    written = np.zeros(got.shape[1], bool)
+    written[slots[valid_np]] = True
+    np.testing.assert_array_equal(got[:, ~written], want[:, ~written])
+    diff = np.abs(got[:, written] - want[:, written])
+    assert (diff <= np.abs(want[:, written]) * 2.0 ** -7 + 2e-6).all()
+    assert (diff > 0).mean() < 0.01
+    kr = kn.to(DEV).clone()
+    atc.rope_apply(kr, posd)
+    valid = torch.from_numpy(valid_np).to(DEV)
+    assert torch.equal(ko[valid], kr[valid])
+    assert torch.isnan(ko[~valid].float()).all()
+    written_rows = torch.from_numpy(slots[valid_np].astype(np.int64)).to(DEV)
+    assert torch.equal(kc.reshape(hkv, -1, d)[:, written_rows].permute(1, 0, 2), kr[valid])
+
+
 def test_kv_append_reports_slot_outside_the_cache():
     """A slot past the cache is not written; the device records it and the host
     reports it.  The other tokens are written (base 0: a plain copy)."""
