@@ -525,7 +525,7 @@ def decode_arm(wl, args, timer, peaks, peak_src, cpu=True):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic("decode_split_paged_b32.md", "decode.cu") if wl.batch == 32 else None,
-                     "traffic_scope": "decode_split_kernel (ncu, scaled from a 4-request capture); merge not included",
+                     "traffic_scope": "decode_split_kernel (ncu, one pass on the full 32-request workload); merge not included",
                      "kernel": "attn::dec::decode_split_kernel + attn::lse_merge_kernel",
                      "kernel_ms": round(ms_kernel, 4), "peak_source": f"{peak_src} HBM copy"},
         "e2e": {"value": round(kv / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
@@ -818,7 +818,7 @@ def decode_int8_arm(wl, args, timer, peaks, peak_src):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic("decode_int8_paged_b32.md", "decode_int8.cu") if wl.batch == 32 else None,
-                     "traffic_scope": "decode_split_int8_kernel (ncu, scaled from a 4-request capture); merge not included",
+                     "traffic_scope": "decode_split_int8_kernel (ncu, one pass on the full 32-request workload); merge not included",
                      "kernel": "attn::dec8::decode_split_int8_kernel + attn::lse_merge_kernel",
                      "kernel_ms": round(ms_kernel, 4), "peak_source": f"{peak_src} HBM copy"},
         "gpu_launches_per_step": 3,
