@@ -133,6 +133,41 @@ def test_rope_strided_token_rows():
     assert np.abs(synth.as_f64(big[:, :H].cpu()) - want).max() <= 2.0 ** -7 * 4
 
 
+@pytest.mark.parametrize("hq,hk,d,dtype", [(64, 8, 128, torch.bfloat16), (5, 1, 64, torch.bfloat16),
+                                           (3, 1, 32, torch.float32), (100, 20, 256, torch.bfloat16)])
+def test_rope_apply_qk_long_equals_strided_calls(hq, hk, d, dtype):
+    """rope_apply_qk on long contiguous Q and K (one launch for both tensors)
+    equals, bit for bit, the same rows rotated one tensor at a time through
+    strided views of wider buffers, and stays within one ulp of the oracle's
+    rounded rotation on sampled tokens; bf16 and fp32, several head counts and
+    head dims."""
+    T = 20011 if hq < 100 else 3001
+    q = synth.randn((T, hq, d), 900 + hq, 0.7071, dtype)
+    k = synth.randn((T, hk, d), 901 + hq, 0.7071, dtype)
+    pos = (np.arange(T, dtype=np.int32) * 3 + 11).astype(np.int32)
+    posd = torch.from_numpy(pos).to(DEV)
+    qd, kd = q.to(DEV), k.to(DEV)
+    atc.rope_apply_qk(qd, kd, posd)
+    # the same rows as strided views of wider buffers: the unstaged kernel
+    qw = torch.zeros((T, hq + 1, d), dtype=dtype, device=DEV)
+    kw = torch.zeros((T, hk + 1, d), dtype=dtype, device=DEV)
+    qw[:, :hq] = q.to(DEV)
+    kw[:, :hk] = k.to(DEV)
+    atc.rope_apply(qw[:, :hq], posd)
+    atc.rope_apply(kw[:, :hk], posd)
+    atc.attn_device_status()
+    assert torch.equal(qd, qw[:, :hq]) and torch.equal(kd, kw[:, :hk])
+    rows = np.unique(np.concatenate([[0, 1, T // 2, T - 1], np.random.default_rng(hq).integers(0, T, 60)]))
+    for x, xd in ((q, qd), (k, kd)):
+        got = synth.as_f64(xd[torch.from_numpy(rows).to(DEV)].cpu())
+        if dtype == torch.bfloat16:
+            want = rotated_bf16(x[torch.from_numpy(rows)], pos[rows])
+            assert (np.abs(got - want) <= np.abs(want) * 2.0 ** -7 + 2e-6).all()
+        else:
+            want = oracle.rope(synth.as_f64(x[torch.from_numpy(rows)]), pos[rows])
+            assert np.abs(got - want).max() < 2e-6
+
+
 # ------------------------------------------------------------------ LSE merge
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
