@@ -27,13 +27,13 @@ Sequence parallelism around the kernels (host code over torch.distributed):
     sp.ring_attention / sp.shard_rows                          ring context parallelism
 """
 from ._binding import (ATTN_BF16, ATTN_FP32, AttnError, attn_decode_paged, attn_decode_paged_int8,
-                       attn_device_status,
+                       attn_device_status, attn_selftest_wait_timeout,
                        attn_kv_append_paged, attn_kv_append_paged_int8, attn_lse_merge, attn_prefill, attn_prefill_fp8,
                        decode_workspace, lib_path, library, prefill, quant_fp8_heads, quant_fp8_rows, rope_apply, rope_apply_qk, rope_quant_fp8_heads,
                        rope_quant_fp8_rows, rope_table)
 from . import sp
 
 __all__ = ["ATTN_BF16", "ATTN_FP32", "AttnError", "attn_decode_paged", "attn_decode_paged_int8", "attn_device_status",
-           "attn_kv_append_paged", "attn_kv_append_paged_int8", "attn_lse_merge", "attn_prefill", "attn_prefill_fp8", "decode_workspace", "lib_path", "library",
+           "attn_selftest_wait_timeout", "attn_kv_append_paged", "attn_kv_append_paged_int8", "attn_lse_merge", "attn_prefill", "attn_prefill_fp8", "decode_workspace", "lib_path", "library",
            "prefill", "quant_fp8_heads", "quant_fp8_rows", "rope_apply", "rope_apply_qk", "rope_quant_fp8_heads",
            "rope_quant_fp8_rows", "rope_table", "sp"]

@@ -40,6 +40,8 @@ def library():
     lib.attn_last_error.restype = C.c_char_p
     lib.attn_device_status.argtypes = [I32]
     lib.attn_device_status.restype = I32
+    lib.attn_selftest_wait_timeout.argtypes = [I32, P]
+    lib.attn_selftest_wait_timeout.restype = I32
     lib.rope_apply.argtypes = [P, I32, I64, I32, I32, I64, P, F64, P]
     lib.rope_apply.restype = I32
     lib.rope_table.argtypes = [P, I64, I32, F64, P, P]
@@ -117,6 +119,13 @@ def _i32(t: Optional[torch.Tensor], name: str) -> Optional[torch.Tensor]:
 def attn_device_status(clear: bool = True) -> None:
     """Synchronise and raise if a kernel recorded a device-side fault."""
     _check(library().attn_device_status(1 if clear else 0))
+
+
+def attn_selftest_wait_timeout(which: int, stream=None) -> None:
+    """Launch the bounded-wait check: a wait on a barrier nothing completes runs
+    out after about 2 s and records its code (which 0: 0x102, 1: 0x105), which
+    the next attn_device_status() raises."""
+    _check(library().attn_selftest_wait_timeout(int(which), _stream(stream)))
 
 
 def rope_apply(x: torch.Tensor, positions: torch.Tensor, base: float = 10000.0, stream=None) -> torch.Tensor:

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "../../include/attn_gb300.h"
+#include "common.cuh"
 #include "kernels.h"
 
 namespace {
@@ -139,11 +140,36 @@ int map_pages_i8(CUtensorMap* m, const void* base, int hkv, int64_t num_pages) {
 
 namespace attn {
 int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+// One block whose thread 0 waits, through the helper `which` selects, on an
+// mbarrier that nothing completes, so the wait runs out after its limit and
+// its code is recorded: 0, mbar_wait (the prefill and decode pipelines'), code
+// DEV_TIMEOUT_MMA; 1, mbar_wait_own (the staged appends'), DEV_TIMEOUT_APPEND.
+__global__ void wait_timeout_selftest_kernel(unsigned* err, int which) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (which == 0)
+    mbar_wait(&bar, 0, err, DEV_TIMEOUT_MMA);
+  else if (!mbar_wait_own(&bar, 0))
+    record_error(err, DEV_TIMEOUT_APPEND);
+}
 }  // namespace attn
 
 extern "C" {
 
 const char* attn_last_error(void) { return g_msg; }
+
+int attn_selftest_wait_timeout(int which, void* stream) {
+  if (which != 0 && which != 1) return fail(ATTN_ERR_ARG, "attn_selftest_wait_timeout: which must be 0 or 1");
+  unsigned* err = nullptr;
+  int rc = device_error_ptr(&err);
+  if (rc) return rc;
+  attn::wait_timeout_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err, which);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_selftest_wait_timeout launch");
+}
 
 int attn_device_status(int clear) {
   unsigned* p = nullptr;

@@ -93,6 +93,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   }
 }
 
+// A wait that ends on the phase or on its own limit (kWaitTimeoutNs) only,
+// whatever other CTAs record: for kernels whose CTAs must carry on past an
+// error another CTA recorded and skipped (a bad cache slot).  Returns false on
+// time-out; the caller records its code.
+__device__ __forceinline__ bool mbar_wait_own(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -517,18 +517,6 @@ __global__ void __launch_bounds__(256, 4) kv_append_int8_kernel(AppendLaunch a, 
   }
 }
 
-// A wait for a staged copy that ends on the phase or on its own time limit
-// only: an error another block records (a bad slot, which is skipped) must not
-// stop the append, as it would through mbar_wait.
-__device__ __forceinline__ bool append_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 1023u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
-  }
-}
-
 // Contiguous global bytes into shared memory (cp.async.bulk), counted on bar.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -616,7 +604,7 @@ __global__ void __launch_bounds__(256, 4) kv_append_int8_staged_kernel(AppendLau
         }
       }
     // one barrier publishes the tables and slots and agrees on the wait
-    if (!__syncthreads_and(append_wait(&full[b], (i >> 1) & 1))) {
+    if (!__syncthreads_and(mbar_wait_own(&full[b], (i >> 1) & 1))) {
       failed = true;
       break;
     }
@@ -669,7 +657,7 @@ __global__ void __launch_bounds__(256, 4) kv_append_int8_staged_kernel(AppendLau
   if (failed && threadIdx.x == 0) {
     record_error(a.err, DEV_TIMEOUT_APPEND);
     for (int k = i; k < i + 2; ++k)
-      if (blockIdx.x + (int64_t)k * gridDim.x < groups) append_wait(&full[k & 1], (k >> 1) & 1);
+      if (blockIdx.x + (int64_t)k * gridDim.x < groups) mbar_wait_own(&full[k & 1], (k >> 1) & 1);
   }
 }
 
@@ -739,7 +727,7 @@ __global__ void __launch_bounds__(256, 4) kv_append_staged_kernel(AppendLaunch a
         const int tt = j / half, ii = j - tt * half;
         if (t0 + tt < a.tokens) pair_sincos(__ldg(a.positions + t0 + tt), f.turns[ii], sn_s[j], cs_s[j]);
       }
-    if (!__syncthreads_and(append_wait(&full[b], (i >> 1) & 1))) {
+    if (!__syncthreads_and(mbar_wait_own(&full[b], (i >> 1) & 1))) {
       failed = true;
       break;
     }
@@ -790,7 +778,7 @@ __global__ void __launch_bounds__(256, 4) kv_append_staged_kernel(AppendLaunch a
   if (failed && threadIdx.x == 0) {
     record_error(a.err, DEV_TIMEOUT_APPEND);
     for (int k = i; k < i + 2; ++k)
-      if (blockIdx.x + (int64_t)k * gridDim.x < groups) append_wait(&full[k & 1], (k >> 1) & 1);
+      if (blockIdx.x + (int64_t)k * gridDim.x < groups) mbar_wait_own(&full[k & 1], (k >> 1) & 1);
   }
 }
 

@@ -70,6 +70,17 @@ ATTN_API const char *attn_last_error(void);
  * happen, the first code recorded is kept. */
 ATTN_API int attn_device_status(int clear);
 
+/* A check of the device-error path that the kernels' bounded waits take, with
+ * no fault: one block waits, through the wait helper `which` selects, on an
+ * mbarrier that nothing completes.  The wait gives up after its limit (2 s)
+ * and records its code: which = 0, the prefill and decode pipelines' wait
+ * (code 0x102); which = 1, the staged cache appends' wait (code 0x105).  The
+ * next attn_device_status() then reports ATTN_ERR_DEVICE with that code, and
+ * the context stays usable.  The pipelines' wait also stops at once when a
+ * code is already recorded (another CTA failed), so clear the status first.
+ * Asynchronous on `stream`; the block runs for about 2 s. */
+ATTN_API int attn_selftest_wait_timeout(int which, void *stream);
+
 /*
  * rope_apply -- rotary position embedding at ABSOLUTE positions, in place.
  *

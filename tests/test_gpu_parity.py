@@ -168,6 +168,26 @@ def test_rope_apply_qk_long_equals_strided_calls(hq, hk, d, dtype):
             assert np.abs(got - want).max() < 2e-6
 
 
+@pytest.mark.parametrize("which,code", [(0, 0x102), (1, 0x105)])
+def test_bounded_wait_runs_out_records_its_code_and_the_context_stays_usable(which, code):
+    """A kernel waits on an mbarrier that nothing completes (no fault, no trap):
+    the wait gives up after its limit, the code is reported by the next status
+    read, and the next call on the same context runs and matches the oracle."""
+    atc.attn_device_status(clear=True)
+    atc.attn_selftest_wait_timeout(which)
+    with pytest.raises(atc.AttnError) as e:
+        atc.attn_device_status(clear=True)
+    assert e.value.status == 6 and f"0x{code:x}" in str(e.value)
+    atc.attn_device_status(clear=True)
+    x = synth.randn((64, 2, 128), 990, 0.7071)
+    pos = np.arange(64, dtype=np.int32)
+    xd = x.to(DEV)
+    atc.rope_apply(xd, torch.from_numpy(pos).to(DEV))
+    atc.attn_device_status()
+    want = rotated_bf16(x, pos)
+    assert (np.abs(synth.as_f64(xd.cpu()) - want) <= np.abs(want) * 2.0 ** -7 + 2e-6).all()
+
+
 # ------------------------------------------------------------------ LSE merge
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
