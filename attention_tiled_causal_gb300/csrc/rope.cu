@@ -527,12 +527,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 
 // kv_append_int8_kernel with the new rows staged through shared memory.  A
 // persistent block walks groups of G whole tokens, whose G * heads key rows
-// (and value rows) are contiguous in k_new (v_new); its thread 0 keeps the
-// next group's bytes in flight (two cp.async.bulk per group into one of two
-// buffers, counted on that buffer's mbarrier) while the block rotates and
-// quantises the current group, so the memory system never waits on the
-// arithmetic.  Per item the arithmetic is kv_append_int8_kernel's, on packed
-// lane pairs where it can be.
+// (and value rows) are contiguous in k_new (v_new).  Its thread 0 copies each
+// group into one of two buffers (two cp.async.bulk, counted on that buffer's
+// mbarrier) as soon as the buffer is free, so while the block rotates and
+// quantises one group the next one is already in flight.  Per item it writes
+// the same bits as kv_append_int8_kernel; the key rotation runs on packed lane
+// pairs (rotate_chunk_packed).
 //
 // Shared memory: four buffers of G * heads * 256 bytes (K and V of buffers 0
 // and 1), then cos, sin and -sin tables [G][64] and the group's slots [G].
