@@ -165,6 +165,8 @@ __global__ void __launch_bounds__(256) lse_merge_d128_kernel(MergeLaunch a) {
   const float* O[R];
   float wgt[R], lse[R];
   bool valid[R];
+  float4 o[R][G];
+  const bool one_group = a.n_parts <= G;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int64_t w = w0 + r;
@@ -174,6 +176,12 @@ __global__ void __launch_bounds__(256) lse_merge_d128_kernel(MergeLaunch a) {
     const uint32_t row = w32 / (uint32_t)a.heads;
     const int h = (int)(w32 - row * (uint32_t)a.heads);
     O[r] = a.part_out + (int64_t)row * a.osr + h * a.osh + i;
+    // with all parts in one group, their rows are requested first: they need
+    // only addresses, so their latency overlaps the LSE loads and the weights
+    if (one_group)
+#pragma unroll
+      for (int k = 0; k < G; ++k)
+        if (valid[r] && k < a.n_parts) o[r][k] = __ldg(reinterpret_cast<const float4*>(O[r] + k * a.osp));
     wgt[r] = (valid[r] && lane < a.n_parts) ? __ldg(a.part_lse + (int64_t)row * a.lsr + h * a.lsh + lane * a.lsp)
                                               : -INFINITY;
   }
@@ -192,12 +200,12 @@ __global__ void __launch_bounds__(256) lse_merge_d128_kernel(MergeLaunch a) {
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int p0 = 0; p0 < a.n_parts; p0 += G) {
-    float4 o[R][G];
+    if (!one_group)
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+      for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int k = 0; k < G; ++k)
-        if (valid[r] && p0 + k < a.n_parts) o[r][k] = __ldg(reinterpret_cast<const float4*>(O[r] + (p0 + k) * a.osp));
+        for (int k = 0; k < G; ++k)
+          if (valid[r] && p0 + k < a.n_parts) o[r][k] = __ldg(reinterpret_cast<const float4*>(O[r] + (p0 + k) * a.osp));
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
