@@ -230,11 +230,86 @@ __global__ void __launch_bounds__(256) lse_merge_d128_kernel(MergeLaunch a) {
   }
 }
 
+// head_dim 128, at most 2 parts: a warp merges 16 (row, head) items.  First
+// lane 2i + k holds part k's LSE of item i; one exchange with the partner lane
+// gives the item's max, sum, LSE and the lane's weight -- the same arithmetic
+// as lse_merge_d128_kernel, done once per 32 lanes instead of once per item.
+// Then the items go two at a time: both parts' 16-byte slices requested
+// first, the weights taken from their lanes by shuffle.
+template <bool OUT_F32>
+__global__ void __launch_bounds__(256) lse_merge_d128_x16_kernel(MergeLaunch a) {
+  constexpr int W = 16;
+  const int64_t items = a.rows * a.heads;
+  const int64_t w0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * W;
+  const int lane = threadIdx.x & 31;
+  if (w0 >= items) return;  // the whole warp
+  // items < 2^31 (checked at launch): 32-bit row / head arithmetic
+  const uint32_t first = (uint32_t)w0;
+  const uint32_t row0 = first / (uint32_t)a.heads;
+  const int h0 = (int)(first - row0 * (uint32_t)a.heads);
+  float wgt, lse;
+  {
+    const int i = lane >> 1, k = lane & 1;
+    const int64_t w = w0 + i;
+    float l = -INFINITY;
+    if (w < items && k < a.n_parts) {
+      const uint32_t row = (uint32_t)w / (uint32_t)a.heads;
+      const int h = (int)((uint32_t)w - row * (uint32_t)a.heads);
+      l = __ldg(a.part_lse + (int64_t)row * a.lsr + h * a.lsh + k * a.lsp);
+    }
+    const float lp = __shfl_xor_sync(0xffffffffu, l, 1);
+    const float mx = fmaxf(l, lp);
+    const float sum = (l == -INFINITY ? 0.f : expf(l - mx)) + (lp == -INFINITY ? 0.f : expf(lp - mx));
+    lse = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
+    wgt = (l == -INFINITY || lse == -INFINITY) ? 0.f : expf(l - lse);
+    if (a.lse_out && k == 0 && w < items) a.lse_out[w] = lse;
+  }
+  const int c = lane * 4;
+  uint32_t row = row0;
+  int h = h0;
+  for (int i = 0; i < W; i += 2) {
+    const float* O[2];
+    bool valid[2];
+    float4 o[2][2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      valid[r] = w0 + i + r < items;
+      O[r] = a.part_out + (int64_t)row * a.osr + h * a.osh + c;
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (valid[r] && k < a.n_parts) o[r][k] = __ldg(reinterpret_cast<const float4*>(O[r] + k * a.osp));
+      if (++h == a.heads) {
+        h = 0;
+        ++row;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, wgt, 2 * (i + r) + k);
+        if (valid[r] && k < a.n_parts && wk != 0.f) fma4(acc, wk, o[r][k]);
+      }
+      if (!valid[r]) continue;
+      const int64_t out_off = (w0 + i + r) * 128 + c;  // (row * heads + h) * 128
+      if (OUT_F32) {
+        *reinterpret_cast<float4*>((float*)a.out + out_off) = acc;
+      } else {
+        uint2 v;
+        v.x = pack_bf16x2(acc.x, acc.y);
+        v.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>((__nv_bfloat16*)a.out + out_off) = v;
+      }
+    }
+  }
+}
+
 template <bool OUT_F32>
 static void launch_d128(const MergeLaunch& a, int64_t items, cudaStream_t s) {
   if (a.n_parts <= 2) {
-    const int64_t warps = (items + 1) / 2;
-    lse_merge_d128_kernel<OUT_F32, 2, 2><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(a);
+    const int64_t warps = (items + 15) / 16;
+    lse_merge_d128_x16_kernel<OUT_F32><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(a);
   } else if (a.n_parts <= 4) {
     const int64_t warps = (items + 1) / 2;
     lse_merge_d128_kernel<OUT_F32, 2, 4><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(a);
