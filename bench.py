@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload all|prefill|decode|long|chunked|fp8|append] [--no-cpu-baseline]
-                    [--decode-requests N]
+                    [--decode-requests N] [--chunked-requests N]
 
 Headline (the JSON `value`): causal GQA prefill, batch 1 x 8192 tokens, 64 query /
 8 KV heads, head_dim 128, bf16 -- one step = RoPE of Q and K at absolute
@@ -748,7 +748,7 @@ def chunked_arm(wl, args, timer, peaks, peak_src, cpu=False):
                         "call over prefix + chunk", "ms": round(ms_f, 4),
                 "value": round(fl / (ms_f * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "frac": round(fl / (ms_f * 1e-3) / 1e12 / peak, 4),
-                "append": hbm_line("attn_kv_append_paged (4 x 8192 tokens, 8 KV heads)", append_bytes, ms_a, peaks,
+                "append": hbm_line(f"attn_kv_append_paged ({wl.batch} x {wl.chunk} tokens, {wl.hkv} KV heads)", append_bytes, ms_a, peaks,
                                    peak_src),
                 "append_int8": hbm_line("attn_kv_append_paged_int8 (the same chunk into an INT8 cache)",
                                         append8_bytes, ms_a8, peaks, peak_src)},
@@ -784,7 +784,7 @@ def append_arm(wl, args, timer, peaks, peak_src):
     atc.attn_device_status()
     append_bytes = 2 * 2 * k_raw.numel() * 2
     append8_bytes = 2 * k_raw.numel() * 2 + 2 * (k_raw.numel() + k_raw.numel() // wl.d * 4)
-    return {"append": hbm_line("attn_kv_append_paged (4 x 8192 tokens, 8 KV heads)", append_bytes, ms_a, peaks,
+    return {"append": hbm_line(f"attn_kv_append_paged ({wl.batch} x {wl.chunk} tokens, {wl.hkv} KV heads)", append_bytes, ms_a, peaks,
                                peak_src),
             "append_int8": hbm_line("attn_kv_append_paged_int8 (the same chunk into an INT8 cache)", append8_bytes,
                                     ms_a8, peaks, peak_src)}
@@ -955,6 +955,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-requests", type=int, default=None,
                     help="decode workload with fewer requests (first N of the seeded 32); for small profiler captures")
+    ap.add_argument("--chunked-requests", type=int, default=None,
+                    help="chunked workload with fewer requests (N of 4, same prefix and chunk lengths); "
+                         "for small profiler captures")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     import synth
@@ -1012,7 +1015,12 @@ def main():
         extra["prefill_64k"] = long_prefill_arm(synth.PREFILL_64K, args, timer, peaks, peak_src, cpu=cpu_leg)
         torch.cuda.empty_cache()
     if args.workload in ("all", "chunked"):
-        extra["chunked"] = chunked_arm(synth.CHUNKED, args, timer, peaks, peak_src, cpu=cpu_leg)
+        cwl = synth.CHUNKED
+        if args.chunked_requests:
+            import dataclasses
+            cwl = dataclasses.replace(cwl, batch=args.chunked_requests,
+                                      name=cwl.name.replace("B4", f"B{args.chunked_requests}"))
+        extra["chunked"] = chunked_arm(cwl, args, timer, peaks, peak_src, cpu=cpu_leg)
         torch.cuda.empty_cache()
     if args.workload == "append":
         extra["append"] = append_arm(synth.CHUNKED, args, timer, peaks, peak_src)

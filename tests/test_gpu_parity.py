@@ -364,6 +364,25 @@ def test_prefill_tc_head_slices_are_bit_identical_to_full_call():
         assert torch.isnan(o[:, :lo].float()).all() and torch.isnan(o[:, hi:].float()).all()
 
 
+def test_prefill_long_sequence_head_slices_are_bit_identical_and_match_oracle():
+    """A 20000-token causal prefill (ragged last tile pair): one-group head
+    slices equal the full call's heads bit for bit, and sampled rows of the
+    full call match the oracle."""
+    lens = [20000]
+    q, k, v, pos, cu = _bf16_case(lens, 64, 8, [0], 311)
+    full_o, full_l = _run_prefill(q, k, v, pos, cu, lens)
+    for lo, hi in ((0, 8), (24, 32), (56, 64)):
+        o, l = _run_prefill(q, k, v, pos, cu, lens, h_lo=lo, h_hi=hi)
+        assert torch.equal(o[:, lo:hi], full_o[:, lo:hi])
+        assert torch.equal(l[:, lo:hi], full_l[:, lo:hi])
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 9999, 19999], synth.sample_rows(20000, 10, 312)]))
+    qr, kr = rotated_bf16(q, pos), rotated_bf16(k, pos)
+    wo, wl = oracle.attention(qr[rows], np.zeros(len(rows), np.int32), pos[rows], kr, synth.as_f64(v),
+                              np.array([0, 20000], np.int32), pos, 128 ** -0.5)
+    check(full_o[torch.from_numpy(rows).to(DEV)], full_l[torch.from_numpy(rows).to(DEV)], wo, wl,
+          what="20000-token prefill")
+
+
 def test_prefill_fully_masked_rows_give_zero_and_minus_inf():
     """Queries at positions 0..9 against keys at positions 50..249: nothing visible."""
     d, hq, hkv = 128, 8, 1
