@@ -782,6 +782,42 @@ __global__ void __launch_bounds__(256, 4) kv_append_staged_kernel(AppendLaunch a
   }
 }
 
+// SMs of device dev, cached per device; 0 if they cannot be read.
+static int device_sms(int dev) {
+  static int sms[64] = {};
+  if (dev < 0 || dev >= 64) return 0;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) sms[dev] = n;
+  }
+  return sms[dev];
+}
+
+// Grid of a persistent staged kernel of 256 threads: its resident blocks for
+// `smem` bytes of dynamic shared memory, at most `groups`; 0 if it does not
+// fit.  The first call on a device raises the kernel's dynamic shared-memory
+// limit to `max_smem` (attr_set: one flag per device, kept by the caller for
+// its kernel).
+static cudaError_t staged_grid(const void* kernel, bool (&attr_set)[64], size_t smem, size_t max_smem,
+                               int64_t groups, int64_t& grid) {
+  grid = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int sms = device_sms(dev);
+  if (sms == 0) return cudaSuccess;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem);
+  if (e != cudaSuccess) return e;
+  grid = std::min<int64_t>(groups, (int64_t)sms * per_sm);
+  return cudaSuccess;
+}
+
 // Shared memory of kv_append_staged_kernel for G tokens per group.
 static size_t staged_bf16_smem_bytes(int heads, int d, int G) {
   return (size_t)4 * G * heads * d * 2 + (size_t)2 * G * (d / 2) * sizeof(float) + (size_t)G * sizeof(int64_t);
@@ -796,25 +832,13 @@ cudaError_t launch_kv_append(const AppendLaunch& a, cudaStream_t s) {
   const int G = std::max(1, 256 / per_token);
   const size_t smem = staged_bf16_smem_bytes(a.heads, a.head_dim, G);
   if (smem <= kStagedMaxSmem) {
-    static int sms[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static bool attr_set[64] = {};
+    const int64_t groups = (a.tokens + G - 1) / G;
+    int64_t grid = 0;
+    const cudaError_t e =
+        staged_grid((const void*)kv_append_staged_kernel, attr_set, smem, kStagedMaxSmem, groups, grid);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && sms[dev] == 0) {
-      int n = 0;
-      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(kv_append_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kStagedMaxSmem);
-      if (e != cudaSuccess) return e;
-      sms[dev] = n;
-    }
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_append_staged_kernel, 256, smem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64 && per_sm > 0) {
-      const int64_t groups = (a.tokens + G - 1) / G;
-      const int64_t grid = std::min<int64_t>(groups, (int64_t)sms[dev] * per_sm);
+    if (grid > 0) {
       kv_append_staged_kernel<<<(unsigned)grid, 256, smem, s>>>(a, f, G, groups);
       return cudaGetLastError();
     }
@@ -837,27 +861,15 @@ cudaError_t launch_kv_append_int8(const AppendLaunch& a, cudaStream_t s) {
     // into 32, else whole tokens below that; one token from 32 heads up.  The
     // group copies start at multiples of 256 bytes of k_new and v_new, whose
     // 16-byte alignment the C-ABI checks.
-    static int sms[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 64 && sms[dev] == 0) {
-      int n = 0;
-      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(kv_append_int8_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)staged_smem_bytes(kStagedMaxHeads, 1));
-      if (e != cudaSuccess) return e;
-      sms[dev] = n;
-    }
+    static bool attr_set[64] = {};
     const int G = a.heads >= 32 ? 1 : 32 / a.heads;
     const int64_t groups = (a.tokens + G - 1) / G;
     const size_t smem = staged_smem_bytes(a.heads, G);
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_append_int8_staged_kernel, 256, smem);
+    int64_t grid = 0;
+    const cudaError_t e = staged_grid((const void*)kv_append_int8_staged_kernel, attr_set, smem,
+                                      staged_smem_bytes(kStagedMaxHeads, 1), groups, grid);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && per_sm > 0) {
-      const int64_t grid = std::min<int64_t>(groups, (int64_t)sms[dev] * per_sm);
+    if (grid > 0) {
       kv_append_int8_staged_kernel<<<(unsigned)grid, 256, smem, s>>>(a, f, G, groups);
       return cudaGetLastError();
     }
