@@ -383,6 +383,56 @@ def test_prefill_long_sequence_head_slices_are_bit_identical_and_match_oracle():
           what="20000-token prefill")
 
 
+def _growing_scores_case(T, seed):
+    """Scores that rise along the keys at a rate set per query head: q_h =
+    noise + a_h u and k_j = noise + (j / 128) u with u all ones, so head h's
+    score grows by about 11.3 a_h (natural units) per 128-key tile.  With a_h =
+    0.15 h, heads 0-3 stay under the kernels' 2^8 rescale threshold and heads
+    4-7 cross it on every tile: each tile moves the row max, O is rescaled in
+    TMEM (bf16) and the e4m3 kernel's lazy check sends the warp back for the
+    row max.  No RoPE (the kernels take the inputs as given)."""
+    hq, hkv, d = 8, 1, 128
+    a = (torch.arange(hq, dtype=torch.float32) * 0.15)[None, :, None]
+    ramp = (torch.arange(T, dtype=torch.float32) / 128.0)[:, None, None]
+    q = (synth.randn((T, hq, d), seed, 0.3).float() + a).to(torch.bfloat16)
+    k = (synth.randn((T, hkv, d), seed + 1, 0.3).float() + ramp).to(torch.bfloat16)
+    v = synth.randn((T, hkv, d), seed + 2, 0.7071)
+    return q, k, v
+
+
+def test_prefill_tc_scores_growing_along_the_keys():
+    """Row maxima that grow on every key tile (O rescaled in TMEM tile after
+    tile) and ones that never cross the threshold, in one call, against the
+    oracle at the bf16 tolerances."""
+    lens = [700]
+    q, k, v = _growing_scores_case(700, 320)
+    pos, cu = synth.positions(lens, [0]), synth.cu_seqlens(lens)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    posd, cud = torch.from_numpy(pos).to(DEV), torch.from_numpy(cu).to(DEV)
+    out, lse = atc.prefill(qd, kd, vd, cud, posd, 700, cu_k=cud, k_pos=posd)
+    atc.attn_device_status()
+    want_o, want_l = oracle.attention(synth.as_f64(q), seq_ids(lens), pos, synth.as_f64(k), synth.as_f64(v), cu, pos,
+                                      128 ** -0.5)
+    assert want_l[-1, 7] - want_l[-1, 0] > 30  # the steep heads' scores are far above the flat ones'
+    check(out, lse, want_o, want_l, what="growing scores")
+
+
+def test_prefill_fp8_scores_growing_along_the_keys():
+    """The same inputs through the e4m3 kernel, against the oracle on the
+    dequantised inputs.  Its steep heads' rows are dominated by a few keys, so
+    the rounding of the largest weights to e4m3 (relative error up to 2^-4)
+    reaches O without averaging: the bound is the worst case, 2^-4 max|v| per
+    element and 2^-4 mean|v| on average; the scores are exact, so the LSE bound
+    stays 1e-3."""
+    lens = [704]
+    q, k, v = _growing_scores_case(704, 330)
+    pos, cu = synth.positions(lens, [0]), synth.cu_seqlens(lens)
+    out, lse = _run_fp8(q, k, v, pos, cu, lens)
+    want_o, want_l, vh = _fp8_oracle(q, k, v, pos, cu, lens)
+    check(out, lse, want_o, want_l, tol_max=_fp8_max_tol(vh), tol_mean=2.0 ** -4 * np.abs(vh).mean(),
+          what="fp8 growing scores")
+
+
 def test_prefill_fully_masked_rows_give_zero_and_minus_inf():
     """Queries at positions 0..9 against keys at positions 50..249: nothing visible."""
     d, hq, hkv = 128, 8, 1
