@@ -809,6 +809,65 @@ def test_chunked_prefill_through_append_is_one_paged_call():
     check(out2, lse2, want_o, want_l, what="two calls + merge")
 
 
+def _growing_decode_case(splits, int8, seed):
+    """Decode inputs whose scores rise along each request's context at a rate
+    set per query head: cached key j (logical, through the shuffled page table)
+    is noise + (j / 64) u and query head h is noise + a_h u (u all ones, a_h =
+    0.15 (h mod 8)), so the heads' scores grow by about 11.3 a_h per 64-token
+    page -- the row max moves page after page in the steep heads and hardly in
+    the flat ones.  The query is used as given (no RoPE)."""
+    ctx = [700, 2049, 130, 1]
+    wl = synth.Decode("decode growing", batch=len(ctx), ctx_lo=0, ctx_hi=0, hq=16, hkv=2, d=128, splits=splits,
+                      seed=seed, ctx_fixed=ctx, int8=int8)
+    inp = wl.make()
+    table = inp["page_table"].numpy()
+    npg = inp["num_pages"]
+    logical = np.full((npg, 64), -1.0)
+    for b, c in enumerate(ctx):
+        j = np.arange(c)
+        logical[table[b, j // 64], j % 64] = j
+    ramp = torch.from_numpy(np.where(logical >= 0, logical / 64.0, 0.0)).float()[None, :, :, None]
+    k = synth.randn((2, npg, 64, 128), seed + 1, 0.3).float() + ramp
+    a = (torch.arange(16) % 8).float()[None, :, None] * 0.15
+    inp["q"] = (synth.randn((len(ctx), 16, 128), seed + 2, 0.3).float() + a).to(torch.bfloat16)
+    if int8:  # symmetric int8 codes of the keys, one fp32 scale per row
+        amax = k.abs().amax(-1)
+        sc = (amax / 127.0).float()
+        inp["k_cache"] = torch.round(k / sc[..., None]).clamp(-127, 127).to(torch.int8)
+        inp["k_scale"] = sc
+    else:
+        inp["k_cache"] = k.to(torch.bfloat16)
+    return wl, inp
+
+
+@pytest.mark.parametrize("int8", [False, True])
+@pytest.mark.parametrize("splits", [1, 16])
+def test_decode_scores_growing_along_the_context(splits, int8):
+    """Split-KV decode with row maxima that move on every page in the steep
+    heads, over a bf16 and an INT8 cache, against the oracle (on the cache's
+    exact values) at the bf16 tolerances; the merge of the splits combines
+    partials whose LSEs differ by hundreds."""
+    wl, inp = _growing_decode_case(splits, int8, 580 + splits + 10 * int8)
+    g = {k: (t.to(DEV) if torch.is_tensor(t) else t) for k, t in inp.items()}
+    po, pl = atc.decode_workspace(wl.batch, wl.hq, splits, wl.d, DEV)
+    out = torch.empty((wl.batch, wl.hq, wl.d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((wl.batch, wl.hq), dtype=torch.float32, device=DEV)
+    if int8:
+        atc.attn_decode_paged_int8(g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"],
+                                   g["ctx_lens"], splits, po, pl, out, lse)
+        kc = oracle.dequant_int8(inp["k_cache"].numpy(), inp["k_scale"].numpy())
+        vc = oracle.dequant_int8(inp["v_cache"].numpy(), inp["v_scale"].numpy())
+    else:
+        atc.attn_decode_paged(g["q"], g["k_cache"], g["v_cache"], g["page_table"], g["ctx_lens"], splits, po, pl,
+                              out, lse)
+        kc, vc = synth.as_f64(inp["k_cache"]), synth.as_f64(inp["v_cache"])
+    atc.attn_device_status()
+    want_o, want_l = oracle.decode_paged(synth.as_f64(inp["q"]), kc, vc, inp["page_table"].numpy(),
+                                         inp["ctx_lens"].numpy(), inp["num_pages"], wl.scale)
+    assert want_l[1, 7] - want_l[1, 0] > 100  # the steep heads' scores are far above the flat ones'
+    check(out, lse, want_o, want_l, what=f"growing decode splits={splits} int8={int8}")
+
+
 # ------------------------------------------------------------------ decode over an INT8 cache
 
 def _decode_int8(wl, inp, splits):
