@@ -383,29 +383,33 @@ def test_prefill_long_sequence_head_slices_are_bit_identical_and_match_oracle():
           what="20000-token prefill")
 
 
-def _growing_scores_case(T, seed):
+def _growing_scores_case(T, seed, sign=1.0):
     """Scores that rise along the keys at a rate set per query head: q_h =
     noise + a_h u and k_j = noise + (j / 128) u with u all ones, so head h's
     score grows by about 11.3 a_h (natural units) per 128-key tile.  With a_h =
     0.15 h, heads 0-3 stay under the kernels' 2^8 rescale threshold and heads
     4-7 cross it on every tile: each tile moves the row max, O is rescaled in
     TMEM (bf16) and the e4m3 kernel's lazy check sends the warp back for the
-    row max.  No RoPE (the kernels take the inputs as given)."""
+    row max.  With sign -1 the scores fall instead: the row max is set on the
+    first tile and later weights underflow towards zero.  No RoPE (the kernels
+    take the inputs as given)."""
     hq, hkv, d = 8, 1, 128
     a = (torch.arange(hq, dtype=torch.float32) * 0.15)[None, :, None]
-    ramp = (torch.arange(T, dtype=torch.float32) / 128.0)[:, None, None]
+    ramp = sign * (torch.arange(T, dtype=torch.float32) / 128.0)[:, None, None]
     q = (synth.randn((T, hq, d), seed, 0.3).float() + a).to(torch.bfloat16)
     k = (synth.randn((T, hkv, d), seed + 1, 0.3).float() + ramp).to(torch.bfloat16)
     v = synth.randn((T, hkv, d), seed + 2, 0.7071)
     return q, k, v
 
 
-def test_prefill_tc_scores_growing_along_the_keys():
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_prefill_tc_scores_growing_along_the_keys(sign):
     """Row maxima that grow on every key tile (O rescaled in TMEM tile after
-    tile) and ones that never cross the threshold, in one call, against the
+    tile) and ones that never cross the threshold, in one call -- or, falling,
+    a max fixed on the first tile and weights that underflow -- against the
     oracle at the bf16 tolerances."""
     lens = [700]
-    q, k, v = _growing_scores_case(700, 320)
+    q, k, v = _growing_scores_case(700, 320, sign)
     pos, cu = synth.positions(lens, [0]), synth.cu_seqlens(lens)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
     posd, cud = torch.from_numpy(pos).to(DEV), torch.from_numpy(cu).to(DEV)
@@ -413,11 +417,13 @@ def test_prefill_tc_scores_growing_along_the_keys():
     atc.attn_device_status()
     want_o, want_l = oracle.attention(synth.as_f64(q), seq_ids(lens), pos, synth.as_f64(k), synth.as_f64(v), cu, pos,
                                       128 ** -0.5)
-    assert want_l[-1, 7] - want_l[-1, 0] > 30  # the steep heads' scores are far above the flat ones'
-    check(out, lse, want_o, want_l, what="growing scores")
+    if sign > 0:
+        assert want_l[-1, 7] - want_l[-1, 0] > 30  # the steep heads' scores are far above the flat ones'
+    check(out, lse, want_o, want_l, what=f"growing scores, sign {sign}")
 
 
-def test_prefill_fp8_scores_growing_along_the_keys():
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_prefill_fp8_scores_growing_along_the_keys(sign):
     """The same inputs through the e4m3 kernel, against the oracle on the
     dequantised inputs.  Its steep heads' rows are dominated by a few keys, so
     the rounding of the largest weights to e4m3 (relative error up to 2^-4)
@@ -425,12 +431,12 @@ def test_prefill_fp8_scores_growing_along_the_keys():
     element and 2^-4 mean|v| on average; the scores are exact, so the LSE bound
     stays 1e-3."""
     lens = [704]
-    q, k, v = _growing_scores_case(704, 330)
+    q, k, v = _growing_scores_case(704, 330, sign)
     pos, cu = synth.positions(lens, [0]), synth.cu_seqlens(lens)
     out, lse = _run_fp8(q, k, v, pos, cu, lens)
     want_o, want_l, vh = _fp8_oracle(q, k, v, pos, cu, lens)
     check(out, lse, want_o, want_l, tol_max=_fp8_max_tol(vh), tol_mean=2.0 ** -4 * np.abs(vh).mean(),
-          what="fp8 growing scores")
+          what=f"fp8 growing scores, sign {sign}")
 
 
 def test_prefill_fully_masked_rows_give_zero_and_minus_inf():
@@ -809,7 +815,7 @@ def test_chunked_prefill_through_append_is_one_paged_call():
     check(out2, lse2, want_o, want_l, what="two calls + merge")
 
 
-def _growing_decode_case(splits, int8, seed):
+def _growing_decode_case(splits, int8, seed, sign=1.0):
     """Decode inputs whose scores rise along each request's context at a rate
     set per query head: cached key j (logical, through the shuffled page table)
     is noise + (j / 64) u and query head h is noise + a_h u (u all ones, a_h =
@@ -826,7 +832,7 @@ def _growing_decode_case(splits, int8, seed):
     for b, c in enumerate(ctx):
         j = np.arange(c)
         logical[table[b, j // 64], j % 64] = j
-    ramp = torch.from_numpy(np.where(logical >= 0, logical / 64.0, 0.0)).float()[None, :, :, None]
+    ramp = sign * torch.from_numpy(np.where(logical >= 0, logical / 64.0, 0.0)).float()[None, :, :, None]
     k = synth.randn((2, npg, 64, 128), seed + 1, 0.3).float() + ramp
     a = (torch.arange(16) % 8).float()[None, :, None] * 0.15
     inp["q"] = (synth.randn((len(ctx), 16, 128), seed + 2, 0.3).float() + a).to(torch.bfloat16)
@@ -840,14 +846,15 @@ def _growing_decode_case(splits, int8, seed):
     return wl, inp
 
 
+@pytest.mark.parametrize("sign", [1.0, -1.0])
 @pytest.mark.parametrize("int8", [False, True])
 @pytest.mark.parametrize("splits", [1, 16])
-def test_decode_scores_growing_along_the_context(splits, int8):
+def test_decode_scores_growing_along_the_context(splits, int8, sign):
     """Split-KV decode with row maxima that move on every page in the steep
     heads, over a bf16 and an INT8 cache, against the oracle (on the cache's
     exact values) at the bf16 tolerances; the merge of the splits combines
     partials whose LSEs differ by hundreds."""
-    wl, inp = _growing_decode_case(splits, int8, 580 + splits + 10 * int8)
+    wl, inp = _growing_decode_case(splits, int8, 580 + splits + 10 * int8, sign)
     g = {k: (t.to(DEV) if torch.is_tensor(t) else t) for k, t in inp.items()}
     po, pl = atc.decode_workspace(wl.batch, wl.hq, splits, wl.d, DEV)
     out = torch.empty((wl.batch, wl.hq, wl.d), dtype=torch.bfloat16, device=DEV)
@@ -864,8 +871,9 @@ def test_decode_scores_growing_along_the_context(splits, int8):
     atc.attn_device_status()
     want_o, want_l = oracle.decode_paged(synth.as_f64(inp["q"]), kc, vc, inp["page_table"].numpy(),
                                          inp["ctx_lens"].numpy(), inp["num_pages"], wl.scale)
-    assert want_l[1, 7] - want_l[1, 0] > 100  # the steep heads' scores are far above the flat ones'
-    check(out, lse, want_o, want_l, what=f"growing decode splits={splits} int8={int8}")
+    if sign > 0:
+        assert want_l[1, 7] - want_l[1, 0] > 100  # the steep heads' scores are far above the flat ones'
+    check(out, lse, want_o, want_l, what=f"growing decode splits={splits} int8={int8} sign={sign}")
 
 
 # ------------------------------------------------------------------ decode over an INT8 cache
