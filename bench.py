@@ -147,7 +147,7 @@ class ClockSampler:
     def summary(self):
         if not self.proc or not os.path.exists(self.path):
             return None
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
@@ -158,14 +158,21 @@ class ClockSampler:
                 mx.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pw.append(0.0)
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         os.unlink(self.path)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+        if max(pw) > 0:  # samples at more than half the window's peak power: the kernels at work
+            busy = [c for c, w in zip(sm, pw) if w > 0.5 * max(pw)]
+            out.update(sm_mhz_under_load=statistics.median(busy), power_w_max=max(pw), samples_under_load=len(busy))
+        return out
 
 
 # ------------------------------------------------------------------ replicas
@@ -579,7 +586,8 @@ def long_prefill_arm(wl, args, timer, peaks, peak_src, cpu=False):
         tf = fl / (ms * 1e-3) / 1e12
         res[f"heads_{lo}_{hi}"] = {"flops": fl, "ms": round(ms, 4), "value": round(tf, 2), "unit": "TFLOP/s",
                                    "frac": round(tf / peak, 4), "peak": peak,
-                                   "peak_source": f"{peak_src} bf16 dense (burst)"}
+                                   "peak_source": f"{peak_src} bf16 dense (burst)",
+                                   "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
     atc.attn_device_status()
     del inp, q, k, v, out
     if sample is not None:
@@ -738,6 +746,7 @@ def chunked_arm(wl, args, timer, peaks, peak_src, cpu=False):
     return {"workload": wl.name + " (paged prefix + causal chunk + LSE merge)", "steps": steps, "warmup": warmup,
             "flops": fl, "ms": round(ms, 4), "value": round(tf, 2), "unit": "TFLOP/s", "frac": round(tf / peak, 4),
             "peak": peak, "peak_source": f"{peak_src} bf16 dense (burst)",
+            "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
             "paged_prefix": {"ms": round(ms_p, 4), "value": round(fl_p / (ms_p * 1e-3) / 1e12, 2),
                              "unit": "TFLOP/s"},
             "causal_chunk": {"ms": round(ms_c, 4), "value": round(fl_c / (ms_c * 1e-3) / 1e12, 2),
@@ -1011,8 +1020,12 @@ def main():
     if args.workload in ("all", "fp8"):
         extra["prefill_fp8"] = fp8_prefill_arm(wl, args, timer, peaks, peak_src, res["inputs"] if res else None)
         torch.cuda.empty_cache()
+    # the long and chunked arms keep the GPU under dense load for seconds: their clocks go on record
+    # beside them (a power-capped clock is what the sustained peak is measured at)
     if args.workload in ("all", "long"):
-        extra["prefill_64k"] = long_prefill_arm(synth.PREFILL_64K, args, timer, peaks, peak_src, cpu=cpu_leg)
+        with ClockSampler(local) as clk_l:
+            extra["prefill_64k"] = long_prefill_arm(synth.PREFILL_64K, args, timer, peaks, peak_src, cpu=cpu_leg)
+        extra["prefill_64k"]["clocks"] = clk_l.summary()
         torch.cuda.empty_cache()
     if args.workload in ("all", "chunked"):
         cwl = synth.CHUNKED
@@ -1020,7 +1033,9 @@ def main():
             import dataclasses
             cwl = dataclasses.replace(cwl, batch=args.chunked_requests,
                                       name=cwl.name.replace("B4", f"B{args.chunked_requests}"))
-        extra["chunked"] = chunked_arm(cwl, args, timer, peaks, peak_src, cpu=cpu_leg)
+        with ClockSampler(local) as clk_c:
+            extra["chunked"] = chunked_arm(cwl, args, timer, peaks, peak_src, cpu=cpu_leg)
+        extra["chunked"]["clocks"] = clk_c.summary()
         torch.cuda.empty_cache()
     if args.workload == "append":
         extra["append"] = append_arm(synth.CHUNKED, args, timer, peaks, peak_src)
